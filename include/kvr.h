@@ -1,0 +1,210 @@
+/*
+ * kvr.h -- C ABI of libkvr: the online hot path of precomputed-KV RAG on one
+ * GPU (GB300, sm_103a).
+ *
+ * A request's prefix is stitched out of token spans [start, end) of per-chunk
+ * KV caches that were computed offline at chunk-local positions; keys are
+ * re-rotated (RoPE) so the spans form one contiguous prefix, values are copied
+ * unchanged; then the request's query tokens run prefill attention over that
+ * prefix, seeing the whole prefix and, causally, each other.
+ *
+ *   CoinRAG blog (liuzhao09.github.io, "CoinRAG: contextualized information
+ *   nugget KV cache reuse"), section 2.2: a retrieval result is a list of
+ *   triples (chunk b_i, start s_i, end e_i);
+ *   section 2.3: C_ctx = C_p (+) Rot(C_b1[s1:e1]; D1) (+) ... (+) Rot(C_bk[sk:ek]; Dk),
+ *   with D_i = |p| + sum_{j<i} len_j, and KV_CoinRAG = C_ctx (+) KV_M(q; C_ctx).
+ *   TurboRAG blog (shibing624), "Attention Mask" and "Position ID": chunks are
+ *   independent, the query attends to every chunk and to itself; positions
+ *   are reordered to be contiguous, RoPE re-applied at the new positions.
+ *   SemPIC page (agihunt.info): on a cache hit, re-rotate the compiled
+ *   document keys at their final positions and interleave the request's own
+ *   inline tokens under a causal mask.
+ *
+ * Conventions shared by every call:
+ *   - Device pointers are CUDA device memory owned by the caller.  The library
+ *     never frees them and keeps none past the call, except the pool pointers
+ *     that a registered pool holds until kvr_pool_unregister.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls enqueue work on it and return without waiting for the GPU, except
+ *     kvr_check, which synchronizes the stream.
+ *   - Every failure is a returned kvr_status; nothing aborts or traps.  Host
+ *     validation runs before any launch, so an error status from validation
+ *     means nothing was enqueued.  kvr_last_error() gives a one-line reason.
+ *   - A pool handle may be used by one host thread at a time.
+ *   - Layouts are row-major, head_dim contiguous; element strides are in
+ *     elements, not bytes.
+ */
+#ifndef KVR_H
+#define KVR_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVR_API __attribute__((visibility("default")))
+#else
+#define KVR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVR_OK = 0,
+    KVR_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, stride or alignment */
+    KVR_ERR_OUT_OF_RANGE = 2,  /* span or offset outside its source / cache    */
+    KVR_ERR_UNSUPPORTED = 3,   /* dtype / head_dim / GPU this build cannot run */
+    KVR_ERR_CUDA = 4,          /* a CUDA runtime call failed                    */
+    KVR_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (kvr_check)   */
+    KVR_ERR_DEVICE_CHECK = 6   /* a kernel flagged bad device-side input        */
+} kvr_status;
+
+enum { KVR_DTYPE_BF16 = 0, KVR_DTYPE_FP32 = 1 };
+
+/* Span source flag: src = KVR_SRC_LOCAL | i names request-local source i
+ * (inline tokens) instead of pool entry src. */
+#define KVR_SRC_LOCAL (1 << 30)
+
+/* kvr_assemble flag: composite positions (every span keeps its chunk-local
+ * ids, no re-rotation) instead of the default reordered contiguous positions.
+ * TurboRAG blog, "Position ID", Figure 5. */
+#define KVR_POSITIONS_COMPOSITE 1u
+
+typedef struct kvr_pool *kvr_pool_t;
+
+/*
+ * Resident pool of precomputed chunk caches C_b (CoinRAG blog section 2.1:
+ * one offline forward pass per full chunk; TurboRAG blog, Figure 3-b).
+ * Entry e, layer l, kv-head h, token t, dim d lives at element
+ *   e*stride[0] + l*stride[1] + h*stride[2] + t*stride[3] + d
+ * of k (and of v).  Keys are RoPE-rotated at their entry-local positions
+ * 0..entry_len-1.  A system-prompt cache C_p is simply another entry.
+ */
+typedef struct {
+    int32_t n_layers;
+    int32_t n_q_heads;    /* query heads; a multiple of n_kv_heads (GQA)        */
+    int32_t n_kv_heads;
+    int32_t head_dim;     /* 64 or 128 (128 for the tensor-core attention path) */
+    int32_t dtype;        /* KVR_DTYPE_BF16 or KVR_DTYPE_FP32                   */
+    int32_t reserved;     /* must be 0                                          */
+    int64_t n_entries;    /* chunks (plus prompt entries) in the pool           */
+    int64_t entry_len;    /* tokens per entry                                   */
+    const void *k;        /* device, caller-owned, valid until unregister       */
+    const void *v;
+    int64_t stride[4];    /* elements: entry, layer, head, token; multiples of 8 */
+    double rope_theta;    /* RoPE base (e.g. 1e6 for Qwen2)                     */
+} kvr_pool_desc;
+
+/* One retrieved span: tokens [start, end) of source src (CoinRAG (b, s, e)). */
+typedef struct {
+    int32_t src;
+    int32_t start;
+    int32_t end;
+} kvr_span;
+
+/* A request-local source (inline tokens, SemPIC): [n_layers, n_kv_heads, len,
+ * head_dim] at the given element strides (layer, head, token), keys rotated
+ * at local positions 0..len-1 exactly like a pool entry.  Device pointers. */
+typedef struct {
+    const void *k;
+    const void *v;
+    int64_t len;
+    int64_t stride[3];
+} kvr_local_src;
+
+/*
+ * kvr_pool_register -- validate a pool layout and create a handle (host only;
+ * no CUDA call).  The first call that enqueues work on the pool binds it to
+ * the then-current device and builds the RoPE cos/sin tables for
+ * (rope_theta, head_dim) there, synchronously (so make that first call
+ * outside any stream capture); these tables, an error word and small staging
+ * buffers are the library's only allocations.
+ * Errors: KVR_ERR_INVALID_ARG (null, negative or unaligned strides, head_dim
+ * odd, n_q_heads % n_kv_heads), KVR_ERR_UNSUPPORTED (dtype, head_dim).
+ * On error *out is left NULL.
+ */
+KVR_API kvr_status kvr_pool_register(const kvr_pool_desc *desc, kvr_pool_t *out);
+
+/* Release a handle and the library's own buffers (synchronizes the device
+ * work the handle enqueued).  NULL is a no-op. */
+KVR_API kvr_status kvr_pool_unregister(kvr_pool_t pool);
+
+/*
+ * kvr_assemble -- gather + re-rotate + stitch (CoinRAG blog section 2.3).
+ *
+ * Request b owns spans[span_offsets[b] .. span_offsets[b+1]) in retrieval
+ * order (a system prompt, if any, is its first span).  Its prefix length is
+ * P_b = sum of its span lengths; span i lands at stitched row
+ * row_i = sum_{j<i} len_j, with position id row_i (reordered) or its source
+ * ids (KVR_POSITIONS_COMPOSITE), and its keys are rotated by
+ * delta_i = position - start (values are copied bit for bit).
+ *
+ * Cache layout (device, caller-owned): request b's block holds
+ * R_b = cache_offsets[b+1] - cache_offsets[b] rows per (layer, kv-head) and
+ * starts at element cache_offsets[b] * n_layers * n_kv_heads * head_dim;
+ * inside it, [n_layers][n_kv_heads][R_b][head_dim].  R_b must be >= P_b;
+ * leave room for the query tokens if kvr_query_attention follows.
+ *
+ *   span_offsets  host [batch+1], non-decreasing, span_offsets[0] = 0
+ *   spans         host [span_offsets[batch]]
+ *   locals        host [n_locals] descriptors of request-local sources
+ *                 (device data), or NULL when n_locals = 0
+ *   cache_offsets host [batch+1] rows, non-decreasing
+ *   pos_ids       device int32 [sum P_b] (request-major, stitched order) or NULL
+ *   src_map       device int32 [sum P_b][2] = (src, source token) or NULL
+ *   prefix_len    host out int32 [batch] = P_b, or NULL
+ *   flags         0 or KVR_POSITIONS_COMPOSITE
+ * Errors: KVR_ERR_INVALID_ARG, KVR_ERR_OUT_OF_RANGE (span outside its source,
+ * unknown source, P_b > R_b, positions >= 2^24), KVR_ERR_CUDA.
+ */
+KVR_API kvr_status kvr_assemble(kvr_pool_t pool, int32_t batch, const int32_t *span_offsets,
+                        const kvr_span *spans, const kvr_local_src *locals, int32_t n_locals,
+                        const int64_t *cache_offsets, void *cache_k, void *cache_v,
+                        int32_t *pos_ids, int32_t *src_map, int32_t *prefix_len,
+                        uint32_t flags, void *stream);
+
+/*
+ * kvr_query_attention -- query prefill over the stitched prefix
+ * (CoinRAG blog section 2.3, KV_M(q; C_ctx); TurboRAG blog "Attention Mask").
+ *
+ * Query token t (0-based) of request b sits at position P_b + t.  The call
+ * rotates its query heads and its key at that position, appends its key and
+ * value at cache row P_b + t of every (layer, kv-head) block, and computes
+ *   O[l, q_offsets[b]+t, h] = sum_j softmax_j(scale * <q, k_j>) v_j
+ * over the P_b prefix rows and query rows 0..t, kv-head = h / (H_q / H_kv).
+ *
+ *   cache_offsets host [batch+1] as in kvr_assemble; need P_b + Lq_b <= R_b
+ *   prefix_len    host [batch] (P_b, e.g. from kvr_assemble)
+ *   q_offsets     host [batch+1]: request b's query tokens are rows
+ *                 q_offsets[b] .. q_offsets[b+1]-1 of the token axis
+ *   q             device [n_layers][T][n_q_heads][head_dim], T = q_offsets[batch],
+ *                 not rotated
+ *   kq, vq        device [n_layers][T][n_kv_heads][head_dim], not rotated
+ *   out           device [n_layers][T][n_q_heads][head_dim], pool dtype
+ *   softmax_scale 0 means 1/sqrt(head_dim)
+ * Errors: KVR_ERR_INVALID_ARG, KVR_ERR_OUT_OF_RANGE, KVR_ERR_UNSUPPORTED,
+ * KVR_ERR_CUDA.  A kernel whose bounded wait ran out records
+ * KVR_ERR_TIMEOUT, reported by kvr_check.
+ */
+KVR_API kvr_status kvr_query_attention(kvr_pool_t pool, int32_t batch, const int64_t *cache_offsets,
+                               const int32_t *prefix_len, const int32_t *q_offsets,
+                               const void *q, const void *kq, const void *vq,
+                               void *cache_k, void *cache_v, void *out,
+                               float softmax_scale, void *stream);
+
+/* Synchronize `stream` and return (then clear) the first error a kernel of
+ * this pool recorded: KVR_OK, KVR_ERR_TIMEOUT, KVR_ERR_DEVICE_CHECK or
+ * KVR_ERR_CUDA. */
+KVR_API kvr_status kvr_check(kvr_pool_t pool, void *stream);
+
+/* Static string naming a status. */
+KVR_API const char *kvr_status_string(kvr_status s);
+
+/* One-line description of the last error raised on this host thread. */
+KVR_API const char *kvr_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVR_H */

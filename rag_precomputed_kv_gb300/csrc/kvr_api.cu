@@ -1,0 +1,616 @@
+// kvr_api.cu -- the C ABI: validation, span tables, staging and launches.
+//
+// Host work per call is bookkeeping only: validate every span against its
+// source and every request against its cache block, lay the span / request
+// tables out (the stitched row of span i is the prefix sum of the lengths
+// before it -- CoinRAG blog section 2.3), copy them to the device with one
+// asynchronous H2D copy from a pinned staging slot, and launch the kernels on
+// the caller's stream.  No call waits for the GPU except kvr_check and
+// pool registration.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kvr_internal.cuh"
+
+using namespace kvr;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvr_status fail(kvr_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+kvr_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(KVR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kSlots = 4;
+
+struct Slot {
+    void *host = nullptr;   // pinned
+    void *dev = nullptr;
+    size_t cap = 0;
+    cudaEvent_t done = nullptr;
+    bool used = false;
+};
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev)
+            cudaSetDevice(dev);
+        else
+            prev = -1;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0)
+            cudaSetDevice(prev);
+    }
+};
+
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+struct kvr_pool {
+    kvr_pool_desc d{};
+    int device = 0;
+    int cc = 0;               // compute capability, major * 10 + minor
+    float2 *rope = nullptr;   // RoPE tables
+    int *err = nullptr;       // device error word
+    Slot slots[kSlots];
+    int next = 0;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    bool ready = false;       // device-side setup done
+
+    int elt() const { return d.dtype == KVR_DTYPE_BF16 ? 2 : 4; }
+    int vec_elems() const { return 16 / elt(); }
+
+    // A staging slot holding at least `bytes`; waits until the slot's last
+    // upload and the kernels that read it are done.
+    kvr_status acquire(size_t bytes, Slot **out)
+    {
+        Slot &s = slots[next];
+        next = (next + 1) % kSlots;
+        cudaError_t e;
+        if (s.used && (e = cudaEventSynchronize(s.done)) != cudaSuccess)
+            return cuda_fail(e, "staging slot wait");
+        if (s.cap < bytes) {
+            size_t cap = std::max<size_t>({bytes, 2 * s.cap, 65536});
+            if (s.host)
+                cudaFreeHost(s.host);
+            if (s.dev)
+                cudaFree(s.dev);
+            s.host = s.dev = nullptr;
+            s.cap = 0;
+            if ((e = cudaMallocHost(&s.host, cap)) != cudaSuccess)
+                return cuda_fail(e, "staging host buffer");
+            if ((e = cudaMalloc(&s.dev, cap)) != cudaSuccess)
+                return cuda_fail(e, "staging device buffer");
+            s.cap = cap;
+        }
+        if (!s.done && (e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "staging event");
+        *out = &s;
+        return KVR_OK;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// registration
+// ---------------------------------------------------------------------------
+extern "C" kvr_status kvr_pool_register(const kvr_pool_desc *desc, kvr_pool_t *out)
+{
+    if (!out)
+        return fail(KVR_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!desc)
+        return fail(KVR_ERR_INVALID_ARG, "desc is NULL");
+    const kvr_pool_desc &d = *desc;
+    if (d.dtype != KVR_DTYPE_BF16 && d.dtype != KVR_DTYPE_FP32)
+        return fail(KVR_ERR_UNSUPPORTED, "dtype %d", d.dtype);
+    if (d.head_dim != 64 && d.head_dim != 128)
+        return fail(KVR_ERR_UNSUPPORTED, "head_dim %d (64 or 128)", d.head_dim);
+    if (d.n_layers < 1 || d.n_kv_heads < 1 || d.n_q_heads < 1 || d.n_q_heads % d.n_kv_heads)
+        return fail(KVR_ERR_INVALID_ARG, "layers %d, q heads %d, kv heads %d", d.n_layers,
+                    d.n_q_heads, d.n_kv_heads);
+    if (d.n_entries < 1 || d.entry_len < 1 || d.entry_len > kMaxPosition)
+        return fail(KVR_ERR_INVALID_ARG, "n_entries %lld, entry_len %lld",
+                    (long long)d.n_entries, (long long)d.entry_len);
+    if (d.reserved != 0)
+        return fail(KVR_ERR_INVALID_ARG, "reserved field must be 0");
+    if (!d.k || !d.v)
+        return fail(KVR_ERR_INVALID_ARG, "pool k / v is NULL");
+    if (!aligned16(d.k) || !aligned16(d.v))
+        return fail(KVR_ERR_INVALID_ARG, "pool k / v not 16-byte aligned");
+    if (!(d.rope_theta > 1.0) || !std::isfinite(d.rope_theta))
+        return fail(KVR_ERR_INVALID_ARG, "rope_theta %g", d.rope_theta);
+    const int vec = 16 / (d.dtype == KVR_DTYPE_BF16 ? 2 : 4);
+    for (int i = 0; i < 4; ++i)
+        if (d.stride[i] < 0 || d.stride[i] % vec)
+            return fail(KVR_ERR_INVALID_ARG, "stride[%d] = %lld must be >= 0 and a multiple of %d",
+                        i, (long long)d.stride[i], vec);
+
+    kvr_pool *p = new kvr_pool();
+    p->d = d;
+    *out = p;
+    return KVR_OK;
+}
+
+// Device-side setup, done by the first call that launches work: the RoPE
+// tables for (rope_theta, head_dim), the error word, the tensor-map encoder.
+static kvr_status ensure_device(kvr_pool *p)
+{
+    if (p->ready)
+        return KVR_OK;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&p->device)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    int maj = 0, min = 0;
+    cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, p->device);
+    cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, p->device);
+    p->cc = maj * 10 + min;
+    const size_t tab = sizeof(float2) * 2 * kRopeSplit * (p->d.head_dim / 2);
+    if ((e = cudaMalloc(&p->rope, tab)) != cudaSuccess ||
+        (e = cudaMalloc(&p->err, sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(p->err, 0, sizeof(int))) != cudaSuccess ||
+        (e = launch_rope_tables(p->rope, p->d.head_dim, p->d.rope_theta, 0)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(0)) != cudaSuccess)
+        return cuda_fail(e, "pool device setup");
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        p->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    p->ready = true;
+    return KVR_OK;
+}
+
+extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
+{
+    if (!p)
+        return KVR_OK;
+    if (!p->ready) {  // device setup never completed: free what it got
+        if (p->rope)
+            cudaFree(p->rope);
+        if (p->err)
+            cudaFree(p->err);
+        delete p;
+        return KVR_OK;
+    }
+    DeviceGuard g(p->device);
+    for (Slot &s : p->slots) {
+        if (s.done) {
+            cudaEventSynchronize(s.done);
+            cudaEventDestroy(s.done);
+        }
+        if (s.host)
+            cudaFreeHost(s.host);
+        if (s.dev)
+            cudaFree(s.dev);
+    }
+    if (p->rope)
+        cudaFree(p->rope);
+    if (p->err)
+        cudaFree(p->err);
+    delete p;
+    return KVR_OK;
+}
+
+// ---------------------------------------------------------------------------
+// assemble
+// ---------------------------------------------------------------------------
+namespace {
+
+kvr_status check_offsets32(const int32_t *o, int32_t batch, const char *name)
+{
+    if (!o)
+        return fail(KVR_ERR_INVALID_ARG, "%s is NULL", name);
+    if (o[0] != 0)
+        return fail(KVR_ERR_INVALID_ARG, "%s[0] = %d, must be 0", name, o[0]);
+    for (int b = 0; b < batch; ++b)
+        if (o[b + 1] < o[b])
+            return fail(KVR_ERR_INVALID_ARG, "%s decreases at %d", name, b);
+    return KVR_OK;
+}
+
+kvr_status check_cache_offsets(const int64_t *o, int32_t batch)
+{
+    if (!o)
+        return fail(KVR_ERR_INVALID_ARG, "cache_offsets is NULL");
+    if (o[0] < 0)
+        return fail(KVR_ERR_INVALID_ARG, "cache_offsets[0] < 0");
+    for (int b = 0; b < batch; ++b)
+        if (o[b + 1] < o[b] || o[b + 1] - o[b] > kMaxPosition)
+            return fail(KVR_ERR_INVALID_ARG, "cache_offsets[%d..%d] invalid", b, b + 1);
+    return KVR_OK;
+}
+
+kvr_status check_local(const kvr_pool &p, const kvr_local_src &lc, int i)
+{
+    if (!lc.k || !lc.v || !aligned16(lc.k) || !aligned16(lc.v))
+        return fail(KVR_ERR_INVALID_ARG, "local source %d: k / v NULL or not 16-byte aligned", i);
+    if (lc.len < 0 || lc.len > kMaxPosition)
+        return fail(KVR_ERR_INVALID_ARG, "local source %d: len %lld", i, (long long)lc.len);
+    for (int s = 0; s < 3; ++s)
+        if (lc.stride[s] < 0 || lc.stride[s] % p.vec_elems())
+            return fail(KVR_ERR_INVALID_ARG, "local source %d: stride[%d] = %lld", i, s,
+                        (long long)lc.stride[s]);
+    return KVR_OK;
+}
+
+// Units of (layer, kv-head) per assemble CTA: about 256 rows per CTA.
+int units_per_cta(int LH, int64_t rows, int64_t n_spans)
+{
+    const int64_t avg = std::max<int64_t>(1, rows / std::max<int64_t>(1, n_spans));
+    return (int)std::min<int64_t>(LH, std::max<int64_t>(1, 256 / avg));
+}
+
+}  // namespace
+
+extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *span_offsets,
+                                   const kvr_span *spans, const kvr_local_src *locals,
+                                   int32_t n_locals, const int64_t *cache_offsets, void *cache_k,
+                                   void *cache_v, int32_t *pos_ids, int32_t *src_map,
+                                   int32_t *prefix_len, uint32_t flags, void *stream)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    if (batch < 0)
+        return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
+    if (batch == 0)
+        return KVR_OK;
+    if (flags & ~KVR_POSITIONS_COMPOSITE)
+        return fail(KVR_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    kvr_status st;
+    if ((st = check_offsets32(span_offsets, batch, "span_offsets")) != KVR_OK ||
+        (st = check_cache_offsets(cache_offsets, batch)) != KVR_OK)
+        return st;
+    const int32_t n_spans = span_offsets[batch];
+    if (n_spans > 0 && !spans)
+        return fail(KVR_ERR_INVALID_ARG, "spans is NULL");
+    if (n_locals < 0 || (n_locals > 0 && !locals))
+        return fail(KVR_ERR_INVALID_ARG, "locals NULL with n_locals %d", n_locals);
+    for (int i = 0; i < n_locals; ++i)
+        if ((st = check_local(*p, locals[i], i)) != KVR_OK)
+            return st;
+    const bool composite = flags & KVR_POSITIONS_COMPOSITE;
+    const int LH = p->d.n_layers * p->d.n_kv_heads;
+
+    std::vector<DevSpan> ds;
+    ds.reserve(n_spans);
+    std::vector<int32_t> plen(batch);
+    int64_t flat = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
+        int64_t row = 0;
+        for (int i = span_offsets[b]; i < span_offsets[b + 1]; ++i) {
+            const kvr_span s = spans[i];
+            int64_t src_len;
+            if (s.src < 0)
+                return fail(KVR_ERR_OUT_OF_RANGE, "span %d: negative source id %d", i, s.src);
+            if (s.src & KVR_SRC_LOCAL) {
+                const int idx = s.src & ~KVR_SRC_LOCAL;
+                if (idx >= n_locals)
+                    return fail(KVR_ERR_OUT_OF_RANGE, "span %d: local source %d of %d", i, idx,
+                                n_locals);
+                src_len = locals[idx].len;
+            } else {
+                if (s.src >= p->d.n_entries)
+                    return fail(KVR_ERR_OUT_OF_RANGE, "span %d: pool entry %d of %lld", i, s.src,
+                                (long long)p->d.n_entries);
+                src_len = p->d.entry_len;
+            }
+            if (s.start < 0 || s.end < s.start || s.end > src_len)
+                return fail(KVR_ERR_OUT_OF_RANGE, "span %d: [%d, %d) outside source of %lld tokens",
+                            i, s.start, s.end, (long long)src_len);
+            const int32_t len = s.end - s.start;
+            const int64_t pos0 = composite ? s.start : row;
+            if (pos0 + len > kMaxPosition)
+                return fail(KVR_ERR_OUT_OF_RANGE, "span %d: positions beyond 2^24", i);
+            if (len > 0) {
+                DevSpan d{};
+                d.dst_row0 = cache_offsets[b] * LH;
+                d.flat0 = flat;
+                d.src = s.src;
+                d.start = s.start;
+                d.len = len;
+                d.row = (int32_t)row;
+                d.pos0 = (int32_t)pos0;
+                d.delta = (int32_t)(pos0 - s.start);
+                d.cap = (int32_t)cap;
+                d.dstep = 0;
+                ds.push_back(d);
+            }
+            row += len;
+            flat += len;
+        }
+        if (row > cap)
+            return fail(KVR_ERR_OUT_OF_RANGE, "request %d: prefix %lld rows > cache block %lld", b,
+                        (long long)row, (long long)cap);
+        plen[b] = (int32_t)row;
+    }
+    if (prefix_len)
+        std::copy(plen.begin(), plen.end(), prefix_len);
+    if (ds.empty())
+        return KVR_OK;
+    if (!cache_k || !cache_v || !aligned16(cache_k) || !aligned16(cache_v))
+        return fail(KVR_ERR_INVALID_ARG, "cache_k / cache_v NULL or not 16-byte aligned");
+    if ((st = ensure_device(p)) != KVR_OK)
+        return st;
+
+    DeviceGuard g(p->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t off_loc = align16(ds.size() * sizeof(DevSpan));
+    const size_t bytes = off_loc + sizeof(DevLocal) * std::max(n_locals, 0);
+    Slot *slot;
+    if ((st = p->acquire(bytes, &slot)) != KVR_OK)
+        return st;
+    char *h = static_cast<char *>(slot->host);
+    std::memcpy(h, ds.data(), ds.size() * sizeof(DevSpan));
+    for (int i = 0; i < n_locals; ++i) {
+        DevLocal l{locals[i].k, locals[i].v, locals[i].stride[0], locals[i].stride[1],
+                   locals[i].stride[2], locals[i].len};
+        std::memcpy(h + off_loc + i * sizeof(DevLocal), &l, sizeof l);
+    }
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(slot->dev, h, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "span table upload");
+    AssembleArgs a{};
+    a.spans = static_cast<const DevSpan *>(slot->dev);
+    a.locals = reinterpret_cast<const DevLocal *>(static_cast<char *>(slot->dev) + off_loc);
+    a.rope = p->rope;
+    a.pool_k = p->d.k;
+    a.pool_v = p->d.v;
+    a.ps_entry = p->d.stride[0];
+    a.ps_layer = p->d.stride[1];
+    a.ps_head = p->d.stride[2];
+    a.ps_tok = p->d.stride[3];
+    a.cache_k = cache_k;
+    a.cache_v = cache_v;
+    a.pos_ids = pos_ids;
+    a.src_map = src_map;
+    a.n_layers = p->d.n_layers;
+    a.n_heads = p->d.n_kv_heads;
+    a.upc = units_per_cta(LH, flat, (int64_t)ds.size());
+    e = launch_assemble(a, p->d.dtype, p->d.head_dim, (int)ds.size(), s);
+    cudaEventRecord(slot->done, s);
+    slot->used = true;
+    if (e != cudaSuccess)
+        return cuda_fail(e, "assemble launch");
+    return KVR_OK;
+}
+
+// ---------------------------------------------------------------------------
+// query attention
+// ---------------------------------------------------------------------------
+namespace {
+
+kvr_status encode_cache_map(const kvr_pool &p, void *base, int64_t rows, CUtensorMap *m)
+{
+    if (!p.encode)
+        return fail(KVR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled not available");
+    const cuuint64_t dims[2] = {(cuuint64_t)p.d.head_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.d.head_dim * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = p.encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return KVR_OK;
+}
+
+}  // namespace
+
+extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int64_t *cache_offsets,
+                                          const int32_t *prefix_len, const int32_t *q_offsets,
+                                          const void *q, const void *kq, const void *vq,
+                                          void *cache_k, void *cache_v, void *out,
+                                          float softmax_scale, void *stream)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    if (batch < 0)
+        return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
+    if (batch == 0)
+        return KVR_OK;
+    kvr_status st;
+    if ((st = check_cache_offsets(cache_offsets, batch)) != KVR_OK ||
+        (st = check_offsets32(q_offsets, batch, "q_offsets")) != KVR_OK)
+        return st;
+    if (!prefix_len)
+        return fail(KVR_ERR_INVALID_ARG, "prefix_len is NULL");
+    if (!(softmax_scale >= 0.f) || !std::isfinite(softmax_scale))
+        return fail(KVR_ERR_INVALID_ARG, "softmax_scale %g", (double)softmax_scale);
+    const int32_t T = q_offsets[batch];
+    if (T == 0)
+        return KVR_OK;
+    const void *ptrs[] = {q, kq, vq, cache_k, cache_v, out};
+    for (const void *x : ptrs)
+        if (!x || !aligned16(x))
+            return fail(KVR_ERR_INVALID_ARG, "q / kq / vq / cache / out NULL or not 16-byte aligned");
+
+    const int L = p->d.n_layers, Hkv = p->d.n_kv_heads, Hq = p->d.n_q_heads, D = p->d.head_dim;
+    const int LH = L * Hkv;
+    const int G = Hq / Hkv;
+    std::vector<DevReq> rq(batch);
+    std::vector<DevSpan> ap;
+    std::vector<DevLocal> al;
+    int32_t m_tiles = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
+        const int32_t P = prefix_len[b];
+        const int32_t Lq = q_offsets[b + 1] - q_offsets[b];
+        if (P < 0 || (int64_t)P + Lq > cap)
+            return fail(KVR_ERR_OUT_OF_RANGE, "request %d: prefix %d + query %d > cache block %lld",
+                        b, P, Lq, (long long)cap);
+    }
+    if ((st = ensure_device(p)) != KVR_OK)
+        return st;
+    const bool tc = attention_tc_supported(p->d.dtype, D) && p->cc == 103 && p->encode;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
+        const int32_t P = prefix_len[b];
+        const int32_t Lq = q_offsets[b + 1] - q_offsets[b];
+        DevReq &r = rq[b];
+        r.cache_row0 = cache_offsets[b] * LH;
+        r.cap = (int32_t)cap;
+        r.prefix = P;
+        r.q_off = q_offsets[b];
+        r.q_len = Lq;
+        r.m_tile0 = m_tiles;
+        m_tiles += (int32_t)((int64_t(G) * Lq + 127) / 128);
+        if (Lq > 0) {
+            // the query tokens' keys / values become cache rows P..P+Lq-1;
+            // their keys arrive un-rotated, so token t turns by P + t
+            DevSpan d{};
+            d.dst_row0 = r.cache_row0;
+            d.flat0 = 0;
+            d.src = KVR_SRC_LOCAL | (int32_t)al.size();
+            d.start = 0;
+            d.len = Lq;
+            d.row = P;
+            d.pos0 = P;
+            d.delta = P;
+            d.cap = (int32_t)cap;
+            d.dstep = 1;
+            ap.push_back(d);
+            const int64_t off = (int64_t)q_offsets[b] * Hkv * D * p->elt();
+            DevLocal l{static_cast<const char *>(kq) + off, static_cast<const char *>(vq) + off,
+                       (int64_t)T * Hkv * D, D, (int64_t)Hkv * D, Lq};
+            al.push_back(l);
+        }
+    }
+
+    DeviceGuard g(p->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t off_sp = align16(rq.size() * sizeof(DevReq));
+    const size_t off_lc = off_sp + align16(ap.size() * sizeof(DevSpan));
+    const size_t bytes = off_lc + al.size() * sizeof(DevLocal);
+    Slot *slot;
+    if ((st = p->acquire(bytes, &slot)) != KVR_OK)
+        return st;
+    char *h = static_cast<char *>(slot->host);
+    std::memcpy(h, rq.data(), rq.size() * sizeof(DevReq));
+    std::memcpy(h + off_sp, ap.data(), ap.size() * sizeof(DevSpan));
+    std::memcpy(h + off_lc, al.data(), al.size() * sizeof(DevLocal));
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(slot->dev, h, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "request table upload");
+    char *dv = static_cast<char *>(slot->dev);
+
+    AssembleArgs a{};
+    a.spans = reinterpret_cast<const DevSpan *>(dv + off_sp);
+    a.locals = reinterpret_cast<const DevLocal *>(dv + off_lc);
+    a.rope = p->rope;
+    a.cache_k = cache_k;
+    a.cache_v = cache_v;
+    a.n_layers = L;
+    a.n_heads = Hkv;
+    a.upc = units_per_cta(LH, (int64_t)T, (int64_t)ap.size());
+    e = launch_assemble(a, p->d.dtype, D, (int)ap.size(), s);
+
+    AttnArgs at{};
+    at.reqs = reinterpret_cast<const DevReq *>(dv);
+    at.n_reqs = batch;
+    at.rope = p->rope;
+    at.q = q;
+    at.cache_k = cache_k;
+    at.cache_v = cache_v;
+    at.out = out;
+    at.n_layers = L;
+    at.n_q_heads = Hq;
+    at.n_kv_heads = Hkv;
+    at.total_q = T;
+    at.scale_log2 = (softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt((float)D)) *
+                    1.4426950408889634f;
+    at.err = p->err;
+    if (e == cudaSuccess) {
+        if (tc) {
+            CUtensorMap mk, mv;
+            const int64_t rows = cache_offsets[batch] * LH;
+            if ((st = encode_cache_map(*p, cache_k, rows, &mk)) != KVR_OK ||
+                (st = encode_cache_map(*p, cache_v, rows, &mv)) != KVR_OK) {
+                cudaEventRecord(slot->done, s);
+                slot->used = true;
+                return st;
+            }
+            TcAttnArgs ta{at, &mk, &mv, m_tiles};
+            e = launch_attention_tc(ta, s);
+        } else {
+            e = launch_attention_simt(at, p->d.dtype, D, s);
+        }
+    }
+    cudaEventRecord(slot->done, s);
+    slot->used = true;
+    if (e != cudaSuccess)
+        return cuda_fail(e, "attention launch");
+    return KVR_OK;
+}
+
+// ---------------------------------------------------------------------------
+// status
+// ---------------------------------------------------------------------------
+extern "C" kvr_status kvr_check(kvr_pool_t p, void *stream)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    kvr_status st;
+    if ((st = ensure_device(p)) != KVR_OK)
+        return st;
+    DeviceGuard g(p->device);
+    cudaError_t e;
+    if ((e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return cuda_fail(e, "stream synchronize");
+    int w = 0;
+    if ((e = cudaMemcpy(&w, p->err, sizeof w, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "error word read");
+    if (w == kDevOk)
+        return KVR_OK;
+    cudaMemset(p->err, 0, sizeof(int));
+    if (w == kDevTimeout)
+        return fail(KVR_ERR_TIMEOUT, "a kernel's bounded wait ran out");
+    return fail(KVR_ERR_DEVICE_CHECK, "a kernel flagged device-side input (code %d)", w);
+}
+
+extern "C" const char *kvr_status_string(kvr_status s)
+{
+    switch (s) {
+    case KVR_OK: return "KVR_OK";
+    case KVR_ERR_INVALID_ARG: return "KVR_ERR_INVALID_ARG";
+    case KVR_ERR_OUT_OF_RANGE: return "KVR_ERR_OUT_OF_RANGE";
+    case KVR_ERR_UNSUPPORTED: return "KVR_ERR_UNSUPPORTED";
+    case KVR_ERR_CUDA: return "KVR_ERR_CUDA";
+    case KVR_ERR_TIMEOUT: return "KVR_ERR_TIMEOUT";
+    case KVR_ERR_DEVICE_CHECK: return "KVR_ERR_DEVICE_CHECK";
+    }
+    return "KVR_ERR_UNKNOWN";
+}
+
+extern "C" const char *kvr_last_error(void) { return g_last_error.c_str(); }

@@ -1,0 +1,232 @@
+// kvr_assemble.cu -- RoPE tables and the fused span-gather + RoPE re-rotation
+// + stitch kernel.
+//
+// CoinRAG blog section 2.3: C_ctx = C_p (+) Rot(C_b1[s1:e1]; D1) (+) ...: each
+// retrieved span is sliced out of its chunk's precomputed cache, its keys are
+// turned to the span's new positions, values are carried over unchanged.
+// TurboRAG blog, "Position ID": re-apply RoPE at the reordered positions.
+// SemPIC page: the same re-rotation places compiled documents and request-side
+// inline tokens at their final logical positions.
+//
+// The kernel is a pure HBM stream: every stitched (token, layer, kv-head) row
+// is read once from the pool and written once into the request's cache.  A
+// CTA owns one span and a group of (layer, kv-head) units; inside a unit the
+// span's rows are contiguous both in the pool and in the cache, so each warp
+// issues 16-byte loads/stores over whole 128-byte lines.
+#include <cuda_bf16.h>
+
+#include "kvr_internal.cuh"
+
+namespace kvr {
+
+// ---------------------------------------------------------------------------
+// RoPE tables (built once per pool registration)
+// ---------------------------------------------------------------------------
+__global__ void k_rope_tables(float2 *tab, int half, double theta, int head_dim)
+{
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= 2 * kRopeSplit * half)
+        return;
+    const int i = idx % half;
+    const int n = (idx / half) % kRopeSplit;
+    const bool hi = idx < kRopeSplit * half;
+    const double w = pow(theta, -2.0 * (double)i / (double)head_dim);
+    const double ang = (hi ? (double)n * (double)kRopeSplit : (double)n) * w;
+    double s, c;
+    sincos(ang, &s, &c);
+    tab[idx] = make_float2((float)c, (float)s);
+}
+
+cudaError_t launch_rope_tables(float2 *tab, int head_dim, double theta, cudaStream_t s)
+{
+    const int half = head_dim / 2;
+    const int n = 2 * kRopeSplit * half;
+    k_rope_tables<<<(n + 255) / 256, 256, 0, s>>>(tab, half, theta, head_dim);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of E elements, rotation of a (lo, hi) pair of vectors
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Vec;
+
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int E = 8;
+    __device__ static void rotate(uint4 &lo, uint4 &hi, const float *c, const float *s)
+    {
+        uint32_t *pl = reinterpret_cast<uint32_t *>(&lo);
+        uint32_t *ph = reinterpret_cast<uint32_t *>(&hi);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&pl[w]));
+            const float2 y = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&ph[w]));
+            const float c0 = c[2 * w], s0 = s[2 * w], c1 = c[2 * w + 1], s1 = s[2 * w + 1];
+            __nv_bfloat162 xo = __floats2bfloat162_rn(fmaf(x.x, c0, -y.x * s0), fmaf(x.y, c1, -y.y * s1));
+            __nv_bfloat162 yo = __floats2bfloat162_rn(fmaf(x.x, s0, y.x * c0), fmaf(x.y, s1, y.y * c1));
+            pl[w] = *reinterpret_cast<uint32_t *>(&xo);
+            ph[w] = *reinterpret_cast<uint32_t *>(&yo);
+        }
+    }
+};
+
+template <>
+struct Vec<float> {
+    static constexpr int E = 4;
+    __device__ static void rotate(uint4 &lo, uint4 &hi, const float *c, const float *s)
+    {
+        float *x = reinterpret_cast<float *>(&lo);
+        float *y = reinterpret_cast<float *>(&hi);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float xo = fmaf(x[e], c[e], -y[e] * s[e]);
+            const float yo = fmaf(x[e], s[e], y[e] * c[e]);
+            x[e] = xo;
+            y[e] = yo;
+        }
+    }
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_vec(void *p, const uint4 &v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+constexpr int kAssembleThreads = 256;
+
+// One CTA = one span x a group of `upc` (layer, kv-head) units.  A row of the
+// span is handled by TPR threads; thread j of a row owns elements
+// [j*E, j*E+E) and their RoPE partners [D/2 + j*E, D/2 + j*E + E).
+template <typename T, int D>
+__global__ void __launch_bounds__(kAssembleThreads) k_assemble(const AssembleArgs a)
+{
+    constexpr int H2 = D / 2;
+    constexpr int E = Vec<T>::E;
+    constexpr int TPR = H2 / E;                   // threads per row
+    constexpr int RPP = kAssembleThreads / TPR;   // rows per pass
+    static_assert(H2 % E == 0 && kAssembleThreads % TPR == 0, "head_dim");
+
+    const DevSpan sp = a.spans[blockIdx.x];
+    const int j = threadIdx.x % TPR;
+
+    // this thread's E (cos, sin) pairs for the span's rotation
+    float c[E], s[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float2 cs = rope_cs(a.rope, H2, sp.delta, j * E + e);
+        c[e] = cs.x;
+        s[e] = cs.y;
+    }
+
+    const T *kb, *vb;
+    int64_t sl, sh, st;
+    if (sp.src & KVR_SRC_LOCAL) {
+        const DevLocal lc = a.locals[sp.src & ~KVR_SRC_LOCAL];
+        kb = static_cast<const T *>(lc.k);
+        vb = static_cast<const T *>(lc.v);
+        sl = lc.s_layer;
+        sh = lc.s_head;
+        st = lc.s_tok;
+    } else {
+        kb = static_cast<const T *>(a.pool_k) + (int64_t)sp.src * a.ps_entry;
+        vb = static_cast<const T *>(a.pool_v) + (int64_t)sp.src * a.ps_entry;
+        sl = a.ps_layer;
+        sh = a.ps_head;
+        st = a.ps_tok;
+    }
+    T *ck = static_cast<T *>(a.cache_k);
+    T *cv = static_cast<T *>(a.cache_v);
+
+    const int LH = a.n_layers * a.n_heads;
+    const int u0 = blockIdx.y * a.upc;
+    const int nu = min(a.upc, LH - u0);
+    const int total = nu * sp.len;
+
+    for (int r0 = threadIdx.x / TPR; r0 < total; r0 += 2 * RPP) {
+        uint4 klo[2], khi[2], vlo[2], vhi[2];
+        int64_t dst[2];
+        bool ok[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int r = r0 + u * RPP;
+            ok[u] = r < total;
+            if (ok[u]) {
+                const int unit = u0 + r / sp.len;
+                const int row = r - (r / sp.len) * sp.len;
+                const int l = unit / a.n_heads, h = unit - l * a.n_heads;
+                const int64_t so = l * sl + h * sh + (int64_t)(sp.start + row) * st + j * E;
+                klo[u] = ld_stream(kb + so);
+                khi[u] = ld_stream(kb + so + H2);
+                vlo[u] = ld_stream(vb + so);
+                vhi[u] = ld_stream(vb + so + H2);
+                dst[u] = (sp.dst_row0 + (int64_t)unit * sp.cap + sp.row + row) * D + j * E;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (ok[u]) {
+                if (sp.dstep) {  // un-rotated source: token t turns by delta + t
+                    const int r = r0 + u * RPP;
+                    const int row = r - (r / sp.len) * sp.len;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float2 cs = rope_cs(a.rope, H2, sp.delta + row, j * E + e);
+                        c[e] = cs.x;
+                        s[e] = cs.y;
+                    }
+                }
+                Vec<T>::rotate(klo[u], khi[u], c, s);
+                st_vec(ck + dst[u], klo[u]);
+                st_vec(ck + dst[u] + H2, khi[u]);
+                st_vec(cv + dst[u], vlo[u]);
+                st_vec(cv + dst[u] + H2, vhi[u]);
+            }
+        }
+    }
+
+    // position ids and source map, written once per span
+    if (blockIdx.y == 0) {
+        for (int t = threadIdx.x; t < sp.len; t += kAssembleThreads) {
+            if (a.pos_ids)
+                a.pos_ids[sp.flat0 + t] = sp.pos0 + t;
+            if (a.src_map) {
+                a.src_map[2 * (sp.flat0 + t)] = sp.src;
+                a.src_map[2 * (sp.flat0 + t) + 1] = sp.start + t;
+            }
+        }
+    }
+}
+
+cudaError_t launch_assemble(const AssembleArgs &a, int dtype, int head_dim, int n_spans,
+                            cudaStream_t s)
+{
+    if (n_spans == 0)
+        return cudaSuccess;
+    const int LH = a.n_layers * a.n_heads;
+    dim3 grid(n_spans, (LH + a.upc - 1) / a.upc);
+    if (dtype == KVR_DTYPE_BF16 && head_dim == 128)
+        k_assemble<__nv_bfloat16, 128><<<grid, kAssembleThreads, 0, s>>>(a);
+    else if (dtype == KVR_DTYPE_BF16 && head_dim == 64)
+        k_assemble<__nv_bfloat16, 64><<<grid, kAssembleThreads, 0, s>>>(a);
+    else if (dtype == KVR_DTYPE_FP32 && head_dim == 128)
+        k_assemble<float, 128><<<grid, kAssembleThreads, 0, s>>>(a);
+    else if (dtype == KVR_DTYPE_FP32 && head_dim == 64)
+        k_assemble<float, 64><<<grid, kAssembleThreads, 0, s>>>(a);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace kvr

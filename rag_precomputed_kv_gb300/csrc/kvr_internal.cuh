@@ -1,0 +1,120 @@
+// kvr_internal.cuh -- types shared by the libkvr translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvr.h"
+
+namespace kvr {
+
+// RoPE tables: angle(n, i) = n * theta^(-2i/D) for n in [0, 2^24) is split as
+// n = hi * 4096 + lo; the table holds (cos, sin) of hi * 4096 * w_i
+// (rows 0..4095) and of lo * w_i (rows 4096..8191), each computed in double
+// precision and rounded to float.  One complex product in float recombines
+// them: the angle-addition identity, with error of a few float ulps for
+// every position (a float product n * w_i would be off by up to ~2e-3 rad at
+// n ~ 3e4).
+constexpr int kRopeSplit = 4096;
+constexpr int kMaxPosition = kRopeSplit * kRopeSplit;  // 2^24
+
+#ifdef __CUDACC__
+// (cos, sin) of pos * w_i for |pos| < 2^24 from the two table halves (angle
+// addition, one complex product in float); a negative pos is the conjugate.
+__device__ __forceinline__ float2 rope_cs(const float2 *__restrict__ tab, int half, int pos, int i)
+{
+    const int a = pos < 0 ? -pos : pos;
+    const float2 h = __ldg(tab + (a >> 12) * half + i);
+    const float2 l = __ldg(tab + (kRopeSplit + (a & (kRopeSplit - 1))) * half + i);
+    const float c = fmaf(h.x, l.x, -h.y * l.y);
+    const float s = fmaf(h.y, l.x, h.x * l.y);
+    return make_float2(c, pos < 0 ? -s : s);
+}
+#endif
+
+// Device copy of one span (48 bytes).
+struct alignas(16) DevSpan {
+    int64_t dst_row0;  // first row of the request's cache block, in head_dim rows
+    int64_t flat0;     // index of the span's first token in the flat pos / src maps
+    int32_t src;       // pool entry, or KVR_SRC_LOCAL | local index
+    int32_t start;     // first source token
+    int32_t len;       // tokens
+    int32_t row;       // first stitched row inside the request's block
+    int32_t delta;     // rotation applied to the keys (positions)
+    int32_t pos0;      // position id of the first token
+    int32_t cap;       // rows per (layer, kv-head) block of the request
+    int32_t dstep;     // 0: source keys carry their source positions (rotate all
+                       //    tokens by delta); 1: source keys are un-rotated
+                       //    (token t is rotated by delta + t)
+};
+
+// Device copy of one request-local source.
+struct alignas(16) DevLocal {
+    const void *k;
+    const void *v;
+    int64_t s_layer, s_head, s_tok;
+    int64_t len;
+};
+
+// Per-request data for the attention kernels (32 bytes).
+struct alignas(16) DevReq {
+    int64_t cache_row0;  // cache_offsets[b] * L * H_kv
+    int32_t cap;         // R_b
+    int32_t prefix;      // P_b
+    int32_t q_off;       // first query token (token axis of q / out)
+    int32_t q_len;       // Lq_b
+    int32_t m_tile0;     // first M-tile index of this request (tensor-core path)
+    int32_t pad;
+};
+
+// Device error word codes (first error wins).
+enum : int { kDevOk = 0, kDevTimeout = 1, kDevBadInput = 2 };
+
+struct AssembleArgs {
+    const DevSpan *spans;
+    const DevLocal *locals;
+    const float2 *rope;
+    const void *pool_k;
+    const void *pool_v;
+    int64_t ps_entry, ps_layer, ps_head, ps_tok;
+    void *cache_k;
+    void *cache_v;
+    int32_t *pos_ids;
+    int32_t *src_map;
+    int32_t n_layers, n_heads;  // kv heads
+    int32_t upc;                // (layer, head) units per CTA
+};
+
+struct AttnArgs {
+    const DevReq *reqs;
+    int32_t n_reqs;
+    const float2 *rope;
+    const void *q;              // [L][T][Hq][D]
+    const void *cache_k;
+    const void *cache_v;
+    void *out;                  // [L][T][Hq][D]
+    int32_t n_layers, n_q_heads, n_kv_heads;
+    int32_t total_q;            // T
+    float scale_log2;           // softmax scale * log2(e)
+    int *err;
+};
+
+// ---- launchers (each returns the cudaGetLastError of its launch) ----
+cudaError_t launch_rope_tables(float2 *tab, int head_dim, double theta, cudaStream_t s);
+cudaError_t launch_assemble(const AssembleArgs &a, int dtype, int head_dim, int n_spans,
+                            cudaStream_t s);
+cudaError_t launch_attention_simt(const AttnArgs &a, int dtype, int head_dim, cudaStream_t s);
+
+// Tensor-core attention (bf16, head_dim 128).  `tmaps` points to two
+// CUtensorMap objects (K then V) describing the cache as a 2-D
+// [rows, head_dim] bf16 tensor.
+struct TcAttnArgs {
+    AttnArgs base;
+    const void *tmap_k;         // host CUtensorMap, passed by value to the kernel
+    const void *tmap_v;
+    int32_t n_m_tiles;          // total M-tiles over all requests
+};
+cudaError_t launch_attention_tc(const TcAttnArgs &a, cudaStream_t s);
+bool attention_tc_supported(int dtype, int head_dim);
+
+}  // namespace kvr

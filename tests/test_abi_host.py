@@ -1,0 +1,155 @@
+"""The C ABI on the CPU: the library loads, exports every declared entry
+point, and rejects bad arguments with a status before touching the GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from rag_precomputed_kv_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    from rag_precomputed_kv_gb300 import kvr
+    return kvr.load()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    return re.findall(r"KVR_API\s+[\w\s\*]+?\b(kvr_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
+              "kvr_check", "kvr_status_string", "kvr_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from rag_precomputed_kv_gb300 import kvr
+    for code, name in kvr.STATUS.items():
+        assert lib.kvr_status_string(code).decode() == name
+
+
+def _desc(**kw):
+    from rag_precomputed_kv_gb300 import kvr
+    d = dict(n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128, dtype=kvr.KVR_DTYPE_BF16,
+             reserved=0, n_entries=4, entry_len=512, k=0x10000, v=0x20000,
+             stride=(2 * 2 * 512 * 128, 2 * 512 * 128, 512 * 128, 128), rope_theta=1e6)
+    d.update(kw)
+    s = d.pop("stride")
+    desc = kvr.PoolDesc(**{k: v for k, v in d.items()})
+    desc.stride = (ctypes.c_int64 * 4)(*s)
+    return desc
+
+
+def _register(lib, desc):
+    h = ctypes.c_void_p()
+    st = lib.kvr_pool_register(ctypes.byref(desc), ctypes.byref(h))
+    return st, h
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(dtype=7), 3), (dict(head_dim=96), 3), (dict(n_q_heads=7), 1), (dict(n_layers=0), 1),
+    (dict(n_entries=0), 1), (dict(reserved=1), 1), (dict(k=0), 1), (dict(k=0x10008), 1),
+    (dict(rope_theta=0.5), 1), (dict(stride=(8, 8, 8, 12)), 1), (dict(stride=(-8, 8, 8, 8)), 1),
+])
+def test_register_rejects_bad_descriptors(lib, bad, status):
+    st, h = _register(lib, _desc(**bad))
+    assert st == status and not h.value
+    assert lib.kvr_last_error().decode()
+
+
+def test_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.kvr_pool_register(None, ctypes.byref(h)) == 1
+    assert lib.kvr_assemble(None, 1, None, None, None, 0, None, None, None, None, None, None, 0, None) == 1
+    assert lib.kvr_query_attention(None, 1, None, None, None, None, None, None, None, None, None,
+                                   ctypes.c_float(0), None) == 1
+    assert lib.kvr_pool_unregister(None) == 0
+
+
+def _assemble(lib, h, spans, span_offsets, cache_offsets, locals_=None, n_locals=0, flags=0,
+              cache=0x100000):
+    from rag_precomputed_kv_gb300 import kvr
+    so = np.ascontiguousarray(span_offsets, np.int32)
+    sp = np.ascontiguousarray(spans, np.int32).reshape(-1, 3)
+    co = np.ascontiguousarray(cache_offsets, np.int64)
+    plen = np.zeros(len(so), np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    st = lib.kvr_assemble(h, len(so) - 1, p(so), p(sp) if sp.size else None, locals_, n_locals,
+                          p(co), cache, cache, None, None, p(plen), flags, None)
+    return st, plen
+
+
+def test_assemble_validates_spans_before_any_gpu_work(lib):
+    st, h = _register(lib, _desc())
+    assert st == 0
+    try:
+        # unknown pool entry, span past the entry end, inverted span, local without locals
+        for spans in ([[4, 0, 8]], [[0, 500, 513]], [[0, 9, 8]], [[-1, 0, 1]], [[(1 << 30) | 0, 0, 4]]):
+            st, _ = _assemble(lib, h, spans, [0, 1], [0, 1000])
+            assert st == 2, spans
+        # prefix longer than the cache block
+        st, _ = _assemble(lib, h, [[0, 0, 512], [1, 0, 512]], [0, 2], [0, 1000])
+        assert st == 2
+        # non-monotone offsets, bad flags
+        assert _assemble(lib, h, [[0, 0, 8]], [1, 1], [0, 100])[0] == 1
+        assert _assemble(lib, h, [[0, 0, 8]], [0, 1], [10, 5])[0] == 1
+        assert _assemble(lib, h, [[0, 0, 8]], [0, 1], [0, 100], flags=4)[0] == 1
+        # misaligned cache pointer
+        assert _assemble(lib, h, [[0, 0, 8]], [0, 1], [0, 100], cache=0x100004)[0] == 1
+        # only empty spans: nothing to launch, prefix lengths are still reported
+        st, plen = _assemble(lib, h, [[0, 3, 3], [2, 0, 0]], [0, 1, 2], [0, 10, 20])
+        assert st == 0 and plen[:2].tolist() == [0, 0]
+    finally:
+        lib.kvr_pool_unregister(h)
+
+
+def test_query_attention_validates_capacity(lib):
+    st, h = _register(lib, _desc())
+    assert st == 0
+    try:
+        co = np.array([0, 100], np.int64)
+        pl = np.array([90], np.int32)
+        qo = np.array([0, 16], np.int32)
+        p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+        buf = 0x100000
+        st = lib.kvr_query_attention(h, 1, p(co), p(pl), p(qo), buf, buf, buf, buf, buf, buf,
+                                     ctypes.c_float(0), None)
+        assert st == 2                         # 90 + 16 > 100 rows
+        st = lib.kvr_query_attention(h, 1, p(co), p(pl), p(qo), buf + 2, buf, buf, buf, buf, buf,
+                                     ctypes.c_float(0), None)
+        assert st == 1                         # misaligned q
+        st = lib.kvr_query_attention(h, 1, p(co), p(pl), p(qo), buf, buf, buf, buf, buf, buf,
+                                     ctypes.c_float(-1.0), None)
+        assert st == 1                         # negative scale
+    finally:
+        lib.kvr_pool_unregister(h)
+
+
+def test_no_gpu_means_cuda_error_not_a_crash(lib):
+    """With valid arguments and no GPU, the first call that needs the device
+    reports KVR_ERR_CUDA (no CPU fallback exists)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, h = _register(lib, _desc())
+    try:
+        st, _ = _assemble(lib, h, [[0, 0, 8]], [0, 1], [0, 100])
+        assert st == 4
+    finally:
+        lib.kvr_pool_unregister(h)
