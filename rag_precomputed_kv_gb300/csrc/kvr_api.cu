@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -555,6 +556,12 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
         if (tc) {
             CUtensorMap mk, mv;
             const int64_t rows = cache_offsets[batch] * LH;
+            if (rows > (int64_t)INT32_MAX - 256) {   // TMA row coordinates are int32
+                cudaEventRecord(slot->done, s);
+                slot->used = true;
+                return fail(KVR_ERR_UNSUPPORTED, "cache of %lld rows exceeds the int32 TMA coordinate range",
+                            (long long)rows);
+            }
             if ((st = encode_cache_map(*p, cache_k, rows, &mk)) != KVR_OK ||
                 (st = encode_cache_map(*p, cache_v, rows, &mv)) != KVR_OK) {
                 cudaEventRecord(slot->done, s);
