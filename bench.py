@@ -1,0 +1,450 @@
+"""Benchmark of the precomputed-KV RAG hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic
+requests: kvr_assemble (span gather + RoPE re-rotation + stitch) followed by
+kvr_query_attention (query RoPE + K/V append + tcgen05 prefill attention).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl kvr|reference]
+
+The default workload is the full-chunk-reuse configuration (Qwen2-7B shape,
+five 512-token chunks after a 32-token system prompt, 64 query tokens,
+batch 1).  Prints ONE JSON line (rank 0).  Timing: CUDA events on the
+launching stream around every step, L2 flushed (256 MiB write) between steps
+outside the events, a barrier and synchronize on both sides of the timed
+region, max over ranks.  Each rank runs its own replica of the batch (the
+path shards by request with no exchange), so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rag_precomputed_kv_gb300 import workloads as W  # noqa: E402
+
+METRIC = "stitched KV tokens/s & HBM GB/s; query-attn TFLOP/s; per-request latency"
+UNIT = "stitched tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
+                    bf16_tflops_sustained=p.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="kvr_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# the CUDA path
+# ----------------------------------------------------------------------------
+class Workload:
+    """A batch of requests with its pool, cache and query tensors on one GPU."""
+
+    def __init__(self, cfg: W.Config, device):
+        import torch
+        from rag_precomputed_kv_gb300 import kvr
+        self.cfg = cfg
+        self.reqs = W.draw_spans(cfg)
+        self.t = W.make_tensors(cfg, self.reqs, device=device)
+        self.locals = [(k, v) for k, v in zip(self.t.local_k, self.t.local_v) if k is not None]
+        remap, n = {}, 0
+        for b, k in enumerate(self.t.local_k):
+            if k is not None:
+                remap[b], n = n, n + 1
+        spans = []
+        for r in self.reqs:
+            sp = r.spans.copy()
+            loc = (sp[:, 0] & W.LOCAL_FLAG) != 0
+            for i in np.nonzero(loc)[0]:
+                sp[i, 0] = W.LOCAL_FLAG | remap[int(sp[i, 0] & ~W.LOCAL_FLAG)]
+            spans.append(sp)
+        self.spans = np.concatenate(spans)
+        self.span_offsets = np.concatenate([[0], np.cumsum([len(s) for s in spans])]).astype(np.int32)
+        self.prefix = np.array([r.prefix_len for r in self.reqs], np.int64)
+        lq = cfg.query_len
+        self.cache_offsets = np.concatenate([[0], np.cumsum(self.prefix + lq)]).astype(np.int64)
+        self.q_offsets = (np.arange(len(self.reqs) + 1) * lq).astype(np.int32)
+        rows = int(self.cache_offsets[-1]) * cfg.n_layers * cfg.n_kv_heads
+        self.cache_k = torch.empty((rows, cfg.head_dim), dtype=self.t.pool_k.dtype, device=device)
+        self.cache_v = torch.empty_like(self.cache_k)
+        self.out = torch.empty_like(self.t.q)
+        self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta)
+        self.plen = self.prefix.astype(np.int32)
+
+    def step(self, q=None, kq=None, vq=None, out=None):
+        self.pool.assemble(self.span_offsets, self.spans, self.cache_offsets, self.cache_k,
+                           self.cache_v, locals_=self.locals)
+        self.pool.query_attention(self.cache_offsets, self.plen, self.q_offsets,
+                                  self.t.q if q is None else q, self.t.kq if kq is None else kq,
+                                  self.t.vq if vq is None else vq, self.cache_k, self.cache_v,
+                                  self.out if out is None else out)
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_kvr(args):
+    import torch
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    wl = Workload(cfg, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    from rag_precomputed_kv_gb300 import kvr as K
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        wl.step()
+    torch.cuda.synchronize()
+    wl.pool.check()
+
+    # ---- timed region: device-resident inputs ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in [x for row in ev for x in row] + e0 + e1:   # create the CUDA events up front
+        e.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        wl.pool.set_timing_events(ev[k])
+        e0[k].record(stream)
+        wl.step()
+        e1[k].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    wl.pool.set_timing_events(None)
+    wl.pool.check()
+    step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
+    asm_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    app_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    att_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+
+    # ---- end to end through the public API with host buffers ----
+    q_h = wl.t.q.cpu().pin_memory()
+    kq_h = wl.t.kq.cpu().pin_memory()
+    vq_h = wl.t.vq.cpu().pin_memory()
+    out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+    q_d, kq_d, vq_d = torch.empty_like(wl.t.q), torch.empty_like(wl.t.kq), torch.empty_like(wl.t.vq)
+    out_d = torch.empty_like(wl.out)
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, kq_h, vq_h))
+    d2h = out_h.numel() * out_h.element_size()
+    for _ in range(args.warmup):
+        flush.zero_()
+        q_d.copy_(q_h, non_blocking=True); kq_d.copy_(kq_h, non_blocking=True)
+        vq_d.copy_(vq_h, non_blocking=True)
+        wl.step(q_d, kq_d, vq_d, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+    torch.cuda.synchronize()
+    f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        f0[k].record(stream)
+        q_d.copy_(q_h, non_blocking=True); kq_d.copy_(kq_h, non_blocking=True)
+        vq_d.copy_(vq_h, non_blocking=True)
+        wl.step(q_d, kq_d, vq_d, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+        f1[k].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(f0, f1)) / 1e3, world)
+    torch.testing.assert_close(out_h, wl.out.cpu(), rtol=0, atol=0)
+
+    # ---- figures ----
+    tokens_per_step = int(wl.prefix.sum())
+    value = tokens_per_step * args.steps * world / total_s
+    e2e_value = tokens_per_step * args.steps * world / e2e_s
+    pk = peaks()
+    asm_bytes = W.assemble_bytes(cfg, wl.reqs)
+    att_flops = W.attention_flops(cfg, wl.reqs)
+    asm_mean, att_mean, app_mean = (statistics.mean(x) for x in (asm_ms, att_ms, app_ms))
+    asm_gbs = asm_bytes / (asm_mean * 1e-3) / 1e9
+    att_tf = att_flops / (att_mean * 1e-3) / 1e12
+    roof_asm = {"kernel": "k_assemble", "bound": "hbm", "achieved": round(asm_gbs, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(asm_gbs / pk["hbm_gbs"], 4),
+                "traffic": None, "algorithmic_bytes": asm_bytes, "ms": round(asm_mean, 5),
+                "peak_source": pk["source"]}
+    roof_att = {"kernel": "k_attention_tc" if wl.pool.attention_path == K.PATH_TCGEN05 else "k_attention_simt",
+                "bound": "tensor", "achieved": round(att_tf, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(att_tf / pk["bf16_tflops"], 4), "traffic": None,
+                "algorithmic_flops": att_flops, "ms": round(att_mean, 5), "peak_source": pk["source"]}
+    dominant, other = (roof_asm, roof_att) if asm_mean >= att_mean else (roof_att, roof_asm)
+    lat = sorted(step_ms)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded N(0,1) K/V/Q, random span draws; no datasets or weights)",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "layers": cfg.n_layers,
+                   "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
+                   "chunk_len": cfg.chunk_len, "pool_entries": cfg.pool_entries,
+                   "stitched_tokens_per_step": tokens_per_step, "query_tokens_per_request": cfg.query_len,
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "parallelism": f"request replicas x{world}"},
+        "roofline": dominant, "roofline_other": other,
+        "assemble_gbs": round(asm_gbs, 1), "attention_tflops": round(att_tf, 2),
+        "append_ms": round(app_mean, 5),
+        "latency_ms": {"p50": round(lat[len(lat) // 2], 5), "p99": round(lat[min(len(lat) - 1, int(0.99 * len(lat)))], 5),
+                       "what": "one step (assemble + query attention) per batch, device time"},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3 / args.steps, 5)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = oracle_baseline(cfg, wl, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------
+class OracleSampler:
+    """Times the fp64 oracle on bounded samples of the workload.
+
+    A sample is the full assemble of U (layer, kv-head) units of request 0
+    (U = the oracle's thread count) and its query attention restricted to the
+    first lq_s query tokens (causal: those rows see exactly what they see in
+    the full call).  The batch time is extrapolated linearly: assemble by
+    stitched rows, attention by (query row, visible key) pairs.
+    """
+
+    def __init__(self, cfg: W.Config, wl=None):
+        import torch
+        import oracle
+        oracle.build()
+        self.oracle, self.cfg = oracle, cfg
+        if wl is not None:
+            self.reqs, t = wl.reqs, wl.t
+            self.span_list = np.split(wl.spans, wl.span_offsets[1:-1])
+            locals_ = wl.locals
+        else:
+            self.reqs = W.draw_spans(cfg)
+            t = W.make_tensors(cfg, self.reqs, device="cpu")
+            self.span_list = [r.spans for r in self.reqs]
+            locals_ = [(k, v) for k, v in zip(t.local_k, t.local_v) if k is not None]
+        H, G, lq = cfg.n_kv_heads, cfg.group, cfg.query_len
+        self.LH = cfg.n_layers * H
+        self.threads = oracle.num_threads()
+        self.units = list(range(min(self.LH, max(1, self.threads))))
+        to64 = lambda x: x.detach().to("cpu", torch.float64).numpy()
+        li = torch.tensor([u // H for u in self.units])
+        hi = torch.tensor([u % H for u in self.units])
+        self.sources = {}
+        for s in np.unique(self.span_list[0][:, 0]):
+            s = int(s)
+            k, v = locals_[s & ~W.LOCAL_FLAG] if s & W.LOCAL_FLAG else (t.pool_k[s], t.pool_v[s])
+            d = k.device
+            self.sources[s] = (to64(k[li.to(d), hi.to(d)])[None], to64(v[li.to(d), hi.to(d)])[None])
+        q, kq, vq = (to64(x[:, 0:lq]) for x in (t.q, t.kq, t.vq))
+        self.qu = np.stack([q[u // H, :, (u % H) * G:(u % H + 1) * G] for u in self.units])
+        self.kqu = np.stack([kq[u // H, :, u % H] for u in self.units])
+        self.vqu = np.stack([vq[u // H, :, u % H] for u in self.units])
+        self.P0 = self.reqs[0].prefix_len
+        self.tokens = int(sum(r.prefix_len for r in self.reqs))
+
+    @staticmethod
+    def pairs(P, n):
+        return n * (P + 1) + n * (n - 1) // 2
+
+    def sample(self, lq_s):
+        """(assemble seconds, attention seconds) of one sample."""
+        o = self.oracle
+        t0 = time.perf_counter()
+        K, V, _ = o.assemble(self.sources, self.span_list[0], self.cfg.rope_theta)
+        t1 = time.perf_counter()
+        o.query_attention(K[0], V[0], self.qu[:, :lq_s], self.kqu[:, :lq_s], self.vqu[:, :lq_s],
+                          self.cfg.rope_theta)
+        return t1 - t0, time.perf_counter() - t1
+
+    def batch_seconds(self, lq_s, t_asm, t_att):
+        U, lq = len(self.units), self.cfg.query_len
+        per_row = t_asm / max(1, self.P0) / U                  # one unit, one stitched row
+        per_pair = t_att / self.pairs(self.P0, lq_s) / U       # one unit, one (row, key) pair
+        total = 0.0
+        for r in self.reqs:
+            total += self.LH * (per_row * r.prefix_len + per_pair * self.pairs(r.prefix_len, lq))
+        return total
+
+    def choose_lq(self, budget_s):
+        """Largest query-token count whose sample fits the budget."""
+        t_asm, t_att1 = self.sample(1)
+        per_pair = t_att1 / self.pairs(self.P0, 1)
+        lq = self.cfg.query_len
+        n = 1
+        while n < lq and t_asm + per_pair * self.pairs(self.P0, n + 1) <= budget_s:
+            n += 1
+        return n
+
+    def describe(self, lq_s):
+        return (f"{len(self.units)} of {self.LH} (layer, kv-head) units of request 0: full assemble "
+                f"({self.P0} stitched rows) + attention of the first {lq_s} of {self.cfg.query_len} query "
+                f"tokens, fp64; extrapolated to the batch by rows and (row, key) pairs")
+
+
+def oracle_baseline(cfg, wl, budget_s):
+    smp = OracleSampler(cfg, wl)
+    lq_s = smp.choose_lq(budget_s)
+    t_asm, t_att = smp.sample(lq_s)
+    value = smp.tokens / smp.batch_seconds(lq_s, t_asm, t_att)
+    return {"value": round(value, 2), "unit": UNIT, "cores": smp.threads, "kind": "oracle",
+            "sample": smp.describe(lq_s) + f" ({t_asm + t_att:.1f} s)"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = W.CONFIGS[args.config]
+    smp = OracleSampler(cfg)
+    per_step = max(0.02, args.ref_budget / (args.steps + args.warmup))
+    lq_s = smp.choose_lq(per_step)
+    for _ in range(args.warmup):
+        smp.sample(lq_s)
+    secs = []
+    for _ in range(args.steps):
+        t_asm, t_att = smp.sample(lq_s)
+        secs.append(smp.batch_seconds(lq_s, t_asm, t_att))
+    step_s = statistics.mean(secs)
+    value = smp.tokens / step_s
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1) K/V/Q, random span draws; no datasets or weights)",
+           "config": {"workload": cfg.name, "batch": cfg.batch, "stitched_tokens_per_step": smp.tokens},
+           "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": smp.threads, "kind": "oracle",
+                            "sample": smp.describe(lq_s) + " per step"},
+           "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2, choices=sorted(W.CONFIGS))
+    ap.add_argument("--impl", default="kvr", choices=["kvr", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="seconds of oracle work for the whole reference-arm run")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvr(args)
+
+
+if __name__ == "__main__":
+    main()

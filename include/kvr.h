@@ -192,6 +192,23 @@ KVR_API kvr_status kvr_query_attention(kvr_pool_t pool, int32_t batch, const int
                                void *cache_k, void *cache_v, void *out,
                                float softmax_scale, void *stream);
 
+/* Attention kernels a pool can select (kvr_attention_path). */
+enum { KVR_PATH_UNBOUND = -1, KVR_PATH_CUDA_CORES = 0, KVR_PATH_TCGEN05 = 1 };
+
+/* Which attention kernel kvr_query_attention runs for this pool: the
+ * tcgen05 tensor-core kernel (bf16, head_dim 128, sm_103) or the CUDA-core
+ * kernel (fp32 or head_dim 64).  KVR_PATH_UNBOUND until the pool's first
+ * call has bound it to a device; -2 for a NULL pool. */
+KVR_API int32_t kvr_attention_path(kvr_pool_t pool);
+
+/* Timing hook.  With events non-NULL, later calls on this pool record, on the
+ * caller's stream, events[0] / events[1] right before / after the assemble
+ * kernel, events[2] / events[3] around the query-append kernel and
+ * events[4] / events[5] around the attention kernel.  The handles are
+ * cudaEvent_t created by the caller (timing enabled); the array is copied.
+ * NULL turns the hook off. */
+KVR_API kvr_status kvr_set_timing_events(kvr_pool_t pool, void *const *events);
+
 /* Synchronize `stream` and return (then clear) the first error a kernel of
  * this pool recorded: KVR_OK, KVR_ERR_TIMEOUT, KVR_ERR_DEVICE_CHECK or
  * KVR_ERR_CUDA. */

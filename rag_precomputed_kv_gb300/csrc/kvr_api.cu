@@ -86,6 +86,14 @@ struct kvr_pool {
     int next = 0;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     bool ready = false;       // device-side setup done
+    cudaEvent_t timing[6] = {};  // optional kernel timing events (caller-owned)
+    bool timed = false;
+
+    void mark(int i, cudaStream_t s) const
+    {
+        if (timed && timing[i])
+            cudaEventRecord(timing[i], s);
+    }
 
     int elt() const { return d.dtype == KVR_DTYPE_BF16 ? 2 : 4; }
     int vec_elems() const { return 16 / elt(); }
@@ -220,6 +228,12 @@ extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
         cudaFree(p->err);
     delete p;
     return KVR_OK;
+}
+
+// The tcgen05 kernel runs for bf16 pools with head_dim 128 on sm_103.
+static bool use_tensor_cores(const kvr_pool &p)
+{
+    return attention_tc_supported(p.d.dtype, p.d.head_dim) && p.cc == 103 && p.encode;
 }
 
 // ---------------------------------------------------------------------------
@@ -398,7 +412,9 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
     a.n_layers = p->d.n_layers;
     a.n_heads = p->d.n_kv_heads;
     a.upc = units_per_cta(LH, flat, (int64_t)ds.size());
+    p->mark(0, s);
     e = launch_assemble(a, p->d.dtype, p->d.head_dim, (int)ds.size(), s);
+    p->mark(1, s);
     cudaEventRecord(slot->done, s);
     slot->used = true;
     if (e != cudaSuccess)
@@ -474,7 +490,7 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
     }
     if ((st = ensure_device(p)) != KVR_OK)
         return st;
-    const bool tc = attention_tc_supported(p->d.dtype, D) && p->cc == 103 && p->encode;
+    const bool tc = use_tensor_cores(*p);
     for (int b = 0; b < batch; ++b) {
         const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
         const int32_t P = prefix_len[b];
@@ -535,7 +551,9 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
     a.n_layers = L;
     a.n_heads = Hkv;
     a.upc = units_per_cta(LH, (int64_t)T, (int64_t)ap.size());
+    p->mark(2, s);
     e = launch_assemble(a, p->d.dtype, D, (int)ap.size(), s);
+    p->mark(3, s);
 
     AttnArgs at{};
     at.reqs = reinterpret_cast<const DevReq *>(dv);
@@ -569,9 +587,13 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
                 return st;
             }
             TcAttnArgs ta{at, &mk, &mv, m_tiles};
+            p->mark(4, s);
             e = launch_attention_tc(ta, s);
+            p->mark(5, s);
         } else {
+            p->mark(4, s);
             e = launch_attention_simt(at, p->d.dtype, D, s);
+            p->mark(5, s);
         }
     }
     cudaEventRecord(slot->done, s);
@@ -621,3 +643,22 @@ extern "C" const char *kvr_status_string(kvr_status s)
 }
 
 extern "C" const char *kvr_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" kvr_status kvr_set_timing_events(kvr_pool_t p, void *const *events)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    p->timed = events != nullptr;
+    for (int i = 0; i < 6; ++i)
+        p->timing[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+    return KVR_OK;
+}
+
+extern "C" int32_t kvr_attention_path(kvr_pool_t p)
+{
+    if (!p)
+        return -2;
+    if (!p->ready)
+        return KVR_PATH_UNBOUND;
+    return use_tensor_cores(*p) ? KVR_PATH_TCGEN05 : KVR_PATH_CUDA_CORES;
+}

@@ -26,7 +26,9 @@ STATUS = {0: "KVR_OK", 1: "KVR_ERR_INVALID_ARG", 2: "KVR_ERR_OUT_OF_RANGE", 3: "
           4: "KVR_ERR_CUDA", 5: "KVR_ERR_TIMEOUT", 6: "KVR_ERR_DEVICE_CHECK"}
 
 EXPORTED = ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
-            "kvr_check", "kvr_status_string", "kvr_last_error")
+            "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
+            "kvr_set_timing_events")
+PATH_UNBOUND, PATH_CUDA_CORES, PATH_TCGEN05 = -1, 0, 1
 
 
 class KvrError(RuntimeError):
@@ -73,6 +75,10 @@ def load(path: str = LIB_PATH):
     lib.kvr_status_string.restype = ctypes.c_char_p
     lib.kvr_status_string.argtypes = [ctypes.c_int]
     lib.kvr_last_error.restype = ctypes.c_char_p
+    lib.kvr_set_timing_events.argtypes = [vp, vp]
+    lib.kvr_set_timing_events.restype = ctypes.c_int
+    lib.kvr_attention_path.argtypes = [vp]
+    lib.kvr_attention_path.restype = ctypes.c_int32
     for name in ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble",
                  "kvr_query_attention", "kvr_check"):
         getattr(lib, name).restype = ctypes.c_int
@@ -166,6 +172,20 @@ class Pool:
         _raise(load().kvr_query_attention(self._h, len(qo) - 1, _np_ptr(co), _np_ptr(pl), _np_ptr(qo),
                                           _ptr(q), _ptr(kq), _ptr(vq), _ptr(cache_k), _ptr(cache_v),
                                           _ptr(out), float(softmax_scale), _stream_ptr(stream)))
+
+    @property
+    def attention_path(self) -> int:
+        """PATH_TCGEN05, PATH_CUDA_CORES, or PATH_UNBOUND before the first call."""
+        return int(load().kvr_attention_path(self._h))
+
+    def set_timing_events(self, events):
+        """Six torch.cuda.Event(enable_timing=True) recorded around the
+        assemble, query-append and attention kernels (None turns it off)."""
+        if events is None:
+            _raise(load().kvr_set_timing_events(self._h, None))
+            return
+        arr = (ctypes.c_void_p * 6)(*[int(e.cuda_event) for e in events])
+        _raise(load().kvr_set_timing_events(self._h, ctypes.cast(arr, ctypes.c_void_p)))
 
     def check(self, stream=None):
         """kvr_check: synchronize and raise on a device-recorded error."""

@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
-              "kvr_check", "kvr_status_string", "kvr_last_error"):
+              "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
+              "kvr_set_timing_events"):
         assert n in names
 
 

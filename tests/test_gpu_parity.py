@@ -29,7 +29,17 @@ def test_config1_composite_positions():
 
 
 def test_config2_whole_chunks_full():
-    _ok(run_parity_case(2))
+    from rag_precomputed_kv_gb300 import kvr
+    case = Case(W.CONFIGS[2])
+    _ok(run_parity_case(cfg=W.CONFIGS[2], case=case))
+    assert case.pool.attention_path == kvr.PATH_TCGEN05
+
+
+def test_fp32_and_head_dim_64_use_cuda_cores():
+    from rag_precomputed_kv_gb300 import kvr
+    case = Case(W.CONFIGS[1])
+    case.run()
+    assert case.pool.attention_path == kvr.PATH_CUDA_CORES
 
 
 def test_config3_nuggets_sampled_units():
