@@ -47,6 +47,23 @@ def peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
+    if there is none for this workload or the kernel source changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("workload") != workload:
+        return None
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha256_16"]:
+            return None
+    return rec["bytes_per_launch"]
+
+
 # ----------------------------------------------------------------------------
 # clocks during the timed region
 # ----------------------------------------------------------------------------
@@ -271,6 +288,8 @@ def run_kvr(args):
                 "bound": "tensor", "achieved": round(att_tf, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(att_tf / pk["bf16_tflops"], 4), "traffic": None,
                 "algorithmic_flops": att_flops, "ms": round(att_mean, 5), "peak_source": pk["source"]}
+    roof_asm["traffic"] = ncu_traffic("k_assemble", cfg.name)
+    roof_att["traffic"] = ncu_traffic(roof_att["kernel"], cfg.name)
     dominant, other = (roof_asm, roof_att) if asm_mean >= att_mean else (roof_att, roof_asm)
     lat = sorted(step_ms)
     res = {
