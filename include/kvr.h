@@ -209,6 +209,37 @@ KVR_API int32_t kvr_attention_path(kvr_pool_t pool);
  * NULL turns the hook off. */
 KVR_API kvr_status kvr_set_timing_events(kvr_pool_t pool, void *const *events);
 
+/*
+ * kvr_assemble_noalloc -- kvr_assemble for callers that cannot allocate.
+ *
+ * The pages have no counterpart: this is a deployment variant.  Some callers
+ * cannot call cudaMalloc (or any allocator) where they stitch a prefix -- an
+ * engine whose caching allocator already holds the free device memory, a
+ * latency-critical request loop that forbids allocations, a plug-in that may
+ * only use its host program's allocator.  This call allocates nothing: it
+ * takes the pool descriptor itself (no handle), builds its span table in a
+ * fixed host array, and keeps its device scratch (span table, local-source
+ * table, RoPE tables: 4.2 MiB) in one file-scope __device__ array that every
+ * GPU loading the library holds until the process exits.  Same arguments,
+ * layout and results as kvr_assemble otherwise (same kernel).
+ *
+ * Limits: at most 4096 non-empty spans and 256 local sources per call, and
+ * head_dim <= 128; beyond them the call returns KVR_ERR_INVALID_ARG before
+ * any GPU work.  The first call on a device looks up the scratch address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the scratch and the host
+ * table: calls from several host threads, or calls that overlap on the GPU
+ * (on different streams), race; the RoPE tables are rebuilt in the scratch,
+ * on the caller's stream, whenever (rope_theta, head_dim) differs from the
+ * previous call on that device.  Nothing in the scratch has to start at zero.
+ */
+KVR_API kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t batch,
+                                        const int32_t *span_offsets, const kvr_span *spans,
+                                        const kvr_local_src *locals, int32_t n_locals,
+                                        const int64_t *cache_offsets, void *cache_k, void *cache_v,
+                                        int32_t *pos_ids, int32_t *src_map, int32_t *prefix_len,
+                                        uint32_t flags, void *stream);
+
 /* Synchronize `stream` and return (then clear) the first error a kernel of
  * this pool recorded: KVR_OK, KVR_ERR_TIMEOUT, KVR_ERR_DEVICE_CHECK or
  * KVR_ERR_CUDA. */
