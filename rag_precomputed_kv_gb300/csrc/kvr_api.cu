@@ -46,9 +46,9 @@ kvr_status cuda_fail(cudaError_t e, const char *what)
 constexpr int kSlots = 4;
 
 struct Slot {
-    void *host = nullptr;   // pinned
-    void *dev = nullptr;
-    size_t cap = 0;
+    void *host = nullptr;   // pinned: tables built by the host
+    void *dev = nullptr;    // device: the uploaded tables, then per-call device scratch
+    size_t host_cap = 0, dev_cap = 0;
     cudaEvent_t done = nullptr;
     bool used = false;
 };
@@ -86,6 +86,13 @@ struct kvr_pool {
     int next = 0;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     bool ready = false;       // device-side setup done
+    int n_sms = 1;
+    // rotated, packed query heads for the tensor-core attention (grown on
+    // demand); q_rot_done orders its reuse after the last call's attention
+    void *q_rot = nullptr;
+    size_t q_rot_cap = 0;
+    cudaEvent_t q_rot_done = nullptr;
+    bool q_rot_used = false;
     cudaEvent_t timing[6] = {};  // optional kernel timing events (caller-owned)
     bool timed = false;
 
@@ -98,28 +105,35 @@ struct kvr_pool {
     int elt() const { return d.dtype == KVR_DTYPE_BF16 ? 2 : 4; }
     int vec_elems() const { return 16 / elt(); }
 
-    // A staging slot holding at least `bytes`; waits until the slot's last
-    // upload and the kernels that read it are done.
-    kvr_status acquire(size_t bytes, Slot **out)
+    // A staging slot with at least `host_bytes` of pinned and `dev_bytes` of
+    // device memory; waits until the slot's last upload and the kernels that
+    // read it are done.
+    kvr_status acquire(size_t host_bytes, size_t dev_bytes, Slot **out)
     {
         Slot &s = slots[next];
         next = (next + 1) % kSlots;
         cudaError_t e;
         if (s.used && (e = cudaEventSynchronize(s.done)) != cudaSuccess)
             return cuda_fail(e, "staging slot wait");
-        if (s.cap < bytes) {
-            size_t cap = std::max<size_t>({bytes, 2 * s.cap, 65536});
+        if (s.host_cap < host_bytes) {
+            const size_t cap = std::max<size_t>({host_bytes, 2 * s.host_cap, 65536});
             if (s.host)
                 cudaFreeHost(s.host);
-            if (s.dev)
-                cudaFree(s.dev);
-            s.host = s.dev = nullptr;
-            s.cap = 0;
+            s.host = nullptr;
+            s.host_cap = 0;
             if ((e = cudaMallocHost(&s.host, cap)) != cudaSuccess)
                 return cuda_fail(e, "staging host buffer");
+            s.host_cap = cap;
+        }
+        if (s.dev_cap < dev_bytes) {
+            const size_t cap = std::max<size_t>({dev_bytes, 2 * s.dev_cap, 65536});
+            if (s.dev)
+                cudaFree(s.dev);
+            s.dev = nullptr;
+            s.dev_cap = 0;
             if ((e = cudaMalloc(&s.dev, cap)) != cudaSuccess)
                 return cuda_fail(e, "staging device buffer");
-            s.cap = cap;
+            s.dev_cap = cap;
         }
         if (!s.done && (e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming)) != cudaSuccess)
             return cuda_fail(e, "staging event");
@@ -182,6 +196,7 @@ static kvr_status ensure_device(kvr_pool *p)
     cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, p->device);
     cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, p->device);
     p->cc = maj * 10 + min;
+    cudaDeviceGetAttribute(&p->n_sms, cudaDevAttrMultiProcessorCount, p->device);
     const size_t tab = sizeof(float2) * 2 * kRopeSplit * (p->d.head_dim / 2);
     if ((e = cudaMalloc(&p->rope, tab)) != cudaSuccess ||
         (e = cudaMalloc(&p->err, sizeof(int))) != cudaSuccess ||
@@ -222,6 +237,12 @@ extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
         if (s.dev)
             cudaFree(s.dev);
     }
+    if (p->q_rot_done) {
+        cudaEventSynchronize(p->q_rot_done);
+        cudaEventDestroy(p->q_rot_done);
+    }
+    if (p->q_rot)
+        cudaFree(p->q_rot);
     if (p->rope)
         cudaFree(p->rope);
     if (p->err)
@@ -380,24 +401,7 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
 
     DeviceGuard g(p->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t off_loc = align16(ds.size() * sizeof(DevSpan));
-    const size_t bytes = off_loc + sizeof(DevLocal) * std::max(n_locals, 0);
-    Slot *slot;
-    if ((st = p->acquire(bytes, &slot)) != KVR_OK)
-        return st;
-    char *h = static_cast<char *>(slot->host);
-    std::memcpy(h, ds.data(), ds.size() * sizeof(DevSpan));
-    for (int i = 0; i < n_locals; ++i) {
-        DevLocal l{locals[i].k, locals[i].v, locals[i].stride[0], locals[i].stride[1],
-                   locals[i].stride[2], locals[i].len};
-        std::memcpy(h + off_loc + i * sizeof(DevLocal), &l, sizeof l);
-    }
-    cudaError_t e;
-    if ((e = cudaMemcpyAsync(slot->dev, h, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_fail(e, "span table upload");
     AssembleArgs a{};
-    a.spans = static_cast<const DevSpan *>(slot->dev);
-    a.locals = reinterpret_cast<const DevLocal *>(static_cast<char *>(slot->dev) + off_loc);
     a.rope = p->rope;
     a.pool_k = p->d.k;
     a.pool_v = p->d.v;
@@ -412,6 +416,37 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
     a.n_layers = p->d.n_layers;
     a.n_heads = p->d.n_kv_heads;
     a.upc = units_per_cta(LH, flat, (int64_t)ds.size());
+    cudaError_t e;
+    if ((int)ds.size() <= kInlineEntries && n_locals <= kInlineEntries) {
+        // small call: the tables travel inside the kernel parameters
+        AssembleTables tab;
+        std::memcpy(tab.spans, ds.data(), ds.size() * sizeof(DevSpan));
+        for (int i = 0; i < n_locals; ++i)
+            tab.locals[i] = DevLocal{locals[i].k, locals[i].v, locals[i].stride[0], locals[i].stride[1],
+                                     locals[i].stride[2], locals[i].len};
+        p->mark(0, s);
+        e = launch_assemble(a, p->d.dtype, p->d.head_dim, (int)ds.size(), s, &tab);
+        p->mark(1, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "assemble launch");
+        return KVR_OK;
+    }
+    const size_t off_loc = align16(ds.size() * sizeof(DevSpan));
+    const size_t bytes = off_loc + sizeof(DevLocal) * std::max(n_locals, 0);
+    Slot *slot;
+    if ((st = p->acquire(bytes, bytes, &slot)) != KVR_OK)
+        return st;
+    char *h = static_cast<char *>(slot->host);
+    std::memcpy(h, ds.data(), ds.size() * sizeof(DevSpan));
+    for (int i = 0; i < n_locals; ++i) {
+        DevLocal l{locals[i].k, locals[i].v, locals[i].stride[0], locals[i].stride[1],
+                   locals[i].stride[2], locals[i].len};
+        std::memcpy(h + off_loc + i * sizeof(DevLocal), &l, sizeof l);
+    }
+    if ((e = cudaMemcpyAsync(slot->dev, h, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "span table upload");
+    a.spans = static_cast<const DevSpan *>(slot->dev);
+    a.locals = reinterpret_cast<const DevLocal *>(static_cast<char *>(slot->dev) + off_loc);
     p->mark(0, s);
     e = launch_assemble(a, p->d.dtype, p->d.head_dim, (int)ds.size(), s);
     p->mark(1, s);
@@ -479,7 +514,7 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
     std::vector<DevReq> rq(batch);
     std::vector<DevSpan> ap;
     std::vector<DevLocal> al;
-    int32_t m_tiles = 0;
+    int32_t m_blocks = 0;
     for (int b = 0; b < batch; ++b) {
         const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
         const int32_t P = prefix_len[b];
@@ -501,8 +536,8 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
         r.prefix = P;
         r.q_off = q_offsets[b];
         r.q_len = Lq;
-        r.m_tile0 = m_tiles;
-        m_tiles += (int32_t)((int64_t(G) * Lq + 127) / 128);
+        r.m_block0 = m_blocks;
+        m_blocks += (int32_t)((int64_t(G) * Lq + 255) / 256);
         if (Lq > 0) {
             // the query tokens' keys / values become cache rows P..P+Lq-1;
             // their keys arrive un-rotated, so token t turns by P + t
@@ -527,36 +562,68 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
 
     DeviceGuard g(p->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+
+    // tensor-core path: rotated packed Q scratch and the three tensor maps,
+    // set up before anything is enqueued
+    CUtensorMap mq, mk, mv;
+    if (tc) {
+        const int64_t rows = cache_offsets[batch] * LH;
+        const int64_t q_rows = (int64_t)L * T * Hq;
+        if (rows > (int64_t)INT32_MAX - 256 || q_rows > (int64_t)INT32_MAX - 256)   // int32 TMA coordinates
+            return fail(KVR_ERR_UNSUPPORTED, "cache or query rows exceed the int32 TMA coordinate range");
+        const size_t q_bytes = (size_t)q_rows * D * 2;
+        if (p->q_rot_cap < q_bytes) {
+            if (p->q_rot_used && (e = cudaEventSynchronize(p->q_rot_done)) != cudaSuccess)
+                return cuda_fail(e, "query scratch wait");
+            if (p->q_rot)
+                cudaFree(p->q_rot);
+            p->q_rot = nullptr;
+            p->q_rot_cap = 0;
+            p->q_rot_used = false;
+            if ((e = cudaMalloc(&p->q_rot, q_bytes)) != cudaSuccess)
+                return cuda_fail(e, "query scratch");
+            p->q_rot_cap = q_bytes;
+        }
+        if (!p->q_rot_done && (e = cudaEventCreateWithFlags(&p->q_rot_done, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "query scratch event");
+        if ((st = encode_cache_map(*p, p->q_rot, q_rows, &mq)) != KVR_OK ||
+            (st = encode_cache_map(*p, cache_k, rows, &mk)) != KVR_OK ||
+            (st = encode_cache_map(*p, cache_v, rows, &mv)) != KVR_OK)
+            return st;
+    }
+
+    const bool inl = batch <= kInlineEntries;   // then ap, al have <= batch entries too
     const size_t off_sp = align16(rq.size() * sizeof(DevReq));
     const size_t off_lc = off_sp + align16(ap.size() * sizeof(DevSpan));
-    const size_t bytes = off_lc + al.size() * sizeof(DevLocal);
-    Slot *slot;
-    if ((st = p->acquire(bytes, &slot)) != KVR_OK)
+    const size_t bytes = inl ? 0 : off_lc + al.size() * sizeof(DevLocal);
+    Slot *slot = nullptr;
+    if (bytes > 0 && (st = p->acquire(bytes, bytes, &slot)) != KVR_OK)
         return st;
-    char *h = static_cast<char *>(slot->host);
-    std::memcpy(h, rq.data(), rq.size() * sizeof(DevReq));
-    std::memcpy(h + off_sp, ap.data(), ap.size() * sizeof(DevSpan));
-    std::memcpy(h + off_lc, al.data(), al.size() * sizeof(DevLocal));
-    cudaError_t e;
-    if ((e = cudaMemcpyAsync(slot->dev, h, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_fail(e, "request table upload");
-    char *dv = static_cast<char *>(slot->dev);
-
+    static const ReqTable no_reqs{};
+    ReqTable rt_inl;
+    AssembleTables tab;
     AssembleArgs a{};
-    a.spans = reinterpret_cast<const DevSpan *>(dv + off_sp);
-    a.locals = reinterpret_cast<const DevLocal *>(dv + off_lc);
-    a.rope = p->rope;
-    a.cache_k = cache_k;
-    a.cache_v = cache_v;
-    a.n_layers = L;
-    a.n_heads = Hkv;
-    a.upc = units_per_cta(LH, (int64_t)T, (int64_t)ap.size());
-    p->mark(2, s);
-    e = launch_assemble(a, p->d.dtype, D, (int)ap.size(), s);
-    p->mark(3, s);
-
     AttnArgs at{};
-    at.reqs = reinterpret_cast<const DevReq *>(dv);
+    if (inl) {
+        std::memcpy(rt_inl.reqs, rq.data(), rq.size() * sizeof(DevReq));
+        std::memcpy(tab.spans, ap.data(), ap.size() * sizeof(DevSpan));
+        std::memcpy(tab.locals, al.data(), al.size() * sizeof(DevLocal));
+        at.reqs = nullptr;
+    } else {
+        char *h = static_cast<char *>(slot->host);
+        char *dv = static_cast<char *>(slot->dev);
+        std::memcpy(h, rq.data(), rq.size() * sizeof(DevReq));
+        std::memcpy(h + off_sp, ap.data(), ap.size() * sizeof(DevSpan));
+        std::memcpy(h + off_lc, al.data(), al.size() * sizeof(DevLocal));
+        if ((e = cudaMemcpyAsync(dv, h, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+            return cuda_fail(e, "request table upload");
+        a.spans = reinterpret_cast<const DevSpan *>(dv + off_sp);
+        a.locals = reinterpret_cast<const DevLocal *>(dv + off_lc);
+        at.reqs = reinterpret_cast<const DevReq *>(dv);
+    }
+    const ReqTable &rt = inl ? rt_inl : no_reqs;
+
     at.n_reqs = batch;
     at.rope = p->rope;
     at.q = q;
@@ -570,34 +637,45 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
     at.scale_log2 = (softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt((float)D)) *
                     1.4426950408889634f;
     at.err = p->err;
-    if (e == cudaSuccess) {
-        if (tc) {
-            CUtensorMap mk, mv;
-            const int64_t rows = cache_offsets[batch] * LH;
-            if (rows > (int64_t)INT32_MAX - 256) {   // TMA row coordinates are int32
-                cudaEventRecord(slot->done, s);
-                slot->used = true;
-                return fail(KVR_ERR_UNSUPPORTED, "cache of %lld rows exceeds the int32 TMA coordinate range",
-                            (long long)rows);
-            }
-            if ((st = encode_cache_map(*p, cache_k, rows, &mk)) != KVR_OK ||
-                (st = encode_cache_map(*p, cache_v, rows, &mv)) != KVR_OK) {
-                cudaEventRecord(slot->done, s);
-                slot->used = true;
-                return st;
-            }
-            TcAttnArgs ta{at, &mk, &mv, m_tiles};
+    if (tc) {
+        // the previous call's attention must be done with the query scratch
+        if (p->q_rot_used && (e = cudaStreamWaitEvent(s, p->q_rot_done, 0)) != cudaSuccess)
+            return cuda_fail(e, "query scratch ordering");
+        QueryPrologueArgs qp{at.reqs, p->rope, q, kq, vq, cache_k, cache_v, p->q_rot, L, Hq, Hkv, T};
+        p->mark(2, s);
+        e = launch_query_prologue(qp, rt, batch, s);
+        p->mark(3, s);
+        if (e == cudaSuccess) {
+            TcAttnArgs ta{at, &rt, &mq, &mk, &mv, m_blocks, p->n_sms};
             p->mark(4, s);
             e = launch_attention_tc(ta, s);
             p->mark(5, s);
-        } else {
+        }
+        cudaEventRecord(p->q_rot_done, s);
+        p->q_rot_used = true;
+    } else {
+        // query keys / values appended by the assemble kernel (un-rotated
+        // source, token t turned by P + t); the query heads are rotated inside
+        // the CUDA-core attention kernel
+        a.rope = p->rope;
+        a.cache_k = cache_k;
+        a.cache_v = cache_v;
+        a.n_layers = L;
+        a.n_heads = Hkv;
+        a.upc = 1;
+        p->mark(2, s);
+        e = launch_assemble(a, p->d.dtype, D, (int)ap.size(), s, inl ? &tab : nullptr);
+        p->mark(3, s);
+        if (e == cudaSuccess) {
             p->mark(4, s);
-            e = launch_attention_simt(at, p->d.dtype, D, s);
+            e = launch_attention_simt(at, rt, p->d.dtype, D, s);
             p->mark(5, s);
         }
     }
-    cudaEventRecord(slot->done, s);
-    slot->used = true;
+    if (slot) {
+        cudaEventRecord(slot->done, s);
+        slot->used = true;
+    }
     if (e != cudaSuccess)
         return cuda_fail(e, "attention launch");
     return KVR_OK;

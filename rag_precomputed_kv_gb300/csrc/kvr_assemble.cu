@@ -110,7 +110,8 @@ constexpr int kAssembleThreads = 256;
 // span is handled by TPR threads; thread j of a row owns elements
 // [j*E, j*E+E) and their RoPE partners [D/2 + j*E, D/2 + j*E + E).
 template <typename T, int D>
-__global__ void __launch_bounds__(kAssembleThreads) k_assemble(const AssembleArgs a)
+__device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSpan *spans,
+                                              const DevLocal *locals)
 {
     constexpr int H2 = D / 2;
     constexpr int E = Vec<T>::E;
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(kAssembleThreads) k_assemble(const AssembleArg
     constexpr int RPP = kAssembleThreads / TPR;   // rows per pass
     static_assert(H2 % E == 0 && kAssembleThreads % TPR == 0, "head_dim");
 
-    const DevSpan sp = a.spans[blockIdx.x];
+    const DevSpan sp = spans[blockIdx.x];
     const int j = threadIdx.x % TPR;
 
     // this thread's E (cos, sin) pairs for the span's rotation
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(kAssembleThreads) k_assemble(const AssembleArg
     const T *kb, *vb;
     int64_t sl, sh, st;
     if (sp.src & KVR_SRC_LOCAL) {
-        const DevLocal lc = a.locals[sp.src & ~KVR_SRC_LOCAL];
+        const DevLocal lc = locals[sp.src & ~KVR_SRC_LOCAL];
         kb = static_cast<const T *>(lc.k);
         vb = static_cast<const T *>(lc.v);
         sl = lc.s_layer;
@@ -209,21 +210,47 @@ __global__ void __launch_bounds__(kAssembleThreads) k_assemble(const AssembleArg
     }
 }
 
+// Tables in global memory (uploaded by the host).
+template <typename T, int D>
+__global__ void __launch_bounds__(kAssembleThreads) k_assemble(const __grid_constant__ AssembleArgs a)
+{
+    assemble_body<T, D>(a, a.spans, a.locals);
+}
+
+// Tables inside the kernel parameters: nothing to upload for small calls.
+template <typename T, int D>
+__global__ void __launch_bounds__(kAssembleThreads)
+    k_assemble_inl(const __grid_constant__ AssembleArgs a, const __grid_constant__ AssembleTables tab)
+{
+    assemble_body<T, D>(a, tab.spans, tab.locals);
+}
+
+template <typename T, int D>
+static void launch_one(const AssembleArgs &a, dim3 grid, cudaStream_t s, const AssembleTables *inl)
+{
+    if (inl)
+        k_assemble_inl<T, D><<<grid, kAssembleThreads, 0, s>>>(a, *inl);
+    else
+        k_assemble<T, D><<<grid, kAssembleThreads, 0, s>>>(a);
+}
+
 cudaError_t launch_assemble(const AssembleArgs &a, int dtype, int head_dim, int n_spans,
-                            cudaStream_t s)
+                            cudaStream_t s, const AssembleTables *inl)
 {
     if (n_spans == 0)
         return cudaSuccess;
+    if (inl && n_spans > kInlineEntries)
+        return cudaErrorInvalidValue;
     const int LH = a.n_layers * a.n_heads;
     dim3 grid(n_spans, (LH + a.upc - 1) / a.upc);
     if (dtype == KVR_DTYPE_BF16 && head_dim == 128)
-        k_assemble<__nv_bfloat16, 128><<<grid, kAssembleThreads, 0, s>>>(a);
+        launch_one<__nv_bfloat16, 128>(a, grid, s, inl);
     else if (dtype == KVR_DTYPE_BF16 && head_dim == 64)
-        k_assemble<__nv_bfloat16, 64><<<grid, kAssembleThreads, 0, s>>>(a);
+        launch_one<__nv_bfloat16, 64>(a, grid, s, inl);
     else if (dtype == KVR_DTYPE_FP32 && head_dim == 128)
-        k_assemble<float, 128><<<grid, kAssembleThreads, 0, s>>>(a);
+        launch_one<float, 128>(a, grid, s, inl);
     else if (dtype == KVR_DTYPE_FP32 && head_dim == 64)
-        k_assemble<float, 64><<<grid, kAssembleThreads, 0, s>>>(a);
+        launch_one<float, 64>(a, grid, s, inl);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

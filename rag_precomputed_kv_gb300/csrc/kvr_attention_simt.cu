@@ -25,8 +25,10 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(128) k_attention_simt(const AttnArgs a)
+__global__ void __launch_bounds__(128)
+    k_attention_simt(const __grid_constant__ AttnArgs a, const __grid_constant__ ReqTable rt)
 {
+    const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
     constexpr int PL = D / 32;  // elements per lane
     const int64_t w = (int64_t)blockIdx.x * 4 + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
@@ -41,14 +43,14 @@ __global__ void __launch_bounds__(128) k_attention_simt(const AttnArgs a)
     int lo = 0, hi = a.n_reqs - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) / 2;
-        if (a.reqs[mid].q_off <= tok)
+        if (reqs[mid].q_off <= tok)
             lo = mid;
         else
             hi = mid - 1;
     }
-    while (lo > 0 && a.reqs[lo].q_len == 0)
+    while (lo > 0 && reqs[lo].q_len == 0)
         --lo;
-    const DevReq rq = a.reqs[lo];
+    const DevReq rq = reqs[lo];
     const int t = tok - rq.q_off;
     const int pos = rq.prefix + t;
     const int G = Hq / a.n_kv_heads;
@@ -100,7 +102,8 @@ __global__ void __launch_bounds__(128) k_attention_simt(const AttnArgs a)
         op[lane + 32 * k] = from_f<T>(acc[k] * inv);
 }
 
-cudaError_t launch_attention_simt(const AttnArgs &a, int dtype, int head_dim, cudaStream_t s)
+cudaError_t launch_attention_simt(const AttnArgs &a, const ReqTable &rt, int dtype, int head_dim,
+                                  cudaStream_t s)
 {
     const int64_t warps = (int64_t)a.n_layers * a.total_q * a.n_q_heads;
     if (warps == 0)
@@ -109,13 +112,13 @@ cudaError_t launch_attention_simt(const AttnArgs &a, int dtype, int head_dim, cu
     if (blocks > 0x7fffffff)
         return cudaErrorInvalidValue;
     if (dtype == KVR_DTYPE_BF16 && head_dim == 128)
-        k_attention_simt<__nv_bfloat16, 128><<<(unsigned)blocks, 128, 0, s>>>(a);
+        k_attention_simt<__nv_bfloat16, 128><<<(unsigned)blocks, 128, 0, s>>>(a, rt);
     else if (dtype == KVR_DTYPE_BF16 && head_dim == 64)
-        k_attention_simt<__nv_bfloat16, 64><<<(unsigned)blocks, 128, 0, s>>>(a);
+        k_attention_simt<__nv_bfloat16, 64><<<(unsigned)blocks, 128, 0, s>>>(a, rt);
     else if (dtype == KVR_DTYPE_FP32 && head_dim == 128)
-        k_attention_simt<float, 128><<<(unsigned)blocks, 128, 0, s>>>(a);
+        k_attention_simt<float, 128><<<(unsigned)blocks, 128, 0, s>>>(a, rt);
     else if (dtype == KVR_DTYPE_FP32 && head_dim == 64)
-        k_attention_simt<float, 64><<<(unsigned)blocks, 128, 0, s>>>(a);
+        k_attention_simt<float, 64><<<(unsigned)blocks, 128, 0, s>>>(a, rt);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

@@ -8,20 +8,31 @@
 // to query rows 0..t of its (layer, kv-head) block of the cache (the query
 // rows were appended, rotated, by the assemble kernel just before).
 //
-// Tiling.  A CTA owns one (request, 128-row M-tile, layer, kv-head).  The
-// G = H_q / H_kv query heads sharing a kv head are packed into M (row
-// r = t * G + g), so each K/V tile feeds all of them.  Per 128-key tile j:
-//   S_j = Q K_j^T      (tcgen05.mma, A = Q smem, B = K smem, D = TMEM, fp32)
-//   P_j = exp2(S_j * scale*log2e - m)   (softmax warps; row r = TMEM lane r)
-//   O  += P_j V_j      (tcgen05.mma, A = P smem, B = V smem (MN-major), D = TMEM)
-// S is double-buffered in TMEM so S_{j+1} runs while the softmax warps work on
-// S_j.  The running max is rescaled lazily: O is rescaled in TMEM only when a
-// row's max grows by more than 8 (log2 units), so that p <= 2^8 stays exact
-// enough in bf16 and the rescale is rare.
+// Tiling.  A work unit is one (request, 256-row query block, layer, kv-head),
+// split into two 128-row tiles A and B; the kernel is persistent (one CTA per
+// SM walks the units), so the next unit's Q load and first S MMAs overlap the
+// current unit's last softmax and its epilogue.  The G = H_q / H_kv query heads that
+// share a kv head are packed into the rows (row r = t * G + g), so each K/V
+// tile is read once for all of them, and once for both tiles.  Per 128-key
+// tile j and tile X in {A, B}:
+//   S_X = Q_X K_j^T          tcgen05.mma, A = Q_X (smem), B = K_j (smem), D = TMEM
+//   P_X = exp2(S_X * c - m)  softmax warpgroup X, one row per thread = TMEM lane;
+//                            P_X is written back into TMEM over S_X as bf16
+//   O_X += P_X V_j           tcgen05.mma, A = P_X (TMEM), B = V_j (smem, MN-major)
+// The MMA warp issues S_A(0), S_B(0), then per tile PV_A(j), S_A(j+1),
+// PV_B(j), S_B(j+1): the tensor core works on one tile while the other
+// tile's warpgroup runs its softmax.  MMAs of one thread execute in issue
+// order, so S_X(j+1) (issued after PV_X(j)) never overwrites P_X(j) before
+// PV_X(j) has read it; and the commit that signals S_X(j+1) covers PV_X(j), so
+// O_X is stable whenever its warpgroup sees a new S_X.  The running max is
+// rescaled lazily: O_X is rescaled in TMEM only when a row's max grows by more
+// than 8 (log2 units).
 //
-// Warp roles (192 threads): warps 0-3 load + rotate Q, run the softmax and
-// the epilogue (one row per thread = one TMEM lane); warp 4 issues the TMA
-// loads; warp 5 owns TMEM and issues the MMAs (one thread).
+// Warp roles (320 threads, one CTA per SM): warps 0-3 and 4-7 are the
+// warpgroups of tiles A and B (softmax, epilogue); warp 8 issues the TMA loads
+// of Q (already rotated and packed by the query-prologue kernel) and of the
+// K/V tiles into a 4-slot ring; warp 9 owns the 512 TMEM columns and issues
+// the MMAs (one thread).  Barrier phases run on across units.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the CTA
 // records KVR_ERR_TIMEOUT in the pool's error word, all roles leave their
@@ -36,28 +47,35 @@ namespace kvr {
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTileM = 128;      // query rows per CTA
+constexpr int kThreads = 320;
+constexpr int kTileM = 128;      // query rows per tile (two tiles per CTA)
 constexpr int kTileN = 128;      // keys per K/V tile
 constexpr int kD = 128;          // head dim
-constexpr int kSlots = 4;        // K/V tile ring (K_j, V_j, K_j+1, ...)
+constexpr int kSlots = 4;        // K/V ring: K_j, V_j, K_j+1, V_j+1
 constexpr int kTileBytes = kTileN * kD * 2;   // 32 KB
 constexpr int kPanelBytes = kTileBytes / 2;   // 16 KB: 128 rows x 64 columns
 constexpr int kTmemCols = 512;
-constexpr int kColS = 0;         // S buffers at columns 0 and 128
-constexpr int kColO = 256;       // O at columns 256..383
+// TMEM columns of tile x: S_x (P_x over its first 64) and O_x
+__host__ __device__ constexpr uint32_t col_s(int x) { return 128u * (uint32_t)x; }
+__host__ __device__ constexpr uint32_t col_o(int x) { return 256u + 128u * (uint32_t)x; }
 constexpr float kRescaleThreshold = 8.0f;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 // shared memory map (offsets from a 1024-aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kTileBytes;
-constexpr int kOffKV = kOffP + kTileBytes;
+constexpr int kOffQ = 0;                          // Q_A, Q_B
+constexpr int kOffKV = kOffQ + 2 * kTileBytes;
 constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
-// barriers: full[kSlots], empty[kSlots], s_full[2], s_empty[2], p_full, o_done, q_ready, drain
-constexpr int kBarFull = 0, kBarEmpty = kSlots, kBarSFull = 2 * kSlots, kBarSEmpty = 2 * kSlots + 2,
-              kBarPFull = 2 * kSlots + 4, kBarODone = 2 * kSlots + 5, kBarQReady = 2 * kSlots + 6,
-              kBarDrain = 2 * kSlots + 7, kNumBars = 2 * kSlots + 8;
+// barriers
+constexpr int kBarFull = 0;                       // [kSlots] K/V tile landed
+constexpr int kBarEmpty = kBarFull + kSlots;      // [kSlots] K/V tile consumed
+constexpr int kBarSFull = kBarEmpty + kSlots;     // [2] S_x computed
+constexpr int kBarPFull = kBarSFull + 2;          // [2] P_x written (128 arrivals)
+constexpr int kBarOFull = kBarPFull + 2;          // [2] O_x final for the unit
+constexpr int kBarOEmpty = kBarOFull + 2;         // [2] O_x read by the epilogue (128 arrivals)
+constexpr int kBarQFull = kBarOEmpty + 2;         // Q tiles landed
+constexpr int kBarQEmpty = kBarQFull + 1;         // all S of the unit done with Q
+constexpr int kBarDrain = kBarQEmpty + 1;
+constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffTmemAddr = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemAddr + 4;
 constexpr int kSmemBytes = kOffAbort + 4 + 1024;   // + alignment slack
@@ -171,6 +189,28 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
                  : "memory");
 }
 
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
 {
@@ -244,12 +284,71 @@ __device__ __forceinline__ void flag_timeout(int *err, volatile int *abort_flag)
     atomicCAS(err, 0, kDevTimeout);
 }
 
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Geometry of one work unit, computed identically by every role.
+struct Unit {
+    DevReq rq;
+    int l, h, lh;
+    int row0[2];        // first packed row of tiles A and B in the request
+    int n_t[2];         // K/V tiles each query tile needs (0: tile has no rows)
+    int n_tiles;        // max of the two
+    int n_valid;        // rows of the (layer, kv-head) block that hold data
+    int m_rows;         // packed query rows of the request
+    int64_t kv_row0;    // first cache row of the block
+    int q_row0;         // first row of tile A in the packed rotated Q
+};
+
+__device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, int n_blocks, int u)
+{
+    Unit w;
+    const int mb = u % n_blocks;
+    w.lh = u / n_blocks;
+    int lo = 0, hi = a.n_reqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (reqs[mid].m_block0 <= mb)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    w.rq = reqs[lo];
+    const int G = a.n_q_heads / a.n_kv_heads;
+    w.l = w.lh / a.n_kv_heads;
+    w.h = w.lh - w.l * a.n_kv_heads;
+    w.m_rows = G * w.rq.q_len;
+    const int base = (mb - w.rq.m_block0) * 2 * kTileM;
+    w.row0[0] = base;
+    w.row0[1] = base + kTileM;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        if (w.row0[x] >= w.m_rows) {
+            w.n_t[x] = 0;
+        } else {
+            const int t_max = min(w.rq.q_len - 1, (w.row0[x] + kTileM - 1) / G);
+            w.n_t[x] = (w.rq.prefix + t_max + 1 + kTileN - 1) / kTileN;
+        }
+    }
+    w.n_tiles = max(w.n_t[0], w.n_t[1]);
+    w.n_valid = w.rq.prefix + w.rq.q_len;
+    w.kv_row0 = w.rq.cache_row0 + (int64_t)w.lh * w.rq.cap;
+    w.q_row0 = (w.lh * a.total_q + w.rq.q_off) * G + base;
+    return w;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_attention_tc(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                   const AttnArgs a)
+    k_attention_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnArgs a,
+                   const __grid_constant__ ReqTable rt, const int n_blocks)
 {
+    const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -260,295 +359,294 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- which (request, M-tile, layer, kv-head) ----
-    const int mt = blockIdx.x;
-    const int lh = blockIdx.y;
-    int lo = 0, hi = a.n_reqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.reqs[mid].m_tile0 <= mt)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    const DevReq rq = a.reqs[lo];
-    const int G = a.n_q_heads / a.n_kv_heads;
-    const int l = lh / a.n_kv_heads, h = lh - l * a.n_kv_heads;
-    const int row0 = (mt - rq.m_tile0) * kTileM;            // first packed row of the tile
-    const int m_rows = G * rq.q_len;                        // packed rows of the request
-    const int t_max = min(rq.q_len - 1, (row0 + kTileM - 1) / G);
-    const int n_keys = rq.prefix + t_max + 1;               // keys any row of the tile sees
-    const int n_tiles = (n_keys + kTileN - 1) / kTileN;
-    const int n_valid = rq.prefix + rq.q_len;               // rows of the block that hold data
-    const int64_t unit_row0 = rq.cache_row0 + (int64_t)lh * rq.cap;
+    const int n_units = n_blocks * a.n_layers * a.n_kv_heads;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumBars; ++i)
-            mbar_init(bar(i), (i == kBarSEmpty || i == kBarSEmpty + 1 || i == kBarPFull || i == kBarQReady)
-                                  ? 128u
-                                  : 1u);
+        for (int i = 0; i < kNumBars; ++i) {
+            const bool wg = (i >= kBarPFull && i < kBarPFull + 2) || (i >= kBarOEmpty && i < kBarOEmpty + 2);
+            mbar_init(bar(i), wg ? 128u : 1u);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5)
+    if (warp == 9)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
-        // =================== softmax / epilogue warpgroup ===================
-        const int r = threadIdx.x;                 // row of the tile = TMEM lane
-        const int rr = row0 + r;                   // packed row in the request
-        const bool row_ok = rr < m_rows;
-        const int t = row_ok ? rr / G : t_max;     // query token of this row
-        const int g = row_ok ? rr - (rr / G) * G : 0;
-        const int pos = rq.prefix + t;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-
-        // Q row: load, rotate at position P + t, store bf16 into the swizzled tile
-        {
-            const __nv_bfloat16 *qp = static_cast<const __nv_bfloat16 *>(a.q) +
-                                      (((int64_t)l * a.total_q + rq.q_off + t) * a.n_q_heads + h * G + g) * kD;
+    if (warp < 8) {
+        // =================== softmax / epilogue warpgroup of tile x ===================
+        const int x = warp >> 2;
+        const int r = threadIdx.x & 127;           // row of the tile = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float sc = a.scale_log2;
+        const int G = a.n_q_heads / a.n_kv_heads;
+        int s_cnt = 0, o_cnt = 0, tt = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit w = unit_at(a, reqs, n_blocks, u);
+            const int tt0 = tt;
+            tt += 2 * w.n_tiles;
+            const int nx = w.n_t[x];
+            if (nx == 0)
+                continue;
+            const int rr = w.row0[x] + r;          // packed row in the request
+            const bool row_ok = rr < w.m_rows;
+            const int t = row_ok ? rr / G : w.rq.q_len - 1;
+            const int g = row_ok ? rr - (rr / G) * G : 0;
+            const int pos = w.rq.prefix + t;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nx; ++j) {
+                if (!mbar_wait(bar(kBarSFull + x), s_cnt & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++s_cnt;
+                tc_fence_after();
+                float s[kTileN];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {          // chunk c (cols 8c..8c+7) with partner chunk c+8
-                uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
-                if (row_ok) {
-                    x = *reinterpret_cast<const uint4 *>(qp + 8 * c);
-                    y = *reinterpret_cast<const uint4 *>(qp + 64 + 8 * c);
-                    uint32_t *px = reinterpret_cast<uint32_t *>(&x);
-                    uint32_t *py = reinterpret_cast<uint32_t *>(&y);
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld32(lane_base + col_s(x) + 32 * q, s + 32 * q);
+                tmem_wait_ld();
+                // key 128j + c is visible to this row iff c < lim
+                const int lim = pos + 1 - j * kTileN;
+                if (lim < kTileN) {
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const float2 fx = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&px[w]));
-                        const float2 fy = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&py[w]));
-                        const float2 c0 = rope_cs(a.rope, kD / 2, pos, 8 * c + 2 * w);
-                        const float2 c1 = rope_cs(a.rope, kD / 2, pos, 8 * c + 2 * w + 1);
-                        __nv_bfloat162 ox = __floats2bfloat162_rn(fmaf(fx.x, c0.x, -fy.x * c0.y),
-                                                                  fmaf(fx.y, c1.x, -fy.y * c1.y));
-                        __nv_bfloat162 oy = __floats2bfloat162_rn(fmaf(fx.x, c0.y, fy.x * c0.x),
-                                                                  fmaf(fx.y, c1.y, fy.y * c1.x));
-                        px[w] = *reinterpret_cast<uint32_t *>(&ox);
-                        py[w] = *reinterpret_cast<uint32_t *>(&oy);
+                    for (int c = 0; c < kTileN; ++c)
+                        s[c] = (c < lim) ? s[c] : -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int c = 1; c < kTileN; ++c)
+                    mx = fmaxf(mx, s[c]);
+                const float mxs = mx * sc;
+                // lazy max: keep m_run unless this tile's max exceeds it by more than
+                // the threshold; O_x and l are rescaled after P_x is written (S is dead)
+                float corr = 1.f;
+                if (j == 0) {
+                    m_run = mxs;
+                } else if (mxs > m_run + kRescaleThreshold) {
+                    corr = ex2(m_run - mxs);
+                    m_run = mxs;
+                }
+                const float nm = -m_run;
+                float sum = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(s[32 * q + 2 * i], sc, nm));
+                        const float p1 = ex2(fmaf(s[32 * q + 2 * i + 1], sc, nm));
+                        sum += p0 + p1;
+                        pk[i] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(lane_base + col_s(x) + 16 * q, pk);
+                }
+                l_run = l_run * corr + sum;
+                if (corr != 1.f) {
+                    // the commit that signalled S_x(j) covers PV_x(j-1): O_x is stable
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float o[32];
+                        tmem_ld32(lane_base + col_o(x) + 32 * q, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] *= corr;
+                        tmem_st32(lane_base + col_o(x) + 32 * q, o);
                     }
                 }
-                *reinterpret_cast<uint4 *>(smem + kOffQ + sw128_off(r, c)) = x;
-                *reinterpret_cast<uint4 *>(smem + kOffQ + sw128_off(r, c + 8)) = y;
+                // last K/V tile of the unit: zero V rows past the block's data so
+                // that p = 0 never meets a non-finite value
+                if (j == w.n_tiles - 1 && j * kTileN + r >= w.n_valid) {
+                    const int tv = tt0 + 2 * j + 1;
+                    if (!mbar_wait(bar(kBarFull + tv % kSlots), (tv / kSlots) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *vt = smem + kOffKV + (tv % kSlots) * kTileBytes;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        *reinterpret_cast<uint4 *>(vt + sw128_off(r, c)) = make_uint4(0, 0, 0, 0);
+                    fence_async_smem();
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(kBarPFull + x));
             }
-            fence_async_smem();
-            mbar_arrive(bar(kBarQReady));
-        }
-
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_tiles && ok; ++j) {
-            const int sb = j & 1;
-            if (!mbar_wait(bar(kBarSFull + sb), (j >> 1) & 1, abort_flag)) {
-                flag_timeout(a.err, abort_flag);
+            if (!ok)
+                break;
+            // epilogue: O / l -> bf16 -> out[l][q_off + t][h*G + g][:]
+            if (!mbar_wait(bar(kBarOFull + x), o_cnt & 1, abort_flag)) {
                 ok = false;
                 break;
             }
+            ++o_cnt;
             tc_fence_after();
-            float s[kTileN];
+            float o[kD];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                tmem_ld32(lane_base + kColS + sb * kTileN + 32 * q, s + 32 * q);
+                tmem_ld32(lane_base + col_o(x) + 32 * q, o + 32 * q);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(bar(kBarSEmpty + sb));
-
-            // mask: key 128j + c is visible to this row iff it is <= P + t
-            const int lim = pos + 1 - j * kTileN;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kTileN; ++c) {
-                s[c] = (c < lim) ? s[c] * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[c]);
-            }
-            bool waited = false;
-            if (j == 0) {
-                m_run = mx;
-            } else if (mx > m_run + kRescaleThreshold) {
-                // O must hold PV_{j-1} before it is rescaled
-                if (!mbar_wait(bar(kBarODone), (j - 1) & 1, abort_flag)) {
-                    flag_timeout(a.err, abort_flag);
-                    ok = false;
-                    break;
-                }
-                waited = true;
-                tc_fence_after();
-                const float corr = ex2(m_run - mx);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float o[32];
-                    tmem_ld32(lane_base + kColO + 32 * q, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] *= corr;
-                    tmem_st32(lane_base + kColO + 32 * q, o);
-                }
-                tmem_wait_st();
-                l_run *= corr;
-                m_run = mx;
-            }
-            float sum = 0.f;
-#pragma unroll
-            for (int c = 0; c < kTileN; ++c) {
-                s[c] = ex2(s[c] - m_run);
-                sum += s[c];
-            }
-            l_run += sum;
-            // the P buffer is free once PV_{j-1} completed
-            if (j > 0 && !waited) {
-                if (!mbar_wait(bar(kBarODone), (j - 1) & 1, abort_flag)) {
-                    flag_timeout(a.err, abort_flag);
-                    ok = false;
-                    break;
-                }
-            }
-            // last tile: zero V rows past the block's data so that p = 0
-            // never meets a non-finite value
-            if (j == n_tiles - 1 && j * kTileN + r >= n_valid) {
-                const int tv = 2 * j + 1;
-                if (!mbar_wait(bar(kBarFull + tv % kSlots), (tv / kSlots) & 1, abort_flag)) {
-                    flag_timeout(a.err, abort_flag);
-                    ok = false;
-                    break;
-                }
-                uint8_t *vt = smem + kOffKV + (tv % kSlots) * kTileBytes;
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    *reinterpret_cast<uint4 *>(vt + sw128_off(r, c)) = make_uint4(0, 0, 0, 0);
-            }
-            uint8_t *pt = smem + kOffP;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint4 v;
-                uint32_t *pv = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(s[8 * c + 2 * w], s[8 * c + 2 * w + 1]);
-                    pv[w] = *reinterpret_cast<uint32_t *>(&b2);
-                }
-                *reinterpret_cast<uint4 *>(pt + sw128_off(r, c)) = v;
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(kBarPFull));
-        }
-        // epilogue: O / l -> bf16 -> out[l][q_off + t][h*G + g][:]
-        if (ok) {
-            if (!mbar_wait(bar(kBarODone), (n_tiles - 1) & 1, abort_flag)) {
-                flag_timeout(a.err, abort_flag);
-            } else {
-                tc_fence_after();
+            mbar_arrive(bar(kBarOEmpty + x));      // O_x may now take the next unit's PV
+            if (row_ok) {
                 const float inv = 1.f / l_run;
                 __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(a.out) +
-                                    (((int64_t)l * a.total_q + rq.q_off + t) * a.n_q_heads + h * G + g) * kD;
+                                    (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float o[32];
-                    tmem_ld32(lane_base + kColO + 32 * q, o);
-                    tmem_wait_ld();
-                    if (row_ok) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint4 v;
-                            uint32_t *pv = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * c + 2 * w] * inv,
-                                                                          o[8 * c + 2 * w + 1] * inv);
-                                pv[w] = *reinterpret_cast<uint32_t *>(&b2);
-                            }
-                            *reinterpret_cast<uint4 *>(op + 32 * q + 8 * c) = v;
-                        }
-                    }
+                for (int c = 0; c < 16; ++c) {
+                    uint4 v;
+                    v.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
+                    v.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                    v.z = pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                    v.w = pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                    *reinterpret_cast<uint4 *>(op + 8 * c) = v;
                 }
             }
         }
-    } else if (warp == 4) {
-        // =================== TMA producer ===================
+        if (!ok)
+            flag_timeout(a.err, abort_flag);
+    } else if (warp == 8) {
+        // =================== TMA producer: Q of each unit, then K_0, V_0, K_1, ... ===================
         if (lane == 0) {
-            int issued = 0;
-            for (int tt = 0; tt < 2 * n_tiles; ++tt) {
-                const int slot = tt % kSlots;
-                if (tt >= kSlots && !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag)) {
-                    flag_timeout(a.err, abort_flag);
+            int tt = 0, nq = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit w = unit_at(a, reqs, n_blocks, u);
+                if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
+                    ok = false;
                     break;
                 }
-                const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
-                const CUtensorMap *map = (tt & 1) ? &tmv : &tmk;
-                const int row = (int)(unit_row0 + (int64_t)(tt >> 1) * kTileN);
-                mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
-                tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
-                tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
-                issued = tt + 1;
-            }
-            // drain: every issued copy lands before the CTA leaves
-            for (int tt = (issued > kSlots ? issued - kSlots : 0); tt < issued; ++tt) {
-                uint64_t t0 = globaltimer();
-                while (!mbar_try_wait(bar(kBarFull + tt % kSlots), (tt / kSlots) & 1) &&
-                       globaltimer() - t0 < kWaitNs) {
+                const int nqt = w.n_t[1] > 0 ? 2 : 1;
+                mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
+                for (int x = 0; x < nqt; ++x) {
+                    const uint32_t dst = sbase + kOffQ + x * kTileBytes;
+                    tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
+                    tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
+                }
+                ++nq;
+                for (int i = 0; i < 2 * w.n_tiles; ++i, ++tt) {
+                    const int slot = tt % kSlots;
+                    if (tt >= kSlots && !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
+                    const CUtensorMap *map = (i & 1) ? &tmv : &tmk;
+                    const int row = (int)(w.kv_row0 + (int64_t)(i >> 1) * kTileN);
+                    mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
+                    tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
+                    tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
                 }
             }
+            if (!ok)
+                flag_timeout(a.err, abort_flag);
+            // drain: every issued copy lands before the CTA leaves
+            const uint64_t t0 = globaltimer();
+            for (int k = (tt > kSlots ? tt - kSlots : 0); k < tt; ++k)
+                while (!mbar_try_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1) &&
+                       globaltimer() - t0 < kWaitNs) {
+                }
+            if (nq > 0)
+                while (!mbar_try_wait(bar(kBarQFull), (nq - 1) & 1) && globaltimer() - t0 < kWaitNs) {
+                }
         }
     } else {
         // =================== MMA issuer ===================
         if (lane == 0) {
-            bool ok = mbar_wait(bar(kBarQReady), 0, abort_flag);
-            if (!ok)
-                flag_timeout(a.err, abort_flag);
-            tc_fence_after();
-            const uint32_t q_base = sbase + kOffQ, p_base = sbase + kOffP;
-            auto issue_s = [&](int j) -> bool {
-                const int tt = 2 * j, slot = tt % kSlots;
-                if (!mbar_wait(bar(kBarFull + slot), (tt / kSlots) & 1, abort_flag))
-                    return false;
-                if (j >= 2 && !mbar_wait(bar(kBarSEmpty + (j & 1)), ((j >> 1) - 1) & 1, abort_flag))
-                    return false;
-                tc_fence_after();
+            int tt = 0, nq = 0;
+            int p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
+            bool o_used[2] = {false, false};
+            bool ok = true;
+            const uint32_t q_base[2] = {sbase + kOffQ, sbase + kOffQ + kTileBytes};
+            // S_x = Q_x K^T with K in ring slot `slot`
+            auto issue_s = [&](int x, int slot) {
                 const uint32_t kb = sbase + kOffKV + slot * kTileBytes;
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
                     const uint32_t off = (k >> 2) * kPanelBytes + (k & 3) * 32;
-                    umma_f16(tmem + kColS + (j & 1) * kTileN, sdesc(q_base + off, 16, 1024),
-                             sdesc(kb + off, 16, 1024), kIdescS, k > 0);
+                    umma_f16(tmem + col_s(x), sdesc(q_base[x] + off, 16, 1024), sdesc(kb + off, 16, 1024),
+                             kIdescS, k > 0);
                 }
-                umma_commit(bar(kBarSFull + (j & 1)));
-                umma_commit(bar(kBarEmpty + slot));
+                umma_commit(bar(kBarSFull + x));
+            };
+            auto wait_kv = [&](int k) -> bool {
+                if (!mbar_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1, abort_flag))
+                    return false;
+                tc_fence_after();
                 return true;
             };
-            if (ok)
-                ok = issue_s(0);
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                if (j + 1 < n_tiles && !(ok = issue_s(j + 1)))
-                    break;
-                const int tt = 2 * j + 1, slot = tt % kSlots;
-                if (!mbar_wait(bar(kBarPFull), j & 1, abort_flag) ||
-                    !mbar_wait(bar(kBarFull + slot), (tt / kSlots) & 1, abort_flag)) {
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit w = unit_at(a, reqs, n_blocks, u);
+                if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag) || !wait_kv(tt)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t vb = sbase + kOffKV + slot * kTileBytes;
+                ++nq;
+                for (int x = 0; x < 2; ++x)
+                    if (w.n_t[x] > 0)
+                        issue_s(x, tt % kSlots);
+                if (w.n_tiles == 1)
+                    umma_commit(bar(kBarQEmpty));
+                umma_commit(bar(kBarEmpty + tt % kSlots));
+                for (int j = 0; j < w.n_tiles && ok; ++j) {
+                    const int tv = tt + 2 * j + 1, tk = tt + 2 * j + 2;
+                    const uint32_t vb = sbase + kOffKV + (tv % kSlots) * kTileBytes;
+                    bool v_ready = false, k_ready = false;
+                    for (int x = 0; x < 2; ++x) {
+                        if (j >= w.n_t[x])
+                            continue;
+                        if (!mbar_wait(bar(kBarPFull + x), p_cnt[x] & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        ++p_cnt[x];
+                        if (!v_ready && !(v_ready = wait_kv(tv))) {
+                            ok = false;
+                            break;
+                        }
+                        if (j == 0 && o_used[x]) {   // O_x still holds the last unit until read
+                            if (!mbar_wait(bar(kBarOEmpty + x), oe_cnt[x] & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            ++oe_cnt[x];
+                        }
+                        tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < kTileN / 16; ++k) {
-                    const uint32_t aoff = (k >> 2) * kPanelBytes + (k & 3) * 32;
-                    umma_f16(tmem + kColO, sdesc(p_base + aoff, 16, 1024),
-                             sdesc(vb + k * 2048, kPanelBytes, 1024), kIdescPV, (j > 0 || k > 0));
+                        for (int k = 0; k < kTileN / 16; ++k)
+                            umma_f16_ts(tmem + col_o(x), tmem + col_s(x) + 8 * k,
+                                        sdesc(vb + k * 2048, kPanelBytes, 1024), kIdescPV, (j > 0 || k > 0));
+                        if (j + 1 == w.n_t[x]) {
+                            umma_commit(bar(kBarOFull + x));
+                            o_used[x] = true;
+                        } else {
+                            if (!k_ready && !(k_ready = wait_kv(tk))) {
+                                ok = false;
+                                break;
+                            }
+                            issue_s(x, tk % kSlots);
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    if (k_ready && j + 2 == w.n_tiles)
+                        umma_commit(bar(kBarQEmpty));   // the unit's last S MMAs are issued
+                    umma_commit(bar(kBarEmpty + tv % kSlots));
+                    if (k_ready)
+                        umma_commit(bar(kBarEmpty + tk % kSlots));
                 }
-                umma_commit(bar(kBarEmpty + slot));
-                umma_commit(bar(kBarODone));
+                tt += 2 * w.n_tiles;
             }
             if (!ok)
                 flag_timeout(a.err, abort_flag);
             // drain: all issued MMAs complete before TMEM is released
             umma_commit(bar(kBarDrain));
-            uint64_t t0 = globaltimer();
+            const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(bar(kBarDrain), 0) && globaltimer() - t0 < kWaitNs) {
             }
         }
@@ -556,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -566,7 +664,7 @@ bool attention_tc_supported(int dtype, int head_dim) { return dtype == KVR_DTYPE
 
 cudaError_t launch_attention_tc(const TcAttnArgs &ta, cudaStream_t s)
 {
-    if (ta.n_m_tiles == 0)
+    if (ta.n_m_blocks == 0)
         return cudaSuccess;
     static bool attr_set = false;
     if (!attr_set) {
@@ -575,10 +673,14 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, cudaStream_t s)
             return e;
         attr_set = true;
     }
-    const int LH = ta.base.n_layers * ta.base.n_kv_heads;
-    dim3 grid(ta.n_m_tiles, LH);
-    k_attention_tc<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap *>(ta.tmap_k),
-                                                      *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base);
+    const int64_t units = (int64_t)ta.n_m_blocks * ta.base.n_layers * ta.base.n_kv_heads;
+    if (units > 0x7fffffff)
+        return cudaErrorInvalidValue;
+    const int grid = (int)(units < ta.n_sms ? units : ta.n_sms);
+    k_attention_tc<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap *>(ta.tmap_q),
+                                                      *static_cast<const CUtensorMap *>(ta.tmap_k),
+                                                      *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base,
+                                                      *ta.rt, ta.n_m_blocks);
     return cudaGetLastError();
 }
 

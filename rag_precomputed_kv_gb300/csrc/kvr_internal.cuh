@@ -63,7 +63,7 @@ struct alignas(16) DevReq {
     int32_t prefix;      // P_b
     int32_t q_off;       // first query token (token axis of q / out)
     int32_t q_len;       // Lq_b
-    int32_t m_tile0;     // first M-tile index of this request (tensor-core path)
+    int32_t m_block0;    // first 256-row block of this request (tensor-core path)
     int32_t pad;
 };
 
@@ -85,6 +85,20 @@ struct AssembleArgs {
     int32_t upc;                // (layer, head) units per CTA
 };
 
+// Span / local-source tables passed inside the kernel parameters (no upload)
+// when a call has at most kInlineEntries of each.
+constexpr int kInlineEntries = 64;
+struct AssembleTables {
+    DevSpan spans[kInlineEntries];
+    DevLocal locals[kInlineEntries];
+};
+
+// Request table passed inside the attention kernels' parameters when
+// batch <= kInlineEntries (AttnArgs::reqs is then NULL).
+struct ReqTable {
+    DevReq reqs[kInlineEntries];
+};
+
 struct AttnArgs {
     const DevReq *reqs;
     int32_t n_reqs;
@@ -99,21 +113,42 @@ struct AttnArgs {
     int *err;
 };
 
+struct QueryPrologueArgs {
+    const DevReq *reqs;         // NULL: the ReqTable parameter holds the requests
+    const float2 *rope;
+    const void *q;              // [L][T][Hq][D], not rotated
+    const void *kq;             // [L][T][Hkv][D], not rotated
+    const void *vq;
+    void *cache_k;
+    void *cache_v;
+    void *q_rot;                // out: [L][Hkv][T][G][D], rotated at P_b + t
+    int32_t n_layers, n_q_heads, n_kv_heads;
+    int32_t total_q;            // T
+};
+
 // ---- launchers (each returns the cudaGetLastError of its launch) ----
 cudaError_t launch_rope_tables(float2 *tab, int head_dim, double theta, cudaStream_t s);
+// `inl` (optional) carries the span and local tables; a.spans / a.locals are
+// then ignored.
 cudaError_t launch_assemble(const AssembleArgs &a, int dtype, int head_dim, int n_spans,
-                            cudaStream_t s);
-cudaError_t launch_attention_simt(const AttnArgs &a, int dtype, int head_dim, cudaStream_t s);
+                            cudaStream_t s, const AssembleTables *inl = nullptr);
+cudaError_t launch_attention_simt(const AttnArgs &a, const ReqTable &rt, int dtype, int head_dim,
+                                  cudaStream_t s);
 
 // Tensor-core attention (bf16, head_dim 128).  `tmaps` points to two
 // CUtensorMap objects (K then V) describing the cache as a 2-D
 // [rows, head_dim] bf16 tensor.
 struct TcAttnArgs {
     AttnArgs base;
-    const void *tmap_k;         // host CUtensorMap, passed by value to the kernel
+    const ReqTable *rt;         // used when base.reqs is NULL
+    const void *tmap_q;         // host CUtensorMaps, passed by value to the kernel:
+    const void *tmap_k;         //   rotated packed Q [L*Hkv*T*G, D], cache K and V [rows, D]
     const void *tmap_v;
-    int32_t n_m_tiles;          // total M-tiles over all requests
+    int32_t n_m_blocks;         // total 256-row query blocks over all requests
+    int32_t n_sms;              // persistent grid size bound
 };
+cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt, int n_reqs,
+                                  cudaStream_t s);
 cudaError_t launch_attention_tc(const TcAttnArgs &a, cudaStream_t s);
 bool attention_tc_supported(int dtype, int head_dim);
 

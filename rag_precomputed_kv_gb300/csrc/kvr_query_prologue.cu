@@ -1,0 +1,102 @@
+// kvr_query_prologue.cu -- the query side of the prefill, before attention.
+//
+// CoinRAG blog section 2.3: the query is the only part computed online,
+// KV_M(q; C_ctx), on top of the stitched prefix.  Query token t of request b
+// sits at position P_b + t (reordered, contiguous positions: TurboRAG blog,
+// "Position ID").  For every (request, layer, kv-head) this kernel
+//   * rotates the token's key by P_b + t and appends it, with its value, at
+//     row P_b + t of the cache block (so attention sees it like a prefix row);
+//   * rotates the G query heads of that kv head by the same angles and writes
+//     them packed as [layer][kv-head][token][G][head_dim] -- the 128-row tiles
+//     the tensor-core attention kernel loads with TMA are then contiguous.
+// Memory-bound: each query-side row is read once and written once.
+#include <cuda_bf16.h>
+
+#include "kvr_internal.cuh"
+
+namespace kvr {
+
+namespace {
+
+constexpr int kQpThreads = 256;
+
+__device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float *c, const float *s)
+{
+    uint32_t *pl = reinterpret_cast<uint32_t *>(&lo);
+    uint32_t *ph = reinterpret_cast<uint32_t *>(&hi);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&pl[w]));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&ph[w]));
+        const float c0 = c[2 * w], s0 = s[2 * w], c1 = c[2 * w + 1], s1 = s[2 * w + 1];
+        __nv_bfloat162 xo = __floats2bfloat162_rn(fmaf(x.x, c0, -y.x * s0), fmaf(x.y, c1, -y.y * s1));
+        __nv_bfloat162 yo = __floats2bfloat162_rn(fmaf(x.x, s0, y.x * c0), fmaf(x.y, s1, y.y * c1));
+        pl[w] = *reinterpret_cast<uint32_t *>(&xo);
+        ph[w] = *reinterpret_cast<uint32_t *>(&yo);
+    }
+}
+
+}  // namespace
+
+// One CTA per (request, layer, kv-head); 8 threads per token, thread j owns
+// elements [8j, 8j+8) and their RoPE partners [64 + 8j, ...).
+__global__ void __launch_bounds__(kQpThreads)
+    k_query_prologue(const __grid_constant__ QueryPrologueArgs a, const __grid_constant__ ReqTable rt)
+{
+    constexpr int D = 128, H2 = 64, E = 8, TPR = 8, RPP = kQpThreads / TPR;
+    const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
+    const DevReq rq = reqs[blockIdx.x];
+    const int lh = blockIdx.y;
+    const int l = lh / a.n_kv_heads, h = lh - l * a.n_kv_heads;
+    const int G = a.n_q_heads / a.n_kv_heads;
+    const int j = threadIdx.x % TPR;
+    const int64_t T = a.total_q;
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
+    const __nv_bfloat16 *kq = static_cast<const __nv_bfloat16 *>(a.kq);
+    const __nv_bfloat16 *vq = static_cast<const __nv_bfloat16 *>(a.vq);
+    __nv_bfloat16 *ck = static_cast<__nv_bfloat16 *>(a.cache_k);
+    __nv_bfloat16 *cv = static_cast<__nv_bfloat16 *>(a.cache_v);
+    __nv_bfloat16 *qr = static_cast<__nv_bfloat16 *>(a.q_rot);
+
+    for (int t = threadIdx.x / TPR; t < rq.q_len; t += RPP) {
+        const int64_t tok = rq.q_off + t;
+        float c[E], s[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float2 cs = rope_cs(a.rope, H2, rq.prefix + t, j * E + e);
+            c[e] = cs.x;
+            s[e] = cs.y;
+        }
+        const int64_t kv_src = ((l * T + tok) * a.n_kv_heads + h) * D + j * E;
+        uint4 klo = *reinterpret_cast<const uint4 *>(kq + kv_src);
+        uint4 khi = *reinterpret_cast<const uint4 *>(kq + kv_src + H2);
+        const uint4 vlo = *reinterpret_cast<const uint4 *>(vq + kv_src);
+        const uint4 vhi = *reinterpret_cast<const uint4 *>(vq + kv_src + H2);
+        rotate8(klo, khi, c, s);
+        const int64_t dst = (rq.cache_row0 + (int64_t)lh * rq.cap + rq.prefix + t) * D + j * E;
+        *reinterpret_cast<uint4 *>(ck + dst) = klo;
+        *reinterpret_cast<uint4 *>(ck + dst + H2) = khi;
+        *reinterpret_cast<uint4 *>(cv + dst) = vlo;
+        *reinterpret_cast<uint4 *>(cv + dst + H2) = vhi;
+        const int64_t q_src = ((l * T + tok) * a.n_q_heads + (int64_t)h * G) * D + j * E;
+        const int64_t q_dst = (((int64_t)lh * T + tok) * G) * D + j * E;
+        for (int g = 0; g < G; ++g) {
+            uint4 lo = *reinterpret_cast<const uint4 *>(q + q_src + (int64_t)g * D);
+            uint4 hi = *reinterpret_cast<const uint4 *>(q + q_src + (int64_t)g * D + H2);
+            rotate8(lo, hi, c, s);
+            *reinterpret_cast<uint4 *>(qr + q_dst + (int64_t)g * D) = lo;
+            *reinterpret_cast<uint4 *>(qr + q_dst + (int64_t)g * D + H2) = hi;
+        }
+    }
+}
+
+cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt, int n_reqs, cudaStream_t s)
+{
+    if (n_reqs == 0)
+        return cudaSuccess;
+    dim3 grid(n_reqs, a.n_layers * a.n_kv_heads);
+    k_query_prologue<<<grid, kQpThreads, 0, s>>>(a, rt);
+    return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -94,6 +94,24 @@ def test_inline_local_sources():
     _ok(run_parity_case(cfg=cfg, case=case))
 
 
+def test_large_batch_uses_uploaded_tables():
+    """More requests and spans than fit inside the kernel parameters: the span
+    and request tables travel through the staging upload instead."""
+    base = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, prompt_len=0, query_len=3)
+    rng = np.random.default_rng(5)
+    lists = []
+    for b in range(70):
+        rows = []
+        for _ in range(int(rng.integers(0, 3))):
+            c = int(rng.integers(0, base.n_chunks))
+            s0 = int(rng.integers(0, 90))
+            rows.append([c, s0, s0 + int(rng.integers(1, 7))])
+        lists.append(rows)
+    cfg, reqs = _custom(base, lists)
+    case = Case(cfg, reqs=reqs)
+    _ok(run_parity_case(cfg=cfg, case=case, requests=[0, 1, 33, 68, 69]))
+
+
 def test_repeat_calls_reuse_staging():
     """More calls than staging slots on one pool give the same results."""
     case = Case(W.CONFIGS[1])
