@@ -285,6 +285,40 @@ __device__ __forceinline__ void flag_timeout(int *err, volatile int *abort_flag)
 }
 
 
+// Packed fp32 pairs (two lanes of one 64-bit register) for the softmax.
+__device__ __forceinline__ uint64_t pk2(float a, float b)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void unpk2(uint64_t r, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -417,10 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < kTileN; ++c)
                         s[c] = (c < lim) ? s[c] : -INFINITY;
                 }
-                float mx = s[0];
+                float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                for (int c = 1; c < kTileN; ++c)
-                    mx = fmaxf(mx, s[c]);
+                for (int c = 4; c < kTileN; c += 8) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        m4[k] = max3(m4[k], s[c + 2 * k], s[c + 2 * k + 1]);
+                }
+                const float mx = max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
                 const float mxs = mx * sc;
                 // lazy max: keep m_run unless this tile's max exceeds it by more than
                 // the threshold; O_x and l are rescaled after P_x is written (S is dead)
@@ -432,18 +470,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_run = mxs;
                 }
                 const float nm = -m_run;
-                float sum = 0.f;
+                const uint64_t sc2 = pk2(sc, sc), nm2 = pk2(nm, nm);
+                uint64_t acc[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(s[32 * q + 2 * i], sc, nm));
-                        const float p1 = ex2(fmaf(s[32 * q + 2 * i + 1], sc, nm));
-                        sum += p0 + p1;
+                        float x0, x1;
+                        unpk2(fma2(pk2(s[32 * q + 2 * i], s[32 * q + 2 * i + 1]), sc2, nm2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        acc[i & 1] = add2(acc[i & 1], pk2(p0, p1));
                         pk[i] = pack_bf16(p0, p1);
                     }
                     tmem_st16(lane_base + col_s(x) + 16 * q, pk);
+                }
+                float sum;
+                {
+                    float a0, a1, b0, b1;
+                    unpk2(acc[0], a0, a1);
+                    unpk2(acc[1], b0, b1);
+                    sum = (a0 + a1) + (b0 + b1);
                 }
                 l_run = l_run * corr + sum;
                 if (corr != 1.f) {
@@ -458,20 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             o[i] *= corr;
                         tmem_st32(lane_base + col_o(x) + 32 * q, o);
                     }
-                }
-                // last K/V tile of the unit: zero V rows past the block's data so
-                // that p = 0 never meets a non-finite value
-                if (j == w.n_tiles - 1 && j * kTileN + r >= w.n_valid) {
-                    const int tv = tt0 + 2 * j + 1;
-                    if (!mbar_wait(bar(kBarFull + tv % kSlots), (tv / kSlots) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *vt = smem + kOffKV + (tv % kSlots) * kTileBytes;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        *reinterpret_cast<uint4 *>(vt + sw128_off(r, c)) = make_uint4(0, 0, 0, 0);
-                    fence_async_smem();
                 }
                 tmem_wait_st();
                 tc_fence_before();

@@ -8,7 +8,8 @@
 //     row P_b + t of the cache block (so attention sees it like a prefix row);
 //   * rotates the G query heads of that kv head by the same angles and writes
 //     them packed as [layer][kv-head][token][G][head_dim] -- the 128-row tiles
-//     the tensor-core attention kernel loads with TMA are then contiguous.
+//     the tensor-core attention kernel loads with TMA are then contiguous;
+//   * zeroes spare V rows up to the end of the block's last 128-key tile.
 // Memory-bound: each query-side row is read once and written once.
 #include <cuda_bf16.h>
 
@@ -87,6 +88,17 @@ __global__ void __launch_bounds__(kQpThreads)
             *reinterpret_cast<uint4 *>(qr + q_dst + (int64_t)g * D) = lo;
             *reinterpret_cast<uint4 *>(qr + q_dst + (int64_t)g * D + H2) = hi;
         }
+    }
+    // V rows between the block's data and the end of its last 128-row key
+    // tile (present only when the block has spare capacity) are zeroed, so
+    // that the attention kernel's masked keys (p = 0) never meet a non-finite
+    // value; rows past the block belong to the next, assembled, block.
+    const int n_valid = rq.prefix + rq.q_len;
+    const int pad_end = min(rq.cap, (n_valid + 127) / 128 * 128);
+    for (int row = n_valid + threadIdx.x / TPR; row < pad_end; row += RPP) {
+        const int64_t dst = (rq.cache_row0 + (int64_t)lh * rq.cap + row) * D + j * E;
+        *reinterpret_cast<uint4 *>(cv + dst) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(cv + dst + H2) = make_uint4(0, 0, 0, 0);
     }
 }
 

@@ -67,7 +67,8 @@ def attn_within_tolerance(gpu, ref, dtype):
 class Case:
     """Inputs, layout and GPU results of one configuration."""
 
-    def __init__(self, cfg: W.Config, device="cuda:0", prerotate=None, reqs=None, composite=False):
+    def __init__(self, cfg: W.Config, device="cuda:0", prerotate=None, reqs=None, composite=False,
+                 spare_rows=0):
         import torch
         from rag_precomputed_kv_gb300 import kvr
         self.cfg, self.device, self.composite = cfg, device, composite
@@ -103,7 +104,8 @@ class Case:
         self.span_offsets = np.concatenate([[0], np.cumsum([len(s) for s in spans])]).astype(np.int32)
         self.prefix = np.array([r.prefix_len for r in self.reqs], np.int64)
         lq = cfg.query_len
-        self.cache_offsets = np.concatenate([[0], np.cumsum(self.prefix + lq)]).astype(np.int64)
+        # cache blocks of P + Lq rows, plus `spare_rows` unused rows (left NaN)
+        self.cache_offsets = np.concatenate([[0], np.cumsum(self.prefix + lq + spare_rows)]).astype(np.int64)
         self.q_offsets = (np.arange(len(self.reqs) + 1) * lq).astype(np.int32)
         rows = int(self.cache_offsets[-1]) * self.LH
         tdt = self.t.pool_k.dtype

@@ -112,6 +112,17 @@ def test_large_batch_uses_uploaded_tables():
     _ok(run_parity_case(cfg=cfg, case=case, requests=[0, 1, 33, 68, 69]))
 
 
+@pytest.mark.parametrize("spare", [1, 37, 200])
+def test_cache_blocks_with_spare_rows(spare):
+    """Cache blocks larger than prefix + query, their spare rows left NaN:
+    masked keys must never pick up the garbage."""
+    cfg = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=21)
+    pid = cfg.n_chunks
+    cfg, reqs = _custom(cfg, [[[pid, 0, 5], [0, 3, 50]], [[1, 0, 96], [2, 7, 9]], []])
+    case = Case(cfg, reqs=reqs, spare_rows=spare)
+    _ok(run_parity_case(cfg=cfg, case=case))
+
+
 def test_repeat_calls_reuse_staging():
     """More calls than staging slots on one pool give the same results."""
     case = Case(W.CONFIGS[1])
