@@ -220,12 +220,15 @@ def run_kvr(args):
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
+    host = 0.0
     for k in range(args.steps):
         flush.zero_()
         wl.pool.set_timing_events(ev[k])
+        h0 = time.perf_counter()
         e0[k].record(stream)
         wl.step()
         e1[k].record(stream)
+        host += time.perf_counter() - h0
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
@@ -306,6 +309,7 @@ def run_kvr(args):
         "roofline": dominant, "roofline_other": other,
         "assemble_gbs": round(asm_gbs, 1), "attention_tflops": round(att_tf, 2),
         "append_ms": round(app_mean, 5),
+        "host_ms_per_step": round(host * 1e3 / args.steps, 5),
         "latency_ms": {"p50": round(lat[len(lat) // 2], 5), "p99": round(lat[min(len(lat) - 1, int(0.99 * len(lat)))], 5),
                        "what": "one step (assemble + query attention) per batch, device time"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

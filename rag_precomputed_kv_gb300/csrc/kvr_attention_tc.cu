@@ -158,7 +158,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
@@ -172,32 +171,10 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 // 16 consecutive 32-bit columns of this thread's TMEM lane.
@@ -208,6 +185,38 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
         "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+// MMA issue with precomputed descriptors: a descriptor's address field is in
+// its low word, so a K-step or a ring slot only adds to the low word (the
+// issuing thread shares its SM sub-partition with two softmax warps, so every
+// instruction it saves shortens the tensor pipe's wait for work).
+__device__ __forceinline__ uint64_t desc_with_lo(uint32_t lo, uint32_t hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
+template <bool ACC>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "n"(ACC ? 1 : 0)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -271,12 +280,6 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 
-// Byte offset of 16-byte chunk `c` (0..15 over 128 columns) of row r in a
-// [128 rows x 128 bf16] tile stored as two 128B-swizzled 64-column panels.
-__device__ __forceinline__ uint32_t sw128_off(int r, int c)
-{
-    return (uint32_t)((c >> 3) * kPanelBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
 
 __device__ __forceinline__ void flag_timeout(int *err, volatile int *abort_flag)
 {
@@ -421,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit w = unit_at(a, reqs, n_blocks, u);
-            const int tt0 = tt;
             tt += 2 * w.n_tiles;
             const int nx = w.n_t[x];
             if (nx == 0)
@@ -595,15 +597,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             int p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
             bool o_used[2] = {false, false};
             bool ok = true;
-            const uint32_t q_base[2] = {sbase + kOffQ, sbase + kOffQ + kTileBytes};
+            // descriptors: K-major 128B-swizzled tiles (Q, K) and the MN-major V tile
+            const uint64_t d_k_major = sdesc(sbase, 16, 1024);
+            const uint64_t d_mn_major = sdesc(sbase, kPanelBytes, 1024);
+            const uint32_t lo_k = (uint32_t)d_k_major, hi_k = (uint32_t)(d_k_major >> 32);
+            const uint32_t lo_v = (uint32_t)d_mn_major, hi_v = (uint32_t)(d_mn_major >> 32);
             // S_x = Q_x K^T with K in ring slot `slot`
             auto issue_s = [&](int x, int slot) {
-                const uint32_t kb = sbase + kOffKV + slot * kTileBytes;
+                const uint32_t qa = lo_k + ((kOffQ + x * kTileBytes) >> 4);
+                const uint32_t kb = lo_k + ((kOffKV + slot * kTileBytes) >> 4);
+                const uint32_t d = tmem + col_s(x);
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kPanelBytes + (k & 3) * 32;
-                    umma_f16(tmem + col_s(x), sdesc(q_base[x] + off, 16, 1024), sdesc(kb + off, 16, 1024),
-                             kIdescS, k > 0);
+                    const uint32_t off = ((k >> 2) * kPanelBytes + (k & 3) * 32) >> 4;
+                    if (k == 0)
+                        mma_ss<false>(d, desc_with_lo(qa + off, hi_k), desc_with_lo(kb + off, hi_k), kIdescS);
+                    else
+                        mma_ss<true>(d, desc_with_lo(qa + off, hi_k), desc_with_lo(kb + off, hi_k), kIdescS);
                 }
                 umma_commit(bar(kBarSFull + x));
             };
@@ -628,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(bar(kBarEmpty + tt % kSlots));
                 for (int j = 0; j < w.n_tiles && ok; ++j) {
                     const int tv = tt + 2 * j + 1, tk = tt + 2 * j + 2;
-                    const uint32_t vb = sbase + kOffKV + (tv % kSlots) * kTileBytes;
+                    const uint32_t vb = lo_v + ((kOffKV + (tv % kSlots) * kTileBytes) >> 4);
                     bool v_ready = false, k_ready = false;
                     for (int x = 0; x < 2; ++x) {
                         if (j >= w.n_t[x])
@@ -650,10 +660,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ++oe_cnt[x];
                         }
                         tc_fence_after();
+                        const uint32_t d = tmem + col_o(x), pa = tmem + col_s(x);
+                        const uint32_t acc0 = j > 0;
 #pragma unroll
                         for (int k = 0; k < kTileN / 16; ++k)
-                            umma_f16_ts(tmem + col_o(x), tmem + col_s(x) + 8 * k,
-                                        sdesc(vb + k * 2048, kPanelBytes, 1024), kIdescPV, (j > 0 || k > 0));
+                            mma_ts(d, pa + 8 * k, desc_with_lo(vb + ((k * 2048) >> 4), hi_v), kIdescPV,
+                                   k > 0 ? 1u : acc0);
                         if (j + 1 == w.n_t[x]) {
                             umma_commit(bar(kBarOFull + x));
                             o_used[x] = true;
