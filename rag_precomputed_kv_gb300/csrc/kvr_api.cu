@@ -641,7 +641,10 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
         // the previous call's attention must be done with the query scratch
         if (p->q_rot_used && (e = cudaStreamWaitEvent(s, p->q_rot_done, 0)) != cudaSuccess)
             return cuda_fail(e, "query scratch ordering");
-        QueryPrologueArgs qp{at.reqs, p->rope, q, kq, vq, cache_k, cache_v, p->q_rot, L, Hq, Hkv, T};
+        int32_t max_lq = 0;
+        for (int b = 0; b < batch; ++b)
+            max_lq = std::max(max_lq, q_offsets[b + 1] - q_offsets[b]);
+        QueryPrologueArgs qp{at.reqs, p->rope, q, kq, vq, cache_k, cache_v, p->q_rot, L, Hq, Hkv, T, max_lq};
         p->mark(2, s);
         e = launch_query_prologue(qp, rt, batch, s);
         p->mark(3, s);

@@ -124,6 +124,7 @@ struct QueryPrologueArgs {
     void *q_rot;                // out: [L][Hkv][T][G][D], rotated at P_b + t
     int32_t n_layers, n_q_heads, n_kv_heads;
     int32_t total_q;            // T
+    int32_t max_q_len;          // longest query of the batch
 };
 
 // ---- launchers (each returns the cudaGetLastError of its launch) ----

@@ -19,7 +19,8 @@ namespace kvr {
 
 namespace {
 
-constexpr int kQpThreads = 256;
+constexpr int kQpTokens = 16;                 // query tokens per CTA
+constexpr int kQpThreads = 8 * kQpTokens;     // 8 threads per token
 
 __device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float *c, const float *s)
 {
@@ -39,14 +40,18 @@ __device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float *c, co
 
 }  // namespace
 
-// One CTA per (request, layer, kv-head); 8 threads per token, thread j owns
-// elements [8j, 8j+8) and their RoPE partners [64 + 8j, ...).
+// One CTA per (request, 16-token chunk of its query, layer, kv-head); 8
+// threads per token, thread j owns elements [8j, 8j+8) and their RoPE
+// partners [64 + 8j, ...).
 __global__ void __launch_bounds__(kQpThreads)
     k_query_prologue(const __grid_constant__ QueryPrologueArgs a, const __grid_constant__ ReqTable rt)
 {
     constexpr int D = 128, H2 = 64, E = 8, TPR = 8, RPP = kQpThreads / TPR;
     const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
-    const DevReq rq = reqs[blockIdx.x];
+    const int n_chunks = (a.max_q_len + kQpTokens - 1) / kQpTokens;
+    const int chunk = blockIdx.x % n_chunks;
+    const DevReq rq = reqs[blockIdx.x / n_chunks];
+    const int t_end = min(rq.q_len, (chunk + 1) * kQpTokens);
     const int lh = blockIdx.y;
     const int l = lh / a.n_kv_heads, h = lh - l * a.n_kv_heads;
     const int G = a.n_q_heads / a.n_kv_heads;
@@ -59,7 +64,7 @@ __global__ void __launch_bounds__(kQpThreads)
     __nv_bfloat16 *cv = static_cast<__nv_bfloat16 *>(a.cache_v);
     __nv_bfloat16 *qr = static_cast<__nv_bfloat16 *>(a.q_rot);
 
-    for (int t = threadIdx.x / TPR; t < rq.q_len; t += RPP) {
+    for (int t = chunk * kQpTokens + threadIdx.x / TPR; t < t_end; t += RPP) {
         const int64_t tok = rq.q_off + t;
         float c[E], s[E];
 #pragma unroll
@@ -94,7 +99,7 @@ __global__ void __launch_bounds__(kQpThreads)
     // that the attention kernel's masked keys (p = 0) never meet a non-finite
     // value; rows past the block belong to the next, assembled, block.
     const int n_valid = rq.prefix + rq.q_len;
-    const int pad_end = min(rq.cap, (n_valid + 127) / 128 * 128);
+    const int pad_end = chunk == 0 ? min(rq.cap, (n_valid + 127) / 128 * 128) : 0;
     for (int row = n_valid + threadIdx.x / TPR; row < pad_end; row += RPP) {
         const int64_t dst = (rq.cache_row0 + (int64_t)lh * rq.cap + row) * D + j * E;
         *reinterpret_cast<uint4 *>(cv + dst) = make_uint4(0, 0, 0, 0);
@@ -106,7 +111,12 @@ cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt
 {
     if (n_reqs == 0)
         return cudaSuccess;
-    dim3 grid(n_reqs, a.n_layers * a.n_kv_heads);
+    const int64_t n_chunks = (a.max_q_len + kQpTokens - 1) / kQpTokens;
+    if (n_chunks == 0)
+        return cudaSuccess;
+    if (n_reqs * n_chunks > 0x7fffffff)
+        return cudaErrorInvalidValue;
+    dim3 grid((unsigned)(n_reqs * n_chunks), a.n_layers * a.n_kv_heads);
     k_query_prologue<<<grid, kQpThreads, 0, s>>>(a, rt);
     return cudaGetLastError();
 }
