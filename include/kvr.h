@@ -192,6 +192,31 @@ KVR_API kvr_status kvr_query_attention(kvr_pool_t pool, int32_t batch, const int
                                void *cache_k, void *cache_v, void *out,
                                float softmax_scale, void *stream);
 
+/*
+ * kvr_prefill -- the whole precomputed-KV prefill in one call: kvr_assemble
+ * followed by kvr_query_attention with P_b taken from the stitch
+ * (CoinRAG blog section 2.3: KV_CoinRAG = C_ctx stitched from stored chunks,
+ * then KV_M(q; C_ctx) computed online).  Arguments mean what they mean in
+ * those two calls (cache_k / cache_v and cache_offsets are shared; the
+ * blocks must hold P_b + Lq_b rows); prefix_len is an optional host output.
+ * Results are identical, bit for bit, to the two calls in a row.
+ *
+ * The difference is scheduling: every check of both halves runs before
+ * anything is enqueued, the table uploads go first, and the kernels follow
+ * one another on the stream with programmatic dependent launch, so the
+ * query-side kernel (rotation and append of the query tokens, which touches
+ * no prefix row) runs alongside the stitch, and the attention kernel's setup
+ * overlaps it.  The timing hook (kvr_set_timing_events) serializes them.
+ * Errors: those of the two calls; nothing is enqueued when a check fails.
+ */
+KVR_API kvr_status kvr_prefill(kvr_pool_t pool, int32_t batch, const int32_t *span_offsets,
+                               const kvr_span *spans, const kvr_local_src *locals, int32_t n_locals,
+                               const int64_t *cache_offsets, void *cache_k, void *cache_v,
+                               int32_t *pos_ids, int32_t *src_map, int32_t *prefix_len,
+                               uint32_t flags, const int32_t *q_offsets, const void *q,
+                               const void *kq, const void *vq, void *out, float softmax_scale,
+                               void *stream);
+
 /* Attention kernels a pool can select (kvr_attention_path). */
 enum { KVR_PATH_UNBOUND = -1, KVR_PATH_CUDA_CORES = 0, KVR_PATH_TCGEN05 = 1 };
 

@@ -308,18 +308,26 @@ int units_per_cta(int LH, int64_t rows, int64_t n_spans)
 
 }  // namespace
 
-extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *span_offsets,
-                                   const kvr_span *spans, const kvr_local_src *locals,
-                                   int32_t n_locals, const int64_t *cache_offsets, void *cache_k,
-                                   void *cache_v, int32_t *pos_ids, int32_t *src_map,
-                                   int32_t *prefix_len, uint32_t flags, void *stream)
+// One assemble call, validated (host tables built), then staged (device
+// tables in kernel parameters or uploaded), then launched.
+struct AsmPlan {
+    std::vector<DevSpan> ds;
+    std::vector<int32_t> plen;
+    int64_t flat = 0;
+    const kvr_local_src *locals = nullptr;
+    int32_t n_locals = 0;
+    void *cache_k = nullptr, *cache_v = nullptr;
+    int32_t *pos_ids = nullptr, *src_map = nullptr;
+    AssembleArgs a{};
+    bool inl = false;
+    AssembleTables tab;
+    Slot *slot = nullptr;
+};
+
+static kvr_status asm_validate(const kvr_pool &p, int32_t batch, const int32_t *span_offsets,
+                               const kvr_span *spans, const kvr_local_src *locals, int32_t n_locals,
+                               const int64_t *cache_offsets, uint32_t flags, AsmPlan &pl)
 {
-    if (!p)
-        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
-    if (batch < 0)
-        return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
-    if (batch == 0)
-        return KVR_OK;
     if (flags & ~KVR_POSITIONS_COMPOSITE)
         return fail(KVR_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     kvr_status st;
@@ -332,14 +340,15 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
     if (n_locals < 0 || (n_locals > 0 && !locals))
         return fail(KVR_ERR_INVALID_ARG, "locals NULL with n_locals %d", n_locals);
     for (int i = 0; i < n_locals; ++i)
-        if ((st = check_local(*p, locals[i], i)) != KVR_OK)
+        if ((st = check_local(p, locals[i], i)) != KVR_OK)
             return st;
     const bool composite = flags & KVR_POSITIONS_COMPOSITE;
-    const int LH = p->d.n_layers * p->d.n_kv_heads;
+    const int LH = p.d.n_layers * p.d.n_kv_heads;
 
-    std::vector<DevSpan> ds;
-    ds.reserve(n_spans);
-    std::vector<int32_t> plen(batch);
+    pl.locals = locals;
+    pl.n_locals = n_locals;
+    pl.ds.reserve(n_spans);
+    pl.plen.assign(batch, 0);
     int64_t flat = 0;
     for (int b = 0; b < batch; ++b) {
         const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
@@ -356,10 +365,10 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
                                 n_locals);
                 src_len = locals[idx].len;
             } else {
-                if (s.src >= p->d.n_entries)
+                if (s.src >= p.d.n_entries)
                     return fail(KVR_ERR_OUT_OF_RANGE, "span %d: pool entry %d of %lld", i, s.src,
-                                (long long)p->d.n_entries);
-                src_len = p->d.entry_len;
+                                (long long)p.d.n_entries);
+                src_len = p.d.entry_len;
             }
             if (s.start < 0 || s.end < s.start || s.end > src_len)
                 return fail(KVR_ERR_OUT_OF_RANGE, "span %d: [%d, %d) outside source of %lld tokens",
@@ -380,7 +389,7 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
                 d.delta = (int32_t)(pos0 - s.start);
                 d.cap = (int32_t)cap;
                 d.dstep = 0;
-                ds.push_back(d);
+                pl.ds.push_back(d);
             }
             row += len;
             flat += len;
@@ -388,20 +397,30 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
         if (row > cap)
             return fail(KVR_ERR_OUT_OF_RANGE, "request %d: prefix %lld rows > cache block %lld", b,
                         (long long)row, (long long)cap);
-        plen[b] = (int32_t)row;
+        pl.plen[b] = (int32_t)row;
     }
-    if (prefix_len)
-        std::copy(plen.begin(), plen.end(), prefix_len);
-    if (ds.empty())
-        return KVR_OK;
+    pl.flat = flat;
+    return KVR_OK;
+}
+
+static kvr_status asm_check_outputs(AsmPlan &pl, void *cache_k, void *cache_v, int32_t *pos_ids,
+                                    int32_t *src_map)
+{
     if (!cache_k || !cache_v || !aligned16(cache_k) || !aligned16(cache_v))
         return fail(KVR_ERR_INVALID_ARG, "cache_k / cache_v NULL or not 16-byte aligned");
-    if ((st = ensure_device(p)) != KVR_OK)
-        return st;
+    pl.cache_k = cache_k;
+    pl.cache_v = cache_v;
+    pl.pos_ids = pos_ids;
+    pl.src_map = src_map;
+    return KVR_OK;
+}
 
-    DeviceGuard g(p->device);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    AssembleArgs a{};
+// Kernel arguments and tables; large tables go up by one H2D copy from a
+// pinned staging slot.  Device setup must be done.
+static kvr_status asm_stage(kvr_pool *p, AsmPlan &pl, cudaStream_t s)
+{
+    const int LH = p->d.n_layers * p->d.n_kv_heads;
+    AssembleArgs &a = pl.a;
     a.rope = p->rope;
     a.pool_k = p->d.k;
     a.pool_v = p->d.v;
@@ -409,52 +428,91 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
     a.ps_layer = p->d.stride[1];
     a.ps_head = p->d.stride[2];
     a.ps_tok = p->d.stride[3];
-    a.cache_k = cache_k;
-    a.cache_v = cache_v;
-    a.pos_ids = pos_ids;
-    a.src_map = src_map;
+    a.cache_k = pl.cache_k;
+    a.cache_v = pl.cache_v;
+    a.pos_ids = pl.pos_ids;
+    a.src_map = pl.src_map;
     a.n_layers = p->d.n_layers;
     a.n_heads = p->d.n_kv_heads;
-    a.upc = units_per_cta(LH, flat, (int64_t)ds.size());
-    cudaError_t e;
-    if ((int)ds.size() <= kInlineEntries && n_locals <= kInlineEntries) {
+    a.upc = units_per_cta(LH, pl.flat, (int64_t)pl.ds.size());
+    const int n_locals = pl.n_locals;
+    const kvr_local_src *locals = pl.locals;
+    pl.inl = (int)pl.ds.size() <= kInlineEntries && n_locals <= kInlineEntries;
+    if (pl.inl) {
         // small call: the tables travel inside the kernel parameters
-        AssembleTables tab;
-        std::memcpy(tab.spans, ds.data(), ds.size() * sizeof(DevSpan));
+        std::memcpy(pl.tab.spans, pl.ds.data(), pl.ds.size() * sizeof(DevSpan));
         for (int i = 0; i < n_locals; ++i)
-            tab.locals[i] = DevLocal{locals[i].k, locals[i].v, locals[i].stride[0], locals[i].stride[1],
-                                     locals[i].stride[2], locals[i].len};
-        p->mark(0, s);
-        e = launch_assemble(a, p->d.dtype, p->d.head_dim, (int)ds.size(), s, &tab);
-        p->mark(1, s);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "assemble launch");
+            pl.tab.locals[i] = DevLocal{locals[i].k, locals[i].v, locals[i].stride[0], locals[i].stride[1],
+                                        locals[i].stride[2], locals[i].len};
         return KVR_OK;
     }
-    const size_t off_loc = align16(ds.size() * sizeof(DevSpan));
+    const size_t off_loc = align16(pl.ds.size() * sizeof(DevSpan));
     const size_t bytes = off_loc + sizeof(DevLocal) * std::max(n_locals, 0);
-    Slot *slot;
-    if ((st = p->acquire(bytes, bytes, &slot)) != KVR_OK)
+    kvr_status st;
+    if ((st = p->acquire(bytes, bytes, &pl.slot)) != KVR_OK)
         return st;
-    char *h = static_cast<char *>(slot->host);
-    std::memcpy(h, ds.data(), ds.size() * sizeof(DevSpan));
+    char *h = static_cast<char *>(pl.slot->host);
+    std::memcpy(h, pl.ds.data(), pl.ds.size() * sizeof(DevSpan));
     for (int i = 0; i < n_locals; ++i) {
         DevLocal l{locals[i].k, locals[i].v, locals[i].stride[0], locals[i].stride[1],
                    locals[i].stride[2], locals[i].len};
         std::memcpy(h + off_loc + i * sizeof(DevLocal), &l, sizeof l);
     }
-    if ((e = cudaMemcpyAsync(slot->dev, h, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    cudaError_t e = cudaMemcpyAsync(pl.slot->dev, h, bytes, cudaMemcpyHostToDevice, s);
+    cudaEventRecord(pl.slot->done, s);   // the slot is busy from here on
+    pl.slot->used = true;
+    if (e != cudaSuccess)
         return cuda_fail(e, "span table upload");
-    a.spans = static_cast<const DevSpan *>(slot->dev);
-    a.locals = reinterpret_cast<const DevLocal *>(static_cast<char *>(slot->dev) + off_loc);
+    a.spans = static_cast<const DevSpan *>(pl.slot->dev);
+    a.locals = reinterpret_cast<const DevLocal *>(static_cast<char *>(pl.slot->dev) + off_loc);
+    return KVR_OK;
+}
+
+// `record_slot` false: the caller records the staging slot's event after the
+// kernels that follow (nothing may sit between this kernel and a dependent
+// launched programmatically after it).
+static kvr_status asm_launch(kvr_pool *p, AsmPlan &pl, cudaStream_t s, bool record_slot = true)
+{
     p->mark(0, s);
-    e = launch_assemble(a, p->d.dtype, p->d.head_dim, (int)ds.size(), s);
+    cudaError_t e = launch_assemble(pl.a, p->d.dtype, p->d.head_dim, (int)pl.ds.size(), s,
+                                    pl.inl ? &pl.tab : nullptr);
     p->mark(1, s);
-    cudaEventRecord(slot->done, s);
-    slot->used = true;
+    if (pl.slot && record_slot)
+        cudaEventRecord(pl.slot->done, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "assemble launch");
     return KVR_OK;
+}
+
+extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *span_offsets,
+                                   const kvr_span *spans, const kvr_local_src *locals,
+                                   int32_t n_locals, const int64_t *cache_offsets, void *cache_k,
+                                   void *cache_v, int32_t *pos_ids, int32_t *src_map,
+                                   int32_t *prefix_len, uint32_t flags, void *stream)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    if (batch < 0)
+        return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
+    if (batch == 0)
+        return KVR_OK;
+    AsmPlan pl;
+    kvr_status st;
+    if ((st = asm_validate(*p, batch, span_offsets, spans, locals, n_locals, cache_offsets, flags,
+                           pl)) != KVR_OK)
+        return st;
+    if (prefix_len)
+        std::copy(pl.plen.begin(), pl.plen.end(), prefix_len);
+    if (pl.ds.empty())
+        return KVR_OK;
+    if ((st = asm_check_outputs(pl, cache_k, cache_v, pos_ids, src_map)) != KVR_OK ||
+        (st = ensure_device(p)) != KVR_OK)
+        return st;
+    DeviceGuard g(p->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = asm_stage(p, pl, s)) != KVR_OK)
+        return st;
+    return asm_launch(p, pl, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -480,18 +538,32 @@ kvr_status encode_cache_map(const kvr_pool &p, void *base, int64_t rows, CUtenso
 
 }  // namespace
 
-extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int64_t *cache_offsets,
-                                          const int32_t *prefix_len, const int32_t *q_offsets,
-                                          const void *q, const void *kq, const void *vq,
-                                          void *cache_k, void *cache_v, void *out,
-                                          float softmax_scale, void *stream)
+// One query-attention call, validated, staged, launched (as the assemble).
+struct QaPlan {
+    int32_t batch = 0, T = 0, m_blocks = 0, max_lq = 0;
+    const int64_t *cache_offsets = nullptr;
+    const int32_t *q_offsets = nullptr;
+    const void *q = nullptr, *kq = nullptr, *vq = nullptr;
+    void *cache_k = nullptr, *cache_v = nullptr, *out = nullptr;
+    float scale = 0.f;
+    std::vector<DevReq> rq;
+    std::vector<DevSpan> ap;     // the query keys / values as append spans (CUDA-core path)
+    std::vector<DevLocal> al;
+    bool tc = false, inl = false;
+    CUtensorMap mq, mk, mv;
+    ReqTable rt_inl;
+    AssembleTables tab;
+    AssembleArgs a{};
+    AttnArgs at{};
+    Slot *slot = nullptr;
+};
+
+// Host checks and tables.  T = 0 (no query token) leaves nothing to do.
+static kvr_status qa_validate(const kvr_pool &p, int32_t batch, const int64_t *cache_offsets,
+                              const int32_t *prefix_len, const int32_t *q_offsets, const void *q,
+                              const void *kq, const void *vq, void *cache_k, void *cache_v, void *out,
+                              float softmax_scale, QaPlan &pl)
 {
-    if (!p)
-        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
-    if (batch < 0)
-        return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
-    if (batch == 0)
-        return KVR_OK;
     kvr_status st;
     if ((st = check_cache_offsets(cache_offsets, batch)) != KVR_OK ||
         (st = check_offsets32(q_offsets, batch, "q_offsets")) != KVR_OK)
@@ -500,21 +572,13 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
         return fail(KVR_ERR_INVALID_ARG, "prefix_len is NULL");
     if (!(softmax_scale >= 0.f) || !std::isfinite(softmax_scale))
         return fail(KVR_ERR_INVALID_ARG, "softmax_scale %g", (double)softmax_scale);
-    const int32_t T = q_offsets[batch];
-    if (T == 0)
+    pl.T = q_offsets[batch];
+    if (pl.T == 0)
         return KVR_OK;
     const void *ptrs[] = {q, kq, vq, cache_k, cache_v, out};
     for (const void *x : ptrs)
         if (!x || !aligned16(x))
             return fail(KVR_ERR_INVALID_ARG, "q / kq / vq / cache / out NULL or not 16-byte aligned");
-
-    const int L = p->d.n_layers, Hkv = p->d.n_kv_heads, Hq = p->d.n_q_heads, D = p->d.head_dim;
-    const int LH = L * Hkv;
-    const int G = Hq / Hkv;
-    std::vector<DevReq> rq(batch);
-    std::vector<DevSpan> ap;
-    std::vector<DevLocal> al;
-    int32_t m_blocks = 0;
     for (int b = 0; b < batch; ++b) {
         const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
         const int32_t P = prefix_len[b];
@@ -523,28 +587,42 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
             return fail(KVR_ERR_OUT_OF_RANGE, "request %d: prefix %d + query %d > cache block %lld",
                         b, P, Lq, (long long)cap);
     }
-    if ((st = ensure_device(p)) != KVR_OK)
-        return st;
-    const bool tc = use_tensor_cores(*p);
+    pl.batch = batch;
+    pl.cache_offsets = cache_offsets;
+    pl.q_offsets = q_offsets;
+    pl.q = q;
+    pl.kq = kq;
+    pl.vq = vq;
+    pl.cache_k = cache_k;
+    pl.cache_v = cache_v;
+    pl.out = out;
+    pl.scale = softmax_scale;
+
+    const int L = p.d.n_layers, Hkv = p.d.n_kv_heads, Hq = p.d.n_q_heads, D = p.d.head_dim;
+    const int LH = L * Hkv;
+    const int G = Hq / Hkv;
+    const int64_t T = pl.T;
+    pl.rq.resize(batch);
     for (int b = 0; b < batch; ++b) {
         const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
         const int32_t P = prefix_len[b];
         const int32_t Lq = q_offsets[b + 1] - q_offsets[b];
-        DevReq &r = rq[b];
+        pl.max_lq = std::max(pl.max_lq, Lq);
+        DevReq &r = pl.rq[b];
         r.cache_row0 = cache_offsets[b] * LH;
         r.cap = (int32_t)cap;
         r.prefix = P;
         r.q_off = q_offsets[b];
         r.q_len = Lq;
-        r.m_block0 = m_blocks;
-        m_blocks += (int32_t)((int64_t(G) * Lq + 255) / 256);
+        r.m_block0 = pl.m_blocks;
+        pl.m_blocks += (int32_t)((int64_t(G) * Lq + 255) / 256);
         if (Lq > 0) {
             // the query tokens' keys / values become cache rows P..P+Lq-1;
             // their keys arrive un-rotated, so token t turns by P + t
             DevSpan d{};
             d.dst_row0 = r.cache_row0;
             d.flat0 = 0;
-            d.src = KVR_SRC_LOCAL | (int32_t)al.size();
+            d.src = KVR_SRC_LOCAL | (int32_t)pl.al.size();
             d.start = 0;
             d.len = Lq;
             d.row = P;
@@ -552,23 +630,28 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
             d.delta = P;
             d.cap = (int32_t)cap;
             d.dstep = 1;
-            ap.push_back(d);
-            const int64_t off = (int64_t)q_offsets[b] * Hkv * D * p->elt();
+            pl.ap.push_back(d);
+            const int64_t off = (int64_t)q_offsets[b] * Hkv * D * p.elt();
             DevLocal l{static_cast<const char *>(kq) + off, static_cast<const char *>(vq) + off,
-                       (int64_t)T * Hkv * D, D, (int64_t)Hkv * D, Lq};
-            al.push_back(l);
+                       T * Hkv * D, D, (int64_t)Hkv * D, Lq};
+            pl.al.push_back(l);
         }
     }
+    return KVR_OK;
+}
 
-    DeviceGuard g(p->device);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaSuccess;
-
-    // tensor-core path: rotated packed Q scratch and the three tensor maps,
-    // set up before anything is enqueued
-    CUtensorMap mq, mk, mv;
-    if (tc) {
-        const int64_t rows = cache_offsets[batch] * LH;
+// Scratch, tensor maps and tables.  Device setup must be done.
+static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
+{
+    const int L = p->d.n_layers, Hkv = p->d.n_kv_heads, Hq = p->d.n_q_heads, D = p->d.head_dim;
+    const int LH = L * Hkv;
+    const int32_t batch = pl.batch, T = pl.T;
+    kvr_status st;
+    cudaError_t e;
+    pl.tc = use_tensor_cores(*p);
+    if (pl.tc) {
+        // rotated packed Q scratch and the three tensor maps
+        const int64_t rows = pl.cache_offsets[batch] * LH;
         const int64_t q_rows = (int64_t)L * T * Hq;
         if (rows > (int64_t)INT32_MAX - 256 || q_rows > (int64_t)INT32_MAX - 256)   // int32 TMA coordinates
             return fail(KVR_ERR_UNSUPPORTED, "cache or query rows exceed the int32 TMA coordinate range");
@@ -587,101 +670,188 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
         }
         if (!p->q_rot_done && (e = cudaEventCreateWithFlags(&p->q_rot_done, cudaEventDisableTiming)) != cudaSuccess)
             return cuda_fail(e, "query scratch event");
-        if ((st = encode_cache_map(*p, p->q_rot, q_rows, &mq)) != KVR_OK ||
-            (st = encode_cache_map(*p, cache_k, rows, &mk)) != KVR_OK ||
-            (st = encode_cache_map(*p, cache_v, rows, &mv)) != KVR_OK)
+        if ((st = encode_cache_map(*p, p->q_rot, q_rows, &pl.mq)) != KVR_OK ||
+            (st = encode_cache_map(*p, pl.cache_k, rows, &pl.mk)) != KVR_OK ||
+            (st = encode_cache_map(*p, pl.cache_v, rows, &pl.mv)) != KVR_OK)
             return st;
+        // the previous call's attention must be done with the query scratch
+        if (p->q_rot_used && (e = cudaStreamWaitEvent(s, p->q_rot_done, 0)) != cudaSuccess)
+            return cuda_fail(e, "query scratch ordering");
     }
 
-    const bool inl = batch <= kInlineEntries;   // then ap, al have <= batch entries too
-    const size_t off_sp = align16(rq.size() * sizeof(DevReq));
-    const size_t off_lc = off_sp + align16(ap.size() * sizeof(DevSpan));
-    const size_t bytes = inl ? 0 : off_lc + al.size() * sizeof(DevLocal);
-    Slot *slot = nullptr;
-    if (bytes > 0 && (st = p->acquire(bytes, bytes, &slot)) != KVR_OK)
-        return st;
-    static const ReqTable no_reqs{};
-    ReqTable rt_inl;
-    AssembleTables tab;
-    AssembleArgs a{};
-    AttnArgs at{};
-    if (inl) {
-        std::memcpy(rt_inl.reqs, rq.data(), rq.size() * sizeof(DevReq));
-        std::memcpy(tab.spans, ap.data(), ap.size() * sizeof(DevSpan));
-        std::memcpy(tab.locals, al.data(), al.size() * sizeof(DevLocal));
+    pl.inl = batch <= kInlineEntries;   // then ap, al have <= batch entries too
+    AssembleArgs &a = pl.a;
+    AttnArgs &at = pl.at;
+    if (pl.inl) {
+        std::memcpy(pl.rt_inl.reqs, pl.rq.data(), pl.rq.size() * sizeof(DevReq));
+        std::memcpy(pl.tab.spans, pl.ap.data(), pl.ap.size() * sizeof(DevSpan));
+        std::memcpy(pl.tab.locals, pl.al.data(), pl.al.size() * sizeof(DevLocal));
         at.reqs = nullptr;
     } else {
-        char *h = static_cast<char *>(slot->host);
-        char *dv = static_cast<char *>(slot->dev);
-        std::memcpy(h, rq.data(), rq.size() * sizeof(DevReq));
-        std::memcpy(h + off_sp, ap.data(), ap.size() * sizeof(DevSpan));
-        std::memcpy(h + off_lc, al.data(), al.size() * sizeof(DevLocal));
-        if ((e = cudaMemcpyAsync(dv, h, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        const size_t off_sp = align16(pl.rq.size() * sizeof(DevReq));
+        const size_t off_lc = off_sp + align16(pl.ap.size() * sizeof(DevSpan));
+        const size_t bytes = off_lc + pl.al.size() * sizeof(DevLocal);
+        if ((st = p->acquire(bytes, bytes, &pl.slot)) != KVR_OK)
+            return st;
+        char *h = static_cast<char *>(pl.slot->host);
+        char *dv = static_cast<char *>(pl.slot->dev);
+        std::memcpy(h, pl.rq.data(), pl.rq.size() * sizeof(DevReq));
+        std::memcpy(h + off_sp, pl.ap.data(), pl.ap.size() * sizeof(DevSpan));
+        std::memcpy(h + off_lc, pl.al.data(), pl.al.size() * sizeof(DevLocal));
+        e = cudaMemcpyAsync(dv, h, bytes, cudaMemcpyHostToDevice, s);
+        cudaEventRecord(pl.slot->done, s);   // the slot is busy from here on
+        pl.slot->used = true;
+        if (e != cudaSuccess)
             return cuda_fail(e, "request table upload");
         a.spans = reinterpret_cast<const DevSpan *>(dv + off_sp);
         a.locals = reinterpret_cast<const DevLocal *>(dv + off_lc);
         at.reqs = reinterpret_cast<const DevReq *>(dv);
     }
-    const ReqTable &rt = inl ? rt_inl : no_reqs;
 
     at.n_reqs = batch;
     at.rope = p->rope;
-    at.q = q;
-    at.cache_k = cache_k;
-    at.cache_v = cache_v;
-    at.out = out;
+    at.q = pl.q;
+    at.cache_k = pl.cache_k;
+    at.cache_v = pl.cache_v;
+    at.out = pl.out;
     at.n_layers = L;
     at.n_q_heads = Hq;
     at.n_kv_heads = Hkv;
     at.total_q = T;
-    at.scale_log2 = (softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt((float)D)) *
-                    1.4426950408889634f;
+    at.scale_log2 = (pl.scale > 0.f ? pl.scale : 1.f / std::sqrt((float)D)) * 1.4426950408889634f;
     at.err = p->err;
-    if (tc) {
-        // the previous call's attention must be done with the query scratch
-        if (p->q_rot_used && (e = cudaStreamWaitEvent(s, p->q_rot_done, 0)) != cudaSuccess)
-            return cuda_fail(e, "query scratch ordering");
-        int32_t max_lq = 0;
-        for (int b = 0; b < batch; ++b)
-            max_lq = std::max(max_lq, q_offsets[b + 1] - q_offsets[b]);
-        QueryPrologueArgs qp{at.reqs, p->rope, q, kq, vq, cache_k, cache_v, p->q_rot, L, Hq, Hkv, T, max_lq};
+    // CUDA-core path: the query keys / values are appended by the assemble
+    // kernel (un-rotated source, token t turned by P + t); the query heads
+    // are rotated inside the CUDA-core attention kernel
+    a.rope = p->rope;
+    a.cache_k = pl.cache_k;
+    a.cache_v = pl.cache_v;
+    a.n_layers = L;
+    a.n_heads = Hkv;
+    a.upc = 1;
+    return KVR_OK;
+}
+
+// `after_assemble`: the kernel just enqueued on `s` is the assemble kernel of
+// the same prefill, so the query prologue may overlap it.  Without the timing
+// hook the attention kernel always overlaps the prologue's tail.
+static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_assemble)
+{
+    static const ReqTable no_reqs{};
+    const ReqTable &rt = pl.inl ? pl.rt_inl : no_reqs;
+    const int D = p->d.head_dim;
+    cudaError_t e;
+    if (pl.tc) {
+        QueryPrologueArgs qp{pl.at.reqs, p->rope, pl.q, pl.kq, pl.vq, pl.cache_k, pl.cache_v, p->q_rot,
+                             p->d.n_layers, p->d.n_q_heads, p->d.n_kv_heads, pl.T, pl.max_lq, pl.batch};
         p->mark(2, s);
-        e = launch_query_prologue(qp, rt, batch, s);
+        e = launch_query_prologue(qp, rt, p->n_sms, after_assemble && !p->timed, s);
         p->mark(3, s);
         if (e == cudaSuccess) {
-            TcAttnArgs ta{at, &rt, &mq, &mk, &mv, m_blocks, p->n_sms};
+            TcAttnArgs ta{pl.at, &rt, &pl.mq, &pl.mk, &pl.mv, pl.m_blocks, p->n_sms};
             p->mark(4, s);
-            e = launch_attention_tc(ta, s);
+            e = launch_attention_tc(ta, !p->timed, s);
             p->mark(5, s);
         }
         cudaEventRecord(p->q_rot_done, s);
         p->q_rot_used = true;
     } else {
-        // query keys / values appended by the assemble kernel (un-rotated
-        // source, token t turned by P + t); the query heads are rotated inside
-        // the CUDA-core attention kernel
-        a.rope = p->rope;
-        a.cache_k = cache_k;
-        a.cache_v = cache_v;
-        a.n_layers = L;
-        a.n_heads = Hkv;
-        a.upc = 1;
         p->mark(2, s);
-        e = launch_assemble(a, p->d.dtype, D, (int)ap.size(), s, inl ? &tab : nullptr);
+        e = launch_assemble(pl.a, p->d.dtype, D, (int)pl.ap.size(), s, pl.inl ? &pl.tab : nullptr);
         p->mark(3, s);
         if (e == cudaSuccess) {
             p->mark(4, s);
-            e = launch_attention_simt(at, rt, p->d.dtype, D, s);
+            e = launch_attention_simt(pl.at, rt, p->d.dtype, D, s);
             p->mark(5, s);
         }
     }
-    if (slot) {
-        cudaEventRecord(slot->done, s);
-        slot->used = true;
-    }
+    if (pl.slot)
+        cudaEventRecord(pl.slot->done, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "attention launch");
     return KVR_OK;
+}
+
+extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int64_t *cache_offsets,
+                                          const int32_t *prefix_len, const int32_t *q_offsets,
+                                          const void *q, const void *kq, const void *vq,
+                                          void *cache_k, void *cache_v, void *out,
+                                          float softmax_scale, void *stream)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    if (batch < 0)
+        return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
+    if (batch == 0)
+        return KVR_OK;
+    QaPlan pl;
+    kvr_status st;
+    if ((st = qa_validate(*p, batch, cache_offsets, prefix_len, q_offsets, q, kq, vq, cache_k, cache_v,
+                          out, softmax_scale, pl)) != KVR_OK)
+        return st;
+    if (pl.T == 0)
+        return KVR_OK;
+    if ((st = ensure_device(p)) != KVR_OK)
+        return st;
+    DeviceGuard g(p->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = qa_stage(p, pl, s)) != KVR_OK)
+        return st;
+    return qa_launch(p, pl, s, false);
+}
+
+// ---------------------------------------------------------------------------
+// prefill = assemble + query attention in one call
+// ---------------------------------------------------------------------------
+extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *span_offsets,
+                                  const kvr_span *spans, const kvr_local_src *locals, int32_t n_locals,
+                                  const int64_t *cache_offsets, void *cache_k, void *cache_v,
+                                  int32_t *pos_ids, int32_t *src_map, int32_t *prefix_len,
+                                  uint32_t flags, const int32_t *q_offsets, const void *q,
+                                  const void *kq, const void *vq, void *out, float softmax_scale,
+                                  void *stream)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    if (batch < 0)
+        return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
+    if (batch == 0)
+        return KVR_OK;
+    // every check of both halves before anything is enqueued
+    AsmPlan ap;
+    QaPlan qp;
+    kvr_status st;
+    if ((st = asm_validate(*p, batch, span_offsets, spans, locals, n_locals, cache_offsets, flags,
+                           ap)) != KVR_OK ||
+        (st = qa_validate(*p, batch, cache_offsets, ap.plen.data(), q_offsets, q, kq, vq, cache_k,
+                          cache_v, out, softmax_scale, qp)) != KVR_OK)
+        return st;
+    const bool stitch = !ap.ds.empty();
+    if (stitch && (st = asm_check_outputs(ap, cache_k, cache_v, pos_ids, src_map)) != KVR_OK)
+        return st;
+    if (prefix_len)
+        std::copy(ap.plen.begin(), ap.plen.end(), prefix_len);
+    if (!stitch && qp.T == 0)
+        return KVR_OK;
+    if ((st = ensure_device(p)) != KVR_OK)
+        return st;
+    DeviceGuard g(p->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // uploads and stream waits first, so that the kernels follow one another
+    // on the stream with nothing in between
+    if ((stitch && (st = asm_stage(p, ap, s)) != KVR_OK) ||
+        (qp.T > 0 && (st = qa_stage(p, qp, s)) != KVR_OK))
+        return st;
+    if (stitch && (st = asm_launch(p, ap, s, false)) != KVR_OK) {
+        if (ap.slot)
+            cudaEventRecord(ap.slot->done, s);
+        return st;
+    }
+    if (qp.T > 0)
+        st = qa_launch(p, qp, s, stitch);
+    if (ap.slot)
+        cudaEventRecord(ap.slot->done, s);
+    return st;
 }
 
 // ---------------------------------------------------------------------------

@@ -119,6 +119,9 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
     constexpr int RPP = kAssembleThreads / TPR;   // rows per pass
     static_assert(H2 % E == 0 && kAssembleThreads % TPR == 0, "head_dim");
 
+    // the next kernel (the query prologue) touches none of this kernel's
+    // rows: it may start alongside
+    pdl_launch_dependents();
     const DevSpan sp = spans[blockIdx.x];
     const int j = threadIdx.x % TPR;
 

@@ -412,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // setup above overlaps the previous kernel's tail; its outputs (the
+    // stitched cache, the rotated queries) are read only from here on
+    pdl_wait_prerequisites();
 
     if (warp < 8) {
         // =================== softmax / epilogue warpgroup of tile x ===================
@@ -707,26 +710,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool attention_tc_supported(int dtype, int head_dim) { return dtype == KVR_DTYPE_BF16 && head_dim == kD; }
 
-cudaError_t launch_attention_tc(const TcAttnArgs &ta, cudaStream_t s)
+cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
 {
     if (ta.n_m_blocks == 0)
         return cudaSuccess;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // the shared-memory opt-in is per device
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(k_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess)
             return e;
-        attr_set = true;
+        if (dev < 64)
+            attr_set[dev] = true;
     }
     const int64_t units = (int64_t)ta.n_m_blocks * ta.base.n_layers * ta.base.n_kv_heads;
     if (units > 0x7fffffff)
         return cudaErrorInvalidValue;
     const int grid = (int)(units < ta.n_sms ? units : ta.n_sms);
-    k_attention_tc<<<grid, kThreads, kSmemBytes, s>>>(*static_cast<const CUtensorMap *>(ta.tmap_q),
-                                                      *static_cast<const CUtensorMap *>(ta.tmap_k),
-                                                      *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base,
-                                                      *ta.rt, ta.n_m_blocks);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_attention_tc, *static_cast<const CUtensorMap *>(ta.tmap_q),
+                              *static_cast<const CUtensorMap *>(ta.tmap_k),
+                              *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base, *ta.rt, ta.n_m_blocks);
 }
 
 }  // namespace kvr

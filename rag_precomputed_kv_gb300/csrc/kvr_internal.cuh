@@ -19,6 +19,12 @@ constexpr int kRopeSplit = 4096;
 constexpr int kMaxPosition = kRopeSplit * kRopeSplit;  // 2^24
 
 #ifdef __CUDACC__
+// Programmatic dependent launch: let the next kernel of the stream (launched
+// with programmatic serialization) start its grid now / wait until the
+// previous kernel of the stream has completed and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // (cos, sin) of pos * w_i for |pos| < 2^24 from the two table halves (angle
 // addition, one complex product in float); a negative pos is the conjugate.
 __device__ __forceinline__ float2 rope_cs(const float2 *__restrict__ tab, int half, int pos, int i)
@@ -125,6 +131,7 @@ struct QueryPrologueArgs {
     int32_t n_layers, n_q_heads, n_kv_heads;
     int32_t total_q;            // T
     int32_t max_q_len;          // longest query of the batch
+    int32_t n_reqs;
 };
 
 // ---- launchers (each returns the cudaGetLastError of its launch) ----
@@ -148,9 +155,14 @@ struct TcAttnArgs {
     int32_t n_m_blocks;         // total 256-row query blocks over all requests
     int32_t n_sms;              // persistent grid size bound
 };
-cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt, int n_reqs,
+// `pdl`: the kernel before it on the stream is the assemble kernel of the
+// same prefill (which it may overlap: it reads only the caller's inputs and
+// writes only query-side rows).
+cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt, int n_sms, bool pdl,
                                   cudaStream_t s);
-cudaError_t launch_attention_tc(const TcAttnArgs &a, cudaStream_t s);
+// `pdl`: the kernel before it on the stream is the query prologue of the
+// same call; the setup (barriers, TMEM) overlaps that kernel's tail.
+cudaError_t launch_attention_tc(const TcAttnArgs &a, bool pdl, cudaStream_t s);
 bool attention_tc_supported(int dtype, int head_dim);
 
 }  // namespace kvr

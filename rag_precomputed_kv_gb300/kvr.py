@@ -26,7 +26,7 @@ STATUS = {0: "KVR_OK", 1: "KVR_ERR_INVALID_ARG", 2: "KVR_ERR_OUT_OF_RANGE", 3: "
           4: "KVR_ERR_CUDA", 5: "KVR_ERR_TIMEOUT", 6: "KVR_ERR_DEVICE_CHECK"}
 
 EXPORTED = ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
-            "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
+            "kvr_prefill", "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
             "kvr_set_timing_events")
 PATH_UNBOUND, PATH_CUDA_CORES, PATH_TCGEN05 = -1, 0, 1
 
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH):
     lib.kvr_pool_unregister.argtypes = [vp]
     lib.kvr_assemble.argtypes = [vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_uint32, vp]
     lib.kvr_query_attention.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
+    lib.kvr_prefill.argtypes = [vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_uint32,
+                                vp, vp, vp, vp, vp, ctypes.c_float, vp]
     lib.kvr_check.argtypes = [vp, vp]
     lib.kvr_status_string.restype = ctypes.c_char_p
     lib.kvr_status_string.argtypes = [ctypes.c_int]
@@ -80,7 +82,7 @@ def load(path: str = LIB_PATH):
     lib.kvr_attention_path.argtypes = [vp]
     lib.kvr_attention_path.restype = ctypes.c_int32
     for name in ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble",
-                 "kvr_query_attention", "kvr_check"):
+                 "kvr_query_attention", "kvr_prefill", "kvr_check"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -112,6 +114,17 @@ def _i64(a) -> np.ndarray:
 
 def _np_ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _span_args(span_offsets, spans, cache_offsets, locals_):
+    so = _i32(span_offsets)
+    sp = _i32(spans).reshape(-1, 3)
+    co = _i64(cache_offsets)
+    loc = (LocalSrc * max(1, len(locals_)))()
+    for i, (lk, lv) in enumerate(locals_):
+        assert lk.stride() == lv.stride() and lk.stride(-1) == 1
+        loc[i] = LocalSrc(_ptr(lk), _ptr(lv), lk.shape[2], (ctypes.c_int64 * 3)(*lk.stride()[:3]))
+    return so, sp, co, loc, len(so) - 1
 
 
 class Pool:
@@ -148,14 +161,7 @@ class Pool:
     def assemble(self, span_offsets: Sequence[int], spans, cache_offsets, cache_k, cache_v,
                  locals_=(), pos_ids=None, src_map=None, composite: bool = False, stream=None):
         """kvr_assemble; returns the per-request prefix lengths (numpy int32)."""
-        so = _i32(span_offsets)
-        sp = _i32(spans).reshape(-1, 3)
-        co = _i64(cache_offsets)
-        batch = len(so) - 1
-        loc = (LocalSrc * max(1, len(locals_)))()
-        for i, (lk, lv) in enumerate(locals_):
-            assert lk.stride() == lv.stride() and lk.stride(-1) == 1
-            loc[i] = LocalSrc(_ptr(lk), _ptr(lv), lk.shape[2], (ctypes.c_int64 * 3)(*lk.stride()[:3]))
+        so, sp, co, loc, batch = _span_args(span_offsets, spans, cache_offsets, locals_)
         plen = np.zeros(max(batch, 1), np.int32)
         _raise(load().kvr_assemble(self._h, batch, _np_ptr(so), _np_ptr(sp) if sp.size else None,
                                    ctypes.cast(loc, ctypes.c_void_p) if len(locals_) else None,
@@ -163,6 +169,23 @@ class Pool:
                                    _ptr(cache_k), _ptr(cache_v), _ptr(pos_ids), _ptr(src_map),
                                    _np_ptr(plen), KVR_POSITIONS_COMPOSITE if composite else 0,
                                    _stream_ptr(stream)))
+        return plen[:batch]
+
+    def prefill(self, span_offsets: Sequence[int], spans, cache_offsets, cache_k, cache_v,
+                q_offsets, q, kq, vq, out, locals_=(), pos_ids=None, src_map=None,
+                composite: bool = False, softmax_scale: float = 0.0, stream=None):
+        """kvr_prefill (assemble + query attention in one call); returns the
+        per-request prefix lengths (numpy int32)."""
+        so, sp, co, loc, batch = _span_args(span_offsets, spans, cache_offsets, locals_)
+        qo = _i32(q_offsets)
+        plen = np.zeros(max(batch, 1), np.int32)
+        _raise(load().kvr_prefill(self._h, batch, _np_ptr(so), _np_ptr(sp) if sp.size else None,
+                                  ctypes.cast(loc, ctypes.c_void_p) if len(locals_) else None,
+                                  len(locals_), _np_ptr(co),
+                                  _ptr(cache_k), _ptr(cache_v), _ptr(pos_ids), _ptr(src_map),
+                                  _np_ptr(plen), KVR_POSITIONS_COMPOSITE if composite else 0,
+                                  _np_ptr(qo), _ptr(q), _ptr(kq), _ptr(vq), _ptr(out),
+                                  float(softmax_scale), _stream_ptr(stream)))
         return plen[:batch]
 
     def query_attention(self, cache_offsets, prefix_len, q_offsets, q, kq, vq, cache_k, cache_v,

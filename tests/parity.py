@@ -117,8 +117,20 @@ class Case:
         self.out = torch.full_like(self.t.q, float("nan"))
         self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta)
 
-    def run(self, attention=True):
+    def run(self, attention=True, prefill=False):
+        """The hot path through the C ABI: kvr_assemble then
+        kvr_query_attention, or (prefill=True) the single kvr_prefill call."""
         import torch
+        if prefill:
+            assert attention
+            plen = self.pool.prefill(self.span_offsets, np.concatenate(self.spans), self.cache_offsets,
+                                     self.cache_k, self.cache_v, self.q_offsets, self.t.q, self.t.kq,
+                                     self.t.vq, self.out, locals_=self.locals, pos_ids=self.pos_ids,
+                                     src_map=self.src_map, composite=self.composite)
+            assert np.array_equal(plen, self.prefix)
+            torch.cuda.synchronize()
+            self.pool.check()
+            return
         plen = self.pool.assemble(self.span_offsets, np.concatenate(self.spans), self.cache_offsets,
                                   self.cache_k, self.cache_v, locals_=self.locals,
                                   pos_ids=self.pos_ids, src_map=self.src_map,
@@ -150,13 +162,13 @@ class Case:
 
 
 def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requests=None,
-                    attention=True, composite=False, seed_units=0, case=None):
+                    attention=True, composite=False, seed_units=0, case=None, prefill=False):
     """Run one configuration and compare with the oracle; returns a summary
     dict with ``ok`` and the worst errors."""
     import torch
     cfg = cfg or W.CONFIGS[cid]
     case = case or Case(cfg, device=device, composite=composite)
-    case.run(attention=attention)
+    case.run(attention=attention, prefill=prefill)
     rng = np.random.default_rng(1234 + seed_units)
     req_ids = range(len(case.reqs)) if requests is None else requests
     L, H, Hq, D = cfg.n_layers, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim

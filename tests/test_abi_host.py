@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
-              "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
+              "kvr_prefill", "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
               "kvr_set_timing_events"):
         assert n in names
 
@@ -80,6 +80,8 @@ def test_null_arguments(lib):
     assert lib.kvr_assemble(None, 1, None, None, None, 0, None, None, None, None, None, None, 0, None) == 1
     assert lib.kvr_query_attention(None, 1, None, None, None, None, None, None, None, None, None,
                                    ctypes.c_float(0), None) == 1
+    assert lib.kvr_prefill(None, 1, None, None, None, 0, None, None, None, None, None, None, 0,
+                           None, None, None, None, None, ctypes.c_float(0), None) == 1
     assert lib.kvr_pool_unregister(None) == 0
 
 
@@ -152,5 +154,55 @@ def test_no_gpu_means_cuda_error_not_a_crash(lib):
     try:
         st, _ = _assemble(lib, h, [[0, 0, 8]], [0, 1], [0, 100])
         assert st == 4
+    finally:
+        lib.kvr_pool_unregister(h)
+
+
+def _prefill(lib, h, spans, span_offsets, cache_offsets, q_offsets, q=0x200000, cache=0x100000,
+             flags=0, scale=0.0):
+    so = np.ascontiguousarray(span_offsets, np.int32)
+    sp = np.ascontiguousarray(spans, np.int32).reshape(-1, 3)
+    co = np.ascontiguousarray(cache_offsets, np.int64)
+    qo = np.ascontiguousarray(q_offsets, np.int32)
+    plen = np.full(len(so), -7, np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    st = lib.kvr_prefill(h, len(so) - 1, p(so), p(sp) if sp.size else None, None, 0, p(co),
+                         cache, cache, None, None, p(plen), flags, p(qo), q, q, q, q,
+                         ctypes.c_float(scale), None)
+    return st, plen
+
+
+def test_prefill_checks_both_halves_before_any_gpu_work(lib):
+    """kvr_prefill rejects a bad stitch and a bad query half alike, without a
+    GPU and before writing its prefix-length output."""
+    st, h = _register(lib, _desc())
+    assert st == 0
+    try:
+        # stitch half: unknown entry, span past the end of its entry
+        for spans in ([[4, 0, 8]], [[0, 500, 513]]):
+            st, plen = _prefill(lib, h, spans, [0, 1], [0, 1000], [0, 4])
+            assert st == 2 and plen[0] == -7, spans
+        # query half: the stitched prefix (512) + 16 query rows overflow 520 rows
+        st, plen = _prefill(lib, h, [[0, 0, 512]], [0, 1], [0, 520], [0, 16])
+        assert st == 2 and plen[0] == -7
+        # query half: misaligned q, negative scale, decreasing q_offsets
+        assert _prefill(lib, h, [[0, 0, 8]], [0, 1], [0, 100], [0, 4], q=0x200002)[0] == 1
+        assert _prefill(lib, h, [[0, 0, 8]], [0, 1], [0, 100], [0, 4], scale=-1.0)[0] == 1
+        assert _prefill(lib, h, [[0, 0, 8], [1, 0, 8]], [0, 1, 2], [0, 100, 200], [0, 4, 2])[0] == 1
+        # nothing to do at all: empty spans and no query tokens; P_b reported
+        st, plen = _prefill(lib, h, [[0, 3, 3]], [0, 1], [0, 10], [0, 0])
+        assert st == 0 and plen[0] == 0
+    finally:
+        lib.kvr_pool_unregister(h)
+
+
+def test_prefill_without_gpu_is_a_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, h = _register(lib, _desc())
+    try:
+        st, plen = _prefill(lib, h, [[0, 0, 8]], [0, 1], [0, 100], [0, 4])
+        assert st == 4 and plen[0] == 8
     finally:
         lib.kvr_pool_unregister(h)

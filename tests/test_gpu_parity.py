@@ -152,6 +152,65 @@ def test_repeat_calls_reuse_staging():
     _ok(run_parity_case(cfg=W.CONFIGS[1], case=case))
 
 
+def _outputs(case):
+    return [x.clone() for x in (case.out, case.cache_k, case.cache_v, case.pos_ids, case.src_map)]
+
+
+def _reset(case):
+    for x in (case.out, case.cache_k, case.cache_v):
+        x.fill_(float("nan"))
+    case.pos_ids.fill_(-1)
+    case.src_map.fill_(-1)
+
+
+def _same_bits(a, b):
+    import torch
+    if a.dtype in (torch.bfloat16, torch.float16):
+        return torch.equal(a.view(torch.int16), b.view(torch.int16))
+    if a.dtype == torch.float32:
+        return torch.equal(a.view(torch.int32), b.view(torch.int32))
+    return torch.equal(a, b)
+
+
+def _prefill_case(name):
+    if name == "cfg2":
+        return W.CONFIGS[2], None
+    if name == "cfg1_fp32":
+        return W.CONFIGS[1], None
+    if name == "no_prefix":      # nothing to stitch: the query kernels run alone
+        cfg = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, prompt_len=0, query_len=19)
+        return _custom(cfg, [[], [[0, 4, 4]]])
+    if name == "uploaded_tables":   # > 64 spans and requests: staged uploads on both halves
+        base = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, prompt_len=0, query_len=3)
+        rng = np.random.default_rng(11)
+        lists = [[[int(rng.integers(0, base.n_chunks)), 5, 5 + int(rng.integers(1, 9))]
+                  for _ in range(int(rng.integers(1, 3)))] for _ in range(66)]
+        return _custom(base, lists)
+    raise ValueError(name)
+
+
+@pytest.mark.parametrize("name", ["cfg2", "cfg1_fp32", "no_prefix", "uploaded_tables"])
+def test_prefill_matches_oracle_and_the_two_calls(name):
+    """kvr_prefill (the stitch and the query kernels launched back to back,
+    overlapping) against the oracle, and bit for bit against kvr_assemble
+    followed by kvr_query_attention."""
+    cfg, reqs = _prefill_case(name)
+    case = Case(cfg, reqs=reqs)
+    few = None if len(case.reqs) <= 4 else [0, 1, len(case.reqs) // 2, len(case.reqs) - 1]
+    _ok(run_parity_case(cfg=cfg, case=case, prefill=True, requests=few))
+    got = _outputs(case)
+    _reset(case)
+    case.run()
+    want = _outputs(case)
+    for g, w in zip(got, want):
+        assert _same_bits(g, w)
+    # and once more through kvr_prefill after the two calls (scratch reuse)
+    _reset(case)
+    case.run(prefill=True)
+    for g, w in zip(_outputs(case), want):
+        assert _same_bits(g, w)
+
+
 def test_config4_inline_docs_sampled():
     _ok(run_parity_case(4, sample_units=2, requests=[0, 7]))
 
