@@ -30,9 +30,17 @@
 //
 // Warp roles (320 threads, one CTA per SM): warps 0-3 and 4-7 are the
 // warpgroups of tiles A and B (softmax, epilogue); warp 8 issues the TMA loads
-// of Q (already rotated and packed by the query-prologue kernel) and of the
-// K/V tiles into a 4-slot ring; warp 9 owns the 512 TMEM columns and issues
-// the MMAs (one thread).  Barrier phases run on across units.
+// of Q (already rotated and packed by the query-prologue kernel; the next
+// unit's Q is prefetched into L2) and of the K/V tiles into a 4-slot ring;
+// warp 9 owns the 512 TMEM columns and runs the MMA schedule on all 32 lanes,
+// one lane (elected once) issuing the tcgen05 instructions: with the
+// schedule's descriptor arithmetic warp-uniform, one MMA issues about as fast
+// as the tensor core retires it (issued from a single-lane branch it was the
+// bottleneck).  Barrier phases run on across units.
+//
+// Epilogue: each softmax thread holds one output row; its warp stages 32 rows
+// x 64 columns at a time in shared memory and writes them back as whole
+// 128-byte lines (row-per-thread stores touch one line per lane).
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the CTA
 // records KVR_ERR_TIMEOUT in the pool's error word, all roles leave their
@@ -64,7 +72,9 @@ constexpr unsigned long long kWaitNs = 2000000000ull;
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;                          // Q_A, Q_B
 constexpr int kOffKV = kOffQ + 2 * kTileBytes;
-constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
+constexpr int kOffStage = kOffKV + kSlots * kTileBytes;
+constexpr int kStageBytes = 8 * 32 * 128;
+constexpr int kOffBar = kOffStage + kStageBytes;
 // barriers
 constexpr int kBarFull = 0;                       // [kSlots] K/V tile landed
 constexpr int kBarEmpty = kBarFull + kSlots;      // [kSlots] K/V tile consumed
@@ -146,6 +156,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             uint32_t bar)
 {
@@ -171,11 +189,47 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-__device__ __forceinline__ void umma_commit(uint32_t bar)
+// The MMA role runs on all 32 lanes of its warp (descriptor arithmetic stays
+// warp-uniform); one lane, elected once, issues the tcgen05 instructions.
+__device__ __forceinline__ uint32_t elect_one()
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+    uint32_t p;
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+    return p;
+}
+
+template <bool ACC>
+__device__ __forceinline__ void mma_ss(uint32_t lead, uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "n"(ACC ? 1 : 0), "r"(lead)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                         uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(lead)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t lead, uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+                 "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+                 "r"(lead)
                  : "memory");
 }
+
 
 // 16 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
@@ -199,26 +253,7 @@ __device__ __forceinline__ uint64_t desc_with_lo(uint32_t lo, uint32_t hi)
     return d;
 }
 
-template <bool ACC>
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "n"(ACC ? 1 : 0)
-        : "memory");
-}
 
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
@@ -287,6 +322,21 @@ __device__ __forceinline__ void flag_timeout(int *err, volatile int *abort_flag)
     atomicCAS(err, 0, kDevTimeout);
 }
 
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
 
 // Packed fp32 pairs (two lanes of one 64-bit register) for the softmax.
 __device__ __forceinline__ uint64_t pk2(float a, float b)
@@ -531,18 +581,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(kBarOEmpty + x));      // O_x may now take the next unit's PV
-            if (row_ok) {
-                const float inv = 1.f / l_run;
-                __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(a.out) +
-                                    (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD;
+            {
+                const float inv = row_ok ? 1.f / l_run : 0.f;
+                const int64_t orow = row_ok ? (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD
+                                            : -1;
+                __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+                const uint32_t stg = sbase + kOffStage + (uint32_t)warp * 32 * 128;
+                const int wr = r & 31;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    uint4 v;
-                    v.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-                    v.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-                    v.z = pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-                    v.w = pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
-                    *reinterpret_cast<uint4 *>(op + 8 * c) = v;
+                for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float *f = o + 64 * hh + 8 * c;
+                        st_shared_v4(stg + wr * 128 + ((c ^ (wr & 7)) << 4), pack_bf16(f[0] * inv, f[1] * inv),
+                                     pack_bf16(f[2] * inv, f[3] * inv), pack_bf16(f[4] * inv, f[5] * inv),
+                                     pack_bf16(f[6] * inv, f[7] * inv));
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = 4 * i + (lane >> 3), c = lane & 7;
+                        const int64_t base = __shfl_sync(0xffffffffu, orow, row);
+                        const uint4 v = ld_shared_v4(stg + row * 128 + ((c ^ (row & 7)) << 4));
+                        if (base >= 0)
+                            *reinterpret_cast<uint4 *>(out + base + 64 * hh + 8 * c) = v;
+                    }
+                    __syncwarp();
                 }
             }
         }
@@ -567,6 +631,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
                 }
                 ++nq;
+                if (u + (int)gridDim.x < n_units) {
+                    const Unit wn = unit_at(a, reqs, n_blocks, u + gridDim.x);
+                    for (int x = 0; x < (wn.n_t[1] > 0 ? 2 : 1); ++x) {
+                        tma_prefetch_2d(&tmq, 0, wn.q_row0 + x * kTileM);
+                        tma_prefetch_2d(&tmq, 64, wn.q_row0 + x * kTileM);
+                    }
+                }
                 for (int i = 0; i < 2 * w.n_tiles; ++i, ++tt) {
                     const int slot = tt % kSlots;
                     if (tt >= kSlots && !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag)) {
@@ -595,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // =================== MMA issuer ===================
-        if (lane == 0) {
+        {
+            const uint32_t lead = elect_one();
             int tt = 0, nq = 0;
             int p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
             bool o_used[2] = {false, false};
@@ -614,11 +686,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < kD / 16; ++k) {
                     const uint32_t off = ((k >> 2) * kPanelBytes + (k & 3) * 32) >> 4;
                     if (k == 0)
-                        mma_ss<false>(d, desc_with_lo(qa + off, hi_k), desc_with_lo(kb + off, hi_k), kIdescS);
+                        mma_ss<false>(lead, d, desc_with_lo(qa + off, hi_k), desc_with_lo(kb + off, hi_k), kIdescS);
                     else
-                        mma_ss<true>(d, desc_with_lo(qa + off, hi_k), desc_with_lo(kb + off, hi_k), kIdescS);
+                        mma_ss<true>(lead, d, desc_with_lo(qa + off, hi_k), desc_with_lo(kb + off, hi_k), kIdescS);
                 }
-                umma_commit(bar(kBarSFull + x));
+                umma_commit(lead, bar(kBarSFull + x));
             };
             auto wait_kv = [&](int k) -> bool {
                 if (!mbar_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1, abort_flag))
@@ -637,8 +709,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (w.n_t[x] > 0)
                         issue_s(x, tt % kSlots);
                 if (w.n_tiles == 1)
-                    umma_commit(bar(kBarQEmpty));
-                umma_commit(bar(kBarEmpty + tt % kSlots));
+                    umma_commit(lead, bar(kBarQEmpty));
+                umma_commit(lead, bar(kBarEmpty + tt % kSlots));
                 for (int j = 0; j < w.n_tiles && ok; ++j) {
                     const int tv = tt + 2 * j + 1, tk = tt + 2 * j + 2;
                     const uint32_t vb = lo_v + ((kOffKV + (tv % kSlots) * kTileBytes) >> 4);
@@ -667,10 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t acc0 = j > 0;
 #pragma unroll
                         for (int k = 0; k < kTileN / 16; ++k)
-                            mma_ts(d, pa + 8 * k, desc_with_lo(vb + ((k * 2048) >> 4), hi_v), kIdescPV,
+                            mma_ts(lead, d, pa + 8 * k, desc_with_lo(vb + ((k * 2048) >> 4), hi_v), kIdescPV,
                                    k > 0 ? 1u : acc0);
                         if (j + 1 == w.n_t[x]) {
-                            umma_commit(bar(kBarOFull + x));
+                            umma_commit(lead, bar(kBarOFull + x));
                             o_used[x] = true;
                         } else {
                             if (!k_ready && !(k_ready = wait_kv(tk))) {
@@ -683,17 +755,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok)
                         break;
                     if (k_ready && j + 2 == w.n_tiles)
-                        umma_commit(bar(kBarQEmpty));   // the unit's last S MMAs are issued
-                    umma_commit(bar(kBarEmpty + tv % kSlots));
+                        umma_commit(lead, bar(kBarQEmpty));   // the unit's last S MMAs are issued
+                    umma_commit(lead, bar(kBarEmpty + tv % kSlots));
                     if (k_ready)
-                        umma_commit(bar(kBarEmpty + tk % kSlots));
+                        umma_commit(lead, bar(kBarEmpty + tk % kSlots));
                 }
                 tt += 2 * w.n_tiles;
             }
             if (!ok)
                 flag_timeout(a.err, abort_flag);
             // drain: all issued MMAs complete before TMEM is released
-            umma_commit(bar(kBarDrain));
+            umma_commit(lead, bar(kBarDrain));
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(bar(kBarDrain), 0) && globaltimer() - t0 < kWaitNs) {
             }
