@@ -155,12 +155,13 @@ class Workload:
         self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta)
         self.plen = self.prefix.astype(np.int32)
 
-    def step(self, q=None, kq=None, vq=None, out=None):
+    def step(self, q=None, kq=None, vq=None, out=None, skip_prefix_cache=False):
         """One prefill of the whole batch: a single kvr_prefill call."""
         self.pool.prefill(self.span_offsets, self.spans, self.cache_offsets, self.cache_k,
                           self.cache_v, self.q_offsets, self.t.q if q is None else q,
                           self.t.kq if kq is None else kq, self.t.vq if vq is None else vq,
-                          self.out if out is None else out, locals_=self.locals)
+                          self.out if out is None else out, locals_=self.locals,
+                          skip_prefix_cache=skip_prefix_cache)
 
 
 def dist_setup():
@@ -259,6 +260,31 @@ def run_kvr(args):
     att_ms = [e[4].elapsed_time(e[5]) for e in ev]
     ser_ms = [e[0].elapsed_time(e[5]) for e in ev]
 
+    # ---- the same prefill with KVR_PREFILL_SKIP_PREFIX_CACHE (the attention
+    # gathers the prefix from the pool; no stitched cache is written), when the
+    # pool and spans allow it ----
+    gather = None
+    if wl.pool.attention_path == K.PATH_TCGEN05 and not wl.locals:
+        n_g = min(args.steps, 500)
+        g0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_g)]
+        g1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_g)]
+        for _ in range(args.warmup):
+            flush.zero_()
+            wl.step(skip_prefix_cache=True)
+        torch.cuda.synchronize()
+        for k in range(n_g):
+            flush.zero_()
+            g0[k].record(stream)
+            wl.step(skip_prefix_cache=True)
+            g1[k].record(stream)
+        torch.cuda.synchronize()
+        wl.pool.check()
+        g_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(g0, g1))
+        gather = {"ms_per_step": round(g_ms, 5), "steps": n_g,
+                  "value": round(int(wl.prefix.sum()) / (g_ms * 1e-3), 1), "unit": UNIT,
+                  "what": "kvr_prefill with KVR_PREFILL_SKIP_PREFIX_CACHE: the attention gathers and "
+                          "re-rotates the prefix from the pool, no stitched cache written"}
+
     # ---- end to end through the public API with host buffers ----
     q_h = wl.t.q.cpu().pin_memory()
     kq_h = wl.t.kq.cpu().pin_memory()
@@ -337,6 +363,7 @@ def run_kvr(args):
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3 / args.steps, 5)},
         "gpu_launches": 3 * args.steps,
+        "skip_prefix_cache": gather,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -70,6 +70,13 @@ enum { KVR_DTYPE_BF16 = 0, KVR_DTYPE_FP32 = 1 };
  * TurboRAG blog, "Position ID", Figure 5. */
 #define KVR_POSITIONS_COMPOSITE 1u
 
+/* kvr_prefill flag: no decode follows, so the stitched prefix is not kept.
+ * The prefix rows [0, P_b) of the cache blocks are left as they are; the
+ * attention gathers the prefix keys and values straight from the pool and
+ * re-rotates the keys on chip (the query rows P_b.. are still appended, and
+ * pos_ids / src_map are still written).  The output is the same. */
+#define KVR_PREFILL_SKIP_PREFIX_CACHE 2u
+
 typedef struct kvr_pool *kvr_pool_t;
 
 /*
@@ -207,6 +214,12 @@ KVR_API kvr_status kvr_query_attention(kvr_pool_t pool, int32_t batch, const int
  * query-side kernel (rotation and append of the query tokens, which touches
  * no prefix row) runs alongside the stitch, and the attention kernel's setup
  * overlaps it.  The timing hook (kvr_set_timing_events) serializes them.
+ *
+ * flags: KVR_POSITIONS_COMPOSITE as in kvr_assemble; KVR_PREFILL_SKIP_PREFIX_CACHE
+ * (above) needs a bf16 pool with head_dim 128, laid out contiguously
+ * ([entries][L][H_kv][entry_len][D], fewer than 2^31 rows), spans from the
+ * pool only (n_locals = 0) and the tensor-core attention; otherwise the call
+ * returns KVR_ERR_UNSUPPORTED before any work.
  * Errors: those of the two calls; nothing is enqueued when a check fails.
  */
 KVR_API kvr_status kvr_prefill(kvr_pool_t pool, int32_t batch, const int32_t *span_offsets,

@@ -313,6 +313,7 @@ int units_per_cta(int LH, int64_t rows, int64_t n_spans)
 struct AsmPlan {
     std::vector<DevSpan> ds;
     std::vector<int32_t> plen;
+    std::vector<int32_t> span0;   // request b's first entry of ds
     int64_t flat = 0;
     const kvr_local_src *locals = nullptr;
     int32_t n_locals = 0;
@@ -328,7 +329,7 @@ static kvr_status asm_validate(const kvr_pool &p, int32_t batch, const int32_t *
                                const kvr_span *spans, const kvr_local_src *locals, int32_t n_locals,
                                const int64_t *cache_offsets, uint32_t flags, AsmPlan &pl)
 {
-    if (flags & ~KVR_POSITIONS_COMPOSITE)
+    if (flags & ~(uint32_t)KVR_POSITIONS_COMPOSITE)
         return fail(KVR_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     kvr_status st;
     if ((st = check_offsets32(span_offsets, batch, "span_offsets")) != KVR_OK ||
@@ -349,10 +350,12 @@ static kvr_status asm_validate(const kvr_pool &p, int32_t batch, const int32_t *
     pl.n_locals = n_locals;
     pl.ds.reserve(n_spans);
     pl.plen.assign(batch, 0);
+    pl.span0.assign(batch, 0);
     int64_t flat = 0;
     for (int b = 0; b < batch; ++b) {
         const int64_t cap = cache_offsets[b + 1] - cache_offsets[b];
         int64_t row = 0;
+        pl.span0[b] = (int32_t)pl.ds.size();
         for (int i = span_offsets[b]; i < span_offsets[b + 1]; ++i) {
             const kvr_span s = spans[i];
             int64_t src_len;
@@ -535,6 +538,33 @@ kvr_status encode_cache_map(const kvr_pool &p, void *base, int64_t rows, CUtenso
         return fail(KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return KVR_OK;
 }
+
+// The pool as a 2-D [entries * L * H_kv * entry_len, D] tensor with a box of
+// one row (64 columns): the attention kernel's gather4 source.
+kvr_status encode_gather_map(const kvr_pool &p, const void *base, CUtensorMap *m, uint32_t box_rows = 1)
+{
+    if (!p.encode)
+        return fail(KVR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled not available");
+    const int64_t rows = p.d.n_entries * p.d.n_layers * p.d.n_kv_heads * p.d.entry_len;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.d.head_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.d.head_dim * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = p.encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(KVR_ERR_CUDA, "cuTensorMapEncodeTiled (pool gather) failed (%d)", (int)r);
+    return KVR_OK;
+}
+
+// What the gathering attention needs beyond a query-attention launch.
+struct GatherLaunch {
+    CUtensorMap mpk, mpv, mbk, mbv;
+    GatherArgs g{};
+    SpanTable st;
+    bool inl = false;
+};
 
 }  // namespace
 
@@ -735,7 +765,8 @@ static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
 // `after_assemble`: the kernel just enqueued on `s` is the assemble kernel of
 // the same prefill, so the query prologue may overlap it.  Without the timing
 // hook the attention kernel always overlaps the prologue's tail.
-static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_assemble)
+static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_assemble,
+                            const GatherLaunch *gl = nullptr)
 {
     static const ReqTable no_reqs{};
     const ReqTable &rt = pl.inl ? pl.rt_inl : no_reqs;
@@ -749,6 +780,15 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         p->mark(3, s);
         if (e == cudaSuccess) {
             TcAttnArgs ta{pl.at, &rt, &pl.mq, &pl.mk, &pl.mv, pl.m_blocks, p->n_sms};
+            if (gl) {
+                ta.gather = true;
+                ta.tmap_pk = &gl->mpk;
+                ta.tmap_pv = &gl->mpv;
+                ta.tmap_bk = &gl->mbk;
+                ta.tmap_bv = &gl->mbv;
+                ta.g = gl->g;
+                ta.st = gl->inl ? &gl->st : nullptr;
+            }
             p->mark(4, s);
             e = launch_attention_tc(ta, !p->timed, s);
             p->mark(5, s);
@@ -818,11 +858,23 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
     if (batch == 0)
         return KVR_OK;
     // every check of both halves before anything is enqueued
+    const bool gather = flags & KVR_PREFILL_SKIP_PREFIX_CACHE;
+    if (gather) {
+        const kvr_pool_desc &d = p->d;
+        const int64_t E = d.entry_len, D = d.head_dim;
+        const bool contiguous = d.stride[3] == D && d.stride[2] == E * D && d.stride[1] == d.n_kv_heads * E * D &&
+                                d.stride[0] == (int64_t)d.n_layers * d.n_kv_heads * E * D;
+        if (d.dtype != KVR_DTYPE_BF16 || D != 128 || n_locals != 0 || !contiguous ||
+            d.n_entries * d.n_layers * d.n_kv_heads * E > INT32_MAX)
+            return fail(KVR_ERR_UNSUPPORTED,
+                        "KVR_PREFILL_SKIP_PREFIX_CACHE needs a contiguous bf16 pool with head_dim 128 "
+                        "(< 2^31 rows) and pool spans only");
+    }
     AsmPlan ap;
     QaPlan qp;
     kvr_status st;
-    if ((st = asm_validate(*p, batch, span_offsets, spans, locals, n_locals, cache_offsets, flags,
-                           ap)) != KVR_OK ||
+    if ((st = asm_validate(*p, batch, span_offsets, spans, locals, n_locals, cache_offsets,
+                           flags & ~(uint32_t)KVR_PREFILL_SKIP_PREFIX_CACHE, ap)) != KVR_OK ||
         (st = qa_validate(*p, batch, cache_offsets, ap.plen.data(), q_offsets, q, kq, vq, cache_k,
                           cache_v, out, softmax_scale, qp)) != KVR_OK)
         return st;
@@ -837,6 +889,35 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
         return st;
     DeviceGuard g(p->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (gather) {
+        // the attention gathers the prefix from the pool; nothing stitched
+        if (!use_tensor_cores(*p))
+            return fail(KVR_ERR_UNSUPPORTED, "KVR_PREFILL_SKIP_PREFIX_CACHE needs the tensor-core attention");
+        if (qp.T == 0)
+            return KVR_OK;
+        GatherLaunch gl;
+        if ((st = encode_gather_map(*p, p->d.k, &gl.mpk)) != KVR_OK ||
+            (st = encode_gather_map(*p, p->d.v, &gl.mpv)) != KVR_OK ||
+            (st = encode_gather_map(*p, p->d.k, &gl.mbk, 32)) != KVR_OK ||
+            (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK)
+            return st;
+        for (int b = 0; b < batch; ++b)
+            qp.rq[b].span0 = ap.span0[b];
+        if ((stitch && (st = asm_stage(p, ap, s)) != KVR_OK) || (st = qa_stage(p, qp, s)) != KVR_OK)
+            return st;
+        gl.inl = !stitch || ap.inl;
+        if (stitch && ap.inl)
+            std::memcpy(gl.st.spans, ap.tab.spans, ap.ds.size() * sizeof(DevSpan));
+        gl.g.spans = gl.inl ? nullptr : ap.a.spans;
+        gl.g.n_spans = (int32_t)ap.ds.size();
+        gl.g.entry_len = (int32_t)p->d.entry_len;
+        gl.g.pos_ids = pos_ids;
+        gl.g.src_map = src_map;
+        st = qa_launch(p, qp, s, false, &gl);
+        if (ap.slot)
+            cudaEventRecord(ap.slot->done, s);
+        return st;
+    }
     // uploads and stream waits first, so that the kernels follow one another
     // on the stream with nothing in between
     if ((stitch && (st = asm_stage(p, ap, s)) != KVR_OK) ||

@@ -56,18 +56,7 @@ struct Vec<__nv_bfloat16> {
     static constexpr int E = 8;
     __device__ static void rotate(uint4 &lo, uint4 &hi, const float *c, const float *s)
     {
-        uint32_t *pl = reinterpret_cast<uint32_t *>(&lo);
-        uint32_t *ph = reinterpret_cast<uint32_t *>(&hi);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&pl[w]));
-            const float2 y = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&ph[w]));
-            const float c0 = c[2 * w], s0 = s[2 * w], c1 = c[2 * w + 1], s1 = s[2 * w + 1];
-            __nv_bfloat162 xo = __floats2bfloat162_rn(fmaf(x.x, c0, -y.x * s0), fmaf(x.y, c1, -y.y * s1));
-            __nv_bfloat162 yo = __floats2bfloat162_rn(fmaf(x.x, s0, y.x * c0), fmaf(x.y, s1, y.y * c1));
-            pl[w] = *reinterpret_cast<uint32_t *>(&xo);
-            ph[w] = *reinterpret_cast<uint32_t *>(&yo);
-        }
+        rotate_bf16x8(lo, hi, c, s);
     }
 };
 

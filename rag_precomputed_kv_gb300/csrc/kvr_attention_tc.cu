@@ -55,7 +55,9 @@ namespace kvr {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;           // stitched-cache variant
+constexpr int kThreadsG = 384;          // gathering variant: + 2 rotator warps
+constexpr int kRotThreads = 64;
 constexpr int kTileM = 128;      // query rows per tile (two tiles per CTA)
 constexpr int kTileN = 128;      // keys per K/V tile
 constexpr int kD = 128;          // head dim
@@ -85,10 +87,14 @@ constexpr int kBarOEmpty = kBarOFull + 2;         // [2] O_x read by the epilogu
 constexpr int kBarQFull = kBarOEmpty + 2;         // Q tiles landed
 constexpr int kBarQEmpty = kBarQFull + 1;         // all S of the unit done with Q
 constexpr int kBarDrain = kBarQEmpty + 1;
-constexpr int kNumBars = kBarDrain + 1;
-constexpr int kOffTmemAddr = kOffBar + 8 * kNumBars;
+constexpr int kBarReady = kBarDrain + 1;          // [kSlots] gathered tile rotated / patched (64 arrivals)
+constexpr int kNumBars = kBarReady + kSlots;
+constexpr int kOffMeta = kOffBar + 8 * kNumBars;  // [2][128] int: rotation of each row of the K slots
+constexpr int kOffTmemAddr = kOffMeta + 2 * kTileN * 4;
 constexpr int kOffAbort = kOffTmemAddr + 4;
 constexpr int kSmemBytes = kOffAbort + 4 + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr int kNoRotation = INT32_MIN;            // meta value of a row that is not a pool row
 
 // instruction descriptors (kind::f16): D fp32, A and B bf16, M = 128, N = 128
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
@@ -156,6 +162,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Four rows (given by row coordinate) x 64 columns of a 2-D tensor whose box
+// is one row high, into four consecutive 128-byte rows of shared memory.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, const int *rows,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(rows[0]), "r"(rows[1]), "r"(rows[2]), "r"(rows[3]),
+        "r"(bar)
+        : "memory");
+}
+
+// Generic-proxy writes to shared memory become visible to the async proxy
+// (the tensor core reads its operands through it).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bring a tile into L2 ahead of its load into shared memory.
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1)
 {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -381,6 +408,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 // Geometry of one work unit, computed identically by every role.
 struct Unit {
     DevReq rq;
+    int b;              // request index
     int l, h, lh;
     int row0[2];        // first packed row of tiles A and B in the request
     int n_t[2];         // K/V tiles each query tile needs (0: tile has no rows)
@@ -405,6 +433,7 @@ __device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, i
             hi = mid - 1;
     }
     w.rq = reqs[lo];
+    w.b = lo;
     const int G = a.n_q_heads / a.n_kv_heads;
     w.l = w.lh / a.n_kv_heads;
     w.h = w.lh - w.l * a.n_kv_heads;
@@ -430,10 +459,14 @@ __device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, i
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kG>
+__global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     k_attention_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnArgs a,
-                   const __grid_constant__ ReqTable rt, const int n_blocks)
+                   const __grid_constant__ ReqTable rt, const int n_blocks,
+                   const __grid_constant__ CUtensorMap tmpk, const __grid_constant__ CUtensorMap tmpv,
+                   const __grid_constant__ CUtensorMap tmbk, const __grid_constant__ CUtensorMap tmbv,
+                   const __grid_constant__ GatherArgs g, const __grid_constant__ SpanTable st)
 {
     const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
     extern __shared__ uint8_t smem_raw[];
@@ -451,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool wg = (i >= kBarPFull && i < kBarPFull + 2) || (i >= kBarOEmpty && i < kBarOEmpty + 2);
-            mbar_init(bar(i), wg ? 128u : 1u);
+            const bool rot = i >= kBarReady && i < kBarReady + kSlots;
+            mbar_init(bar(i), wg ? 128u : rot ? (uint32_t)kRotThreads : 1u);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -613,58 +647,176 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok)
             flag_timeout(a.err, abort_flag);
     } else if (warp == 8) {
-        // =================== TMA producer: Q of each unit, then K_0, V_0, K_1, ... ===================
-        if (lane == 0) {
-            int tt = 0, nq = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit w = unit_at(a, reqs, n_blocks, u);
-                if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const int nqt = w.n_t[1] > 0 ? 2 : 1;
-                mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
-                for (int x = 0; x < nqt; ++x) {
-                    const uint32_t dst = sbase + kOffQ + x * kTileBytes;
-                    tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
-                    tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
-                }
-                ++nq;
-                if (u + (int)gridDim.x < n_units) {
-                    const Unit wn = unit_at(a, reqs, n_blocks, u + gridDim.x);
-                    for (int x = 0; x < (wn.n_t[1] > 0 ? 2 : 1); ++x) {
-                        tma_prefetch_2d(&tmq, 0, wn.q_row0 + x * kTileM);
-                        tma_prefetch_2d(&tmq, 64, wn.q_row0 + x * kTileM);
-                    }
-                }
-                for (int i = 0; i < 2 * w.n_tiles; ++i, ++tt) {
-                    const int slot = tt % kSlots;
-                    if (tt >= kSlots && !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag)) {
+        if constexpr (!kG) {
+            if (lane == 0) {
+                int tt = 0, nq = 0;
+                bool ok = true;
+                for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                    const Unit w = unit_at(a, reqs, n_blocks, u);
+                    if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
-                    const CUtensorMap *map = (i & 1) ? &tmv : &tmk;
-                    const int row = (int)(w.kv_row0 + (int64_t)(i >> 1) * kTileN);
-                    mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
-                    tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
-                    tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
+                    const int nqt = w.n_t[1] > 0 ? 2 : 1;
+                    mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
+                    for (int x = 0; x < nqt; ++x) {
+                        const uint32_t dst = sbase + kOffQ + x * kTileBytes;
+                        tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
+                        tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
+                    }
+                    ++nq;
+                    if (u + (int)gridDim.x < n_units) {
+                        const Unit wn = unit_at(a, reqs, n_blocks, u + gridDim.x);
+                        for (int x = 0; x < (wn.n_t[1] > 0 ? 2 : 1); ++x) {
+                            tma_prefetch_2d(&tmq, 0, wn.q_row0 + x * kTileM);
+                            tma_prefetch_2d(&tmq, 64, wn.q_row0 + x * kTileM);
+                        }
+                    }
+                    for (int i = 0; i < 2 * w.n_tiles; ++i, ++tt) {
+                        const int slot = tt % kSlots;
+                        if (tt >= kSlots && !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
+                        const CUtensorMap *map = (i & 1) ? &tmv : &tmk;
+                        const int row = (int)(w.kv_row0 + (int64_t)(i >> 1) * kTileN);
+                        mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
+                        tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
+                        tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
+                    }
+                }
+                if (!ok)
+                    flag_timeout(a.err, abort_flag);
+                // drain: every issued copy lands before the CTA leaves
+                const uint64_t t0 = globaltimer();
+                for (int k = (tt > kSlots ? tt - kSlots : 0); k < tt; ++k)
+                    while (!mbar_try_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1) &&
+                           globaltimer() - t0 < kWaitNs) {
+                    }
+                if (nq > 0)
+                    while (!mbar_try_wait(bar(kBarQFull), (nq - 1) & 1) && globaltimer() - t0 < kWaitNs) {
+                    }
+            }
+        } else {
+            // ====== gathering producer: Q as above (lane 0); each K/V tile is 128
+            // stitched rows resolved through the span table, lane i loading rows
+            // 4i..4i+3 with one gather4 per 64-column panel ======
+            int tt = 0, nq = 0;
+            bool ok = true;
+            const DevSpan *spans = g.spans ? g.spans : st.spans;
+            int *meta = reinterpret_cast<int *>(smem + kOffMeta);
+            const int64_t e_rows = (int64_t)a.n_layers * a.n_kv_heads * g.entry_len;   // pool rows per entry
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit w = unit_at(a, reqs, n_blocks, u);
+                if (lane == 0) {
+                    if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
+                        ok = false;
+                    } else {
+                        const int nqt = w.n_t[1] > 0 ? 2 : 1;
+                        mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
+                        for (int x = 0; x < nqt; ++x) {
+                            const uint32_t dst = sbase + kOffQ + x * kTileBytes;
+                            tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
+                            tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
+                        }
+                        if (u + (int)gridDim.x < n_units) {
+                            const Unit wn = unit_at(a, reqs, n_blocks, u + gridDim.x);
+                            for (int x = 0; x < (wn.n_t[1] > 0 ? 2 : 1); ++x) {
+                                tma_prefetch_2d(&tmq, 0, wn.q_row0 + x * kTileM);
+                                tma_prefetch_2d(&tmq, 64, wn.q_row0 + x * kTileM);
+                            }
+                        }
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                ++nq;
+                const int s_end = w.b + 1 < a.n_reqs ? reqs[w.b + 1].span0 : g.n_spans;
+                const int64_t lh_row = (int64_t)w.lh * g.entry_len;    // (layer, kv-head) block inside an entry
+                const bool maps = w.lh == 0 && w.row0[0] == 0 && (g.pos_ids || g.src_map);
+                int cur = w.rq.span0;
+                int rows[4] = {0, 0, 0, 0};
+                bool run32 = false;   // this lane's 32-row group is 32 consecutive pool rows
+                for (int i = 0; i < 2 * w.n_tiles; ++i, ++tt) {
+                    const int slot = tt % kSlots;
+                    bool okw = true;
+                    if (tt >= kSlots)
+                        okw = mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag);
+                    if (!__all_sync(0xffffffffu, okw)) {
+                        ok = false;
+                        break;
+                    }
+                    if ((i & 1) == 0) {
+                        // K tile j: resolve its rows (the V tile that follows reuses them)
+                        const int j = i >> 1;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int rr = j * kTileN + 4 * lane + k;
+                            int d = kNoRotation;
+                            rows[k] = 0;   // rows past the prefix: any pool row (patched on chip)
+                            if (rr < w.rq.prefix) {
+                                while (cur + 1 < s_end && spans[cur].row + spans[cur].len <= rr)
+                                    ++cur;
+                                const DevSpan &sp = spans[cur];
+                                const int off = rr - sp.row;
+                                rows[k] = (int)((int64_t)sp.src * e_rows + lh_row + sp.start + off);
+                                d = sp.delta;
+                                if (maps) {
+                                    if (g.pos_ids)
+                                        g.pos_ids[sp.flat0 + off] = sp.pos0 + off;
+                                    if (g.src_map) {
+                                        g.src_map[2 * (sp.flat0 + off)] = sp.src;
+                                        g.src_map[2 * (sp.flat0 + off) + 1] = sp.start + off;
+                                    }
+                                }
+                            }
+                            meta[(slot >> 1) * kTileN + 4 * lane + k] = d;
+                        }
+                        // a group of 8 lanes whose 32 rows are consecutive pool rows takes
+                        // one 32-row box load per panel instead of eight gather4s
+                        const int last = __shfl_up_sync(0xffffffffu, rows[3], 1);
+                        const bool mine = (j * kTileN + 4 * lane + 3 < w.rq.prefix) && rows[1] == rows[0] + 1 &&
+                                          rows[2] == rows[0] + 2 && rows[3] == rows[0] + 3 &&
+                                          ((lane & 7) == 0 || rows[0] == last + 1);
+                        const unsigned ball = __ballot_sync(0xffffffffu, mine);
+                        run32 = ((ball >> (lane & ~7)) & 0xffu) == 0xffu;
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
+                    __syncwarp();
+                    const uint32_t dst = sbase + kOffKV + slot * kTileBytes + (uint32_t)(4 * lane) * 128u;
+                    if (run32) {
+                        if ((lane & 7) == 0) {
+                            const CUtensorMap *map = (i & 1) ? &tmbv : &tmbk;
+                            tma_load_2d(dst, map, 0, rows[0], bar(kBarFull + slot));
+                            tma_load_2d(dst + kPanelBytes, map, 64, rows[0], bar(kBarFull + slot));
+                        }
+                    } else {
+                        const CUtensorMap *map = (i & 1) ? &tmpv : &tmpk;
+                        tma_gather4(dst, map, 0, rows, bar(kBarFull + slot));
+                        tma_gather4(dst + kPanelBytes, map, 64, rows, bar(kBarFull + slot));
+                    }
                 }
             }
             if (!ok)
                 flag_timeout(a.err, abort_flag);
             // drain: every issued copy lands before the CTA leaves
-            const uint64_t t0 = globaltimer();
-            for (int k = (tt > kSlots ? tt - kSlots : 0); k < tt; ++k)
-                while (!mbar_try_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1) &&
-                       globaltimer() - t0 < kWaitNs) {
-                }
-            if (nq > 0)
-                while (!mbar_try_wait(bar(kBarQFull), (nq - 1) & 1) && globaltimer() - t0 < kWaitNs) {
-                }
+            if (lane == 0) {
+                const uint64_t t0 = globaltimer();
+                for (int k = (tt > kSlots ? tt - kSlots : 0); k < tt; ++k)
+                    while (!mbar_try_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1) &&
+                           globaltimer() - t0 < kWaitNs) {
+                    }
+                if (nq > 0)
+                    while (!mbar_try_wait(bar(kBarQFull), (nq - 1) & 1) && globaltimer() - t0 < kWaitNs) {
+                    }
+            }
         }
-    } else {
+    } else if (warp == 9) {
         // =================== MMA issuer ===================
         {
             const uint32_t lead = elect_one();
@@ -693,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(lead, bar(kBarSFull + x));
             };
             auto wait_kv = [&](int k) -> bool {
-                if (!mbar_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1, abort_flag))
+                if (!mbar_wait(bar((kG ? kBarReady : kBarFull) + k % kSlots), (k / kSlots) & 1, abort_flag))
                     return false;
                 tc_fence_after();
                 return true;
@@ -770,6 +922,108 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (!mbar_try_wait(bar(kBarDrain), 0) && globaltimer() - t0 < kWaitNs) {
             }
         }
+    } else if constexpr (kG) {
+        // =================== rotator (gathering variant, warps 10-11) ===================
+        // Thread t owns 16-byte chunk p = t % 8 of each row half (elements
+        // [8p, 8p+8) and their RoPE partners [64 + 8p, ...)) in rows t / 8 + 8k.
+        // Pool rows of a K tile are turned by their span's delta (the same
+        // arithmetic as the stitch kernel); rows past the prefix are the query
+        // rows (already rotated and appended to the cache by the query
+        // prologue) and zero padding, in both the K and the V tile.
+        const int t = threadIdx.x - 10 * 32;
+        const int p = t & 7, r0 = t >> 3;
+        const int *meta = reinterpret_cast<const int *>(smem + kOffMeta);
+        const __nv_bfloat16 *ck = static_cast<const __nv_bfloat16 *>(a.cache_k);
+        const __nv_bfloat16 *cv = static_cast<const __nv_bfloat16 *>(a.cache_v);
+        int tt = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit w = unit_at(a, reqs, n_blocks, u);
+            for (int j = 0; j < w.n_tiles; ++j, tt += 2) {
+                const int sk = tt % kSlots, sv = (tt + 1) % kSlots;
+                if (!mbar_wait(bar(kBarFull + sk), (tt / kSlots) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kb = sbase + kOffKV + sk * kTileBytes;
+                int d_cur = kNoRotation;
+                float c[8], sn[8];
+                // four rows at a time: all loads first, then the rotations, then the stores
+                for (int k0 = 0; k0 < kTileN / 8; k0 += 4) {
+                    uint4 lo[4], hi[4];
+                    int dd[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = r0 + 8 * (k0 + q), rr = j * kTileN + r;
+                        const uint32_t lo_a = kb + r * 128 + ((p ^ (r & 7)) << 4);
+                        dd[q] = kNoRotation;
+                        if (rr < w.rq.prefix) {
+                            dd[q] = meta[(sk >> 1) * kTileN + r];
+                            lo[q] = ld_shared_v4(lo_a);
+                            hi[q] = ld_shared_v4(lo_a + kPanelBytes);
+                        } else if (rr < w.n_valid) {
+                            const __nv_bfloat16 *src = ck + (w.kv_row0 + rr) * kD + 8 * p;
+                            lo[q] = __ldg(reinterpret_cast<const uint4 *>(src));
+                            hi[q] = __ldg(reinterpret_cast<const uint4 *>(src + kD / 2));
+                        } else {
+                            lo[q] = make_uint4(0u, 0u, 0u, 0u);
+                            hi[q] = lo[q];
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (dd[q] == kNoRotation)
+                            continue;
+                        if (dd[q] != d_cur) {
+                            d_cur = dd[q];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float2 cs = rope_cs(a.rope, kD / 2, d_cur, 8 * p + e);
+                                c[e] = cs.x;
+                                sn[e] = cs.y;
+                            }
+                        }
+                        rotate_bf16x8(lo[q], hi[q], c, sn);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = r0 + 8 * (k0 + q);
+                        const uint32_t lo_a = kb + r * 128 + ((p ^ (r & 7)) << 4);
+                        st_shared_v4(lo_a, lo[q].x, lo[q].y, lo[q].z, lo[q].w);
+                        st_shared_v4(lo_a + kPanelBytes, hi[q].x, hi[q].y, hi[q].z, hi[q].w);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(kBarReady + sk));
+                if (!mbar_wait(bar(kBarFull + sv), ((tt + 1) / kSlots) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t vb = sbase + kOffKV + sv * kTileBytes;
+                if ((j + 1) * kTileN > w.rq.prefix) {
+                    for (int k = 0; k < kTileN / 8; ++k) {
+                        const int r = r0 + 8 * k, rr = j * kTileN + r;
+                        if (rr < w.rq.prefix)
+                            continue;
+                        const uint32_t lo_a = vb + r * 128 + ((p ^ (r & 7)) << 4), hi_a = lo_a + kPanelBytes;
+                        if (rr < w.n_valid) {
+                            const __nv_bfloat16 *src = cv + (w.kv_row0 + rr) * kD + 8 * p;
+                            const uint4 lo = __ldg(reinterpret_cast<const uint4 *>(src));
+                            const uint4 hi = __ldg(reinterpret_cast<const uint4 *>(src + kD / 2));
+                            st_shared_v4(lo_a, lo.x, lo.y, lo.z, lo.w);
+                            st_shared_v4(hi_a, hi.x, hi.y, hi.z, hi.w);
+                        } else {
+                            st_shared_v4(lo_a, 0u, 0u, 0u, 0u);
+                            st_shared_v4(hi_a, 0u, 0u, 0u, 0u);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                mbar_arrive(bar(kBarReady + sv));
+            }
+        }
+        if (!ok)
+            flag_timeout(a.err, abort_flag);
     }
 
     tc_fence_before();
@@ -782,30 +1036,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool attention_tc_supported(int dtype, int head_dim) { return dtype == KVR_DTYPE_BF16 && head_dim == kD; }
 
-cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
+template <bool kG>
+static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, cudaStream_t s)
 {
-    if (ta.n_m_blocks == 0)
-        return cudaSuccess;
-    // the shared-memory opt-in is per device
+    // the shared-memory opt-in is per device and per kernel
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(k_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(k_attention_tc<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess)
             return e;
         if (dev < 64)
             attr_set[dev] = true;
     }
-    const int64_t units = (int64_t)ta.n_m_blocks * ta.base.n_layers * ta.base.n_kv_heads;
-    if (units > 0x7fffffff)
-        return cudaErrorInvalidValue;
-    const int grid = (int)(units < ta.n_sms ? units : ta.n_sms);
+    static const CUtensorMap no_map{};
+    static const GatherArgs no_gather{};
+    static const SpanTable no_spans{};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kG ? kThreadsG : kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr;
@@ -813,9 +1065,25 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_attention_tc, *static_cast<const CUtensorMap *>(ta.tmap_q),
+    return cudaLaunchKernelEx(&cfg, k_attention_tc<kG>, *static_cast<const CUtensorMap *>(ta.tmap_q),
                               *static_cast<const CUtensorMap *>(ta.tmap_k),
-                              *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base, *ta.rt, ta.n_m_blocks);
+                              *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base, *ta.rt, ta.n_m_blocks,
+                              kG ? *static_cast<const CUtensorMap *>(ta.tmap_pk) : no_map,
+                              kG ? *static_cast<const CUtensorMap *>(ta.tmap_pv) : no_map,
+                              kG ? *static_cast<const CUtensorMap *>(ta.tmap_bk) : no_map,
+                              kG ? *static_cast<const CUtensorMap *>(ta.tmap_bv) : no_map, kG ? ta.g : no_gather,
+                              kG && ta.st ? *ta.st : no_spans);
+}
+
+cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
+{
+    if (ta.n_m_blocks == 0)
+        return cudaSuccess;
+    const int64_t units = (int64_t)ta.n_m_blocks * ta.base.n_layers * ta.base.n_kv_heads;
+    if (units > 0x7fffffff)
+        return cudaErrorInvalidValue;
+    const int grid = (int)(units < ta.n_sms ? units : ta.n_sms);
+    return ta.gather ? launch_variant<true>(ta, grid, pdl, s) : launch_variant<false>(ta, grid, pdl, s);
 }
 
 }  // namespace kvr

@@ -6,6 +6,10 @@
 
 #include "../../include/kvr.h"
 
+#ifdef __CUDACC__
+#include <cuda_bf16.h>
+#endif
+
 namespace kvr {
 
 // RoPE tables: angle(n, i) = n * theta^(-2i/D) for n in [0, 2^24) is split as
@@ -35,6 +39,37 @@ __device__ __forceinline__ float2 rope_cs(const float2 *__restrict__ tab, int ha
     const float c = fmaf(h.x, l.x, -h.y * l.y);
     const float s = fmaf(h.y, l.x, h.x * l.y);
     return make_float2(c, pos < 0 ? -s : s);
+}
+
+// RoPE rotation of 8 bf16 pairs: lo holds elements [8j, 8j+8) of a row, hi
+// their partners [D/2 + 8j, ...); (c, s) of each pair.  The one definition of
+// the key re-rotation (the stitch kernel and the gathering attention kernel
+// produce the same bits).
+// Per pair: x' = fma(x, c, -(y s)), y' = fma(x, s, y c), rounded once to bf16;
+// computed two lanes at a time with the packed fp32 instructions (each lane
+// is the IEEE operation of the scalar form).
+__device__ __forceinline__ void rotate_bf16x8(uint4 &lo, uint4 &hi, const float *c, const float *s)
+{
+    uint32_t *pl = reinterpret_cast<uint32_t *>(&lo);
+    uint32_t *ph = reinterpret_cast<uint32_t *>(&hi);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        // bf16 pair -> two fp32 lanes (a bf16 is the high half of its fp32)
+        const uint64_t x = ((uint64_t)(pl[w] & 0xffff0000u) << 32) | (uint64_t)(pl[w] << 16);
+        const uint64_t y = ((uint64_t)(ph[w] & 0xffff0000u) << 32) | (uint64_t)(ph[w] << 16);
+        const uint64_t cc = ((uint64_t)__float_as_uint(c[2 * w + 1]) << 32) | __float_as_uint(c[2 * w]);
+        const uint64_t ns = ((uint64_t)__float_as_uint(-s[2 * w + 1]) << 32) | __float_as_uint(-s[2 * w]);
+        const uint64_t ss = ((uint64_t)__float_as_uint(s[2 * w + 1]) << 32) | __float_as_uint(s[2 * w]);
+        uint64_t ys, yc, xo, yo;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(ys) : "l"(y), "l"(ns));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(yc) : "l"(y), "l"(cc));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(xo) : "l"(x), "l"(cc), "l"(ys));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(yo) : "l"(x), "l"(ss), "l"(yc));
+        __nv_bfloat162 xb = __floats2bfloat162_rn(__uint_as_float((uint32_t)xo), __uint_as_float((uint32_t)(xo >> 32)));
+        __nv_bfloat162 yb = __floats2bfloat162_rn(__uint_as_float((uint32_t)yo), __uint_as_float((uint32_t)(yo >> 32)));
+        pl[w] = *reinterpret_cast<uint32_t *>(&xb);
+        ph[w] = *reinterpret_cast<uint32_t *>(&yb);
+    }
 }
 #endif
 
@@ -70,7 +105,7 @@ struct alignas(16) DevReq {
     int32_t q_off;       // first query token (token axis of q / out)
     int32_t q_len;       // Lq_b
     int32_t m_block0;    // first 256-row block of this request (tensor-core path)
-    int32_t pad;
+    int32_t span0;       // first non-empty span of this request (gathering attention)
 };
 
 // Device error word codes (first error wins).
@@ -146,6 +181,20 @@ cudaError_t launch_attention_simt(const AttnArgs &a, const ReqTable &rt, int dty
 // Tensor-core attention (bf16, head_dim 128).  `tmaps` points to two
 // CUtensorMap objects (K then V) describing the cache as a 2-D
 // [rows, head_dim] bf16 tensor.
+// The tensor-core attention's gathering variant (kvr_prefill): K/V tiles are
+// gathered from the pool, seen as a 2-D [entries * L * H_kv * entry_len, D]
+// tensor, through the batch's span table; keys are re-rotated on chip.
+struct SpanTable {
+    DevSpan spans[kInlineEntries];
+};
+struct GatherArgs {
+    const DevSpan *spans;       // the batch's spans in global memory, or NULL: the SpanTable parameter
+    int32_t n_spans;            // non-empty spans of the batch (request b's start at DevReq::span0)
+    int32_t entry_len;          // pool tokens per entry
+    int32_t *pos_ids;           // optional position ids / source map, as kvr_assemble writes them
+    int32_t *src_map;
+};
+
 struct TcAttnArgs {
     AttnArgs base;
     const ReqTable *rt;         // used when base.reqs is NULL
@@ -154,6 +203,13 @@ struct TcAttnArgs {
     const void *tmap_v;
     int32_t n_m_blocks;         // total 256-row query blocks over all requests
     int32_t n_sms;              // persistent grid size bound
+    bool gather;                // K/V from the pool (tmap_pk / tmap_pv, g, st) instead of the cache
+    const void *tmap_pk;        // pool K and V as [rows, D] with a one-row box (gather4)
+    const void *tmap_pv;
+    const void *tmap_bk;        // the same with a 32-row box (runs of consecutive pool rows)
+    const void *tmap_bv;
+    GatherArgs g;
+    const SpanTable *st;
 };
 // `pdl`: the kernel before it on the stream is the assemble kernel of the
 // same prefill (which it may overlap: it reads only the caller's inputs and

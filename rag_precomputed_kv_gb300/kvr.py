@@ -21,6 +21,7 @@ KVR_DTYPE_BF16 = 0
 KVR_DTYPE_FP32 = 1
 KVR_SRC_LOCAL = 1 << 30
 KVR_POSITIONS_COMPOSITE = 1
+KVR_PREFILL_SKIP_PREFIX_CACHE = 2
 
 STATUS = {0: "KVR_OK", 1: "KVR_ERR_INVALID_ARG", 2: "KVR_ERR_OUT_OF_RANGE", 3: "KVR_ERR_UNSUPPORTED",
           4: "KVR_ERR_CUDA", 5: "KVR_ERR_TIMEOUT", 6: "KVR_ERR_DEVICE_CHECK"}
@@ -173,9 +174,12 @@ class Pool:
 
     def prefill(self, span_offsets: Sequence[int], spans, cache_offsets, cache_k, cache_v,
                 q_offsets, q, kq, vq, out, locals_=(), pos_ids=None, src_map=None,
-                composite: bool = False, softmax_scale: float = 0.0, stream=None):
+                composite: bool = False, softmax_scale: float = 0.0, skip_prefix_cache: bool = False,
+                stream=None):
         """kvr_prefill (assemble + query attention in one call); returns the
-        per-request prefix lengths (numpy int32)."""
+        per-request prefix lengths (numpy int32).  skip_prefix_cache: the
+        attention gathers the prefix from the pool and the cache's prefix rows
+        are not written (KVR_PREFILL_SKIP_PREFIX_CACHE)."""
         so, sp, co, loc, batch = _span_args(span_offsets, spans, cache_offsets, locals_)
         qo = _i32(q_offsets)
         plen = np.zeros(max(batch, 1), np.int32)
@@ -183,7 +187,8 @@ class Pool:
                                   ctypes.cast(loc, ctypes.c_void_p) if len(locals_) else None,
                                   len(locals_), _np_ptr(co),
                                   _ptr(cache_k), _ptr(cache_v), _ptr(pos_ids), _ptr(src_map),
-                                  _np_ptr(plen), KVR_POSITIONS_COMPOSITE if composite else 0,
+                                  _np_ptr(plen), (KVR_POSITIONS_COMPOSITE if composite else 0) |
+                                  (KVR_PREFILL_SKIP_PREFIX_CACHE if skip_prefix_cache else 0),
                                   _np_ptr(qo), _ptr(q), _ptr(kq), _ptr(vq), _ptr(out),
                                   float(softmax_scale), _stream_ptr(stream)))
         return plen[:batch]

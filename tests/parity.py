@@ -117,7 +117,7 @@ class Case:
         self.out = torch.full_like(self.t.q, float("nan"))
         self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta)
 
-    def run(self, attention=True, prefill=False):
+    def run(self, attention=True, prefill=False, skip_prefix=False):
         """The hot path through the C ABI: kvr_assemble then
         kvr_query_attention, or (prefill=True) the single kvr_prefill call."""
         import torch
@@ -126,7 +126,8 @@ class Case:
             plen = self.pool.prefill(self.span_offsets, np.concatenate(self.spans), self.cache_offsets,
                                      self.cache_k, self.cache_v, self.q_offsets, self.t.q, self.t.kq,
                                      self.t.vq, self.out, locals_=self.locals, pos_ids=self.pos_ids,
-                                     src_map=self.src_map, composite=self.composite)
+                                     src_map=self.src_map, composite=self.composite,
+                                     skip_prefix_cache=skip_prefix)
             assert np.array_equal(plen, self.prefix)
             torch.cuda.synchronize()
             self.pool.check()
@@ -162,13 +163,16 @@ class Case:
 
 
 def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requests=None,
-                    attention=True, composite=False, seed_units=0, case=None, prefill=False):
+                    attention=True, composite=False, seed_units=0, case=None, prefill=False,
+                    skip_prefix=False):
     """Run one configuration and compare with the oracle; returns a summary
-    dict with ``ok`` and the worst errors."""
+    dict with ``ok`` and the worst errors.  skip_prefix: kvr_prefill with
+    KVR_PREFILL_SKIP_PREFIX_CACHE, whose cache prefix rows must stay as they
+    were (NaN), everything else compared as usual."""
     import torch
     cfg = cfg or W.CONFIGS[cid]
     case = case or Case(cfg, device=device, composite=composite)
-    case.run(attention=attention, prefill=prefill)
+    case.run(attention=attention, prefill=prefill, skip_prefix=skip_prefix)
     rng = np.random.default_rng(1234 + seed_units)
     req_ids = range(len(case.reqs)) if requests is None else requests
     L, H, Hq, D = cfg.n_layers, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
@@ -198,12 +202,17 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
             res["maps"] = f"request {b}: position / source map mismatch"
         ck = to_np64(case.cache_block("k", b)[units])
         cv = to_np64(case.cache_block("v", b)[units])
-        if not np.array_equal(cv[:, :P], V_ref[0]):
-            res["ok"] = False
-            res["v"] = f"request {b}: gathered V differs"
-        okk, ratio = k_within_tolerance(ck[:, :P], K_ref[0], cfg.dtype)
-        res["k_ratio"] = max(res["k_ratio"], ratio)
-        res["ok"] &= okk
+        if skip_prefix:
+            if not (np.isnan(ck[:, :P]).all() and np.isnan(cv[:, :P]).all()):
+                res["ok"] = False
+                res["prefix"] = f"request {b}: prefix rows were written"
+        else:
+            if not np.array_equal(cv[:, :P], V_ref[0]):
+                res["ok"] = False
+                res["v"] = f"request {b}: gathered V differs"
+            okk, ratio = k_within_tolerance(ck[:, :P], K_ref[0], cfg.dtype)
+            res["k_ratio"] = max(res["k_ratio"], ratio)
+            res["ok"] &= okk
         if attention:
             qo = int(case.q_offsets[b])
             li = [u // H for u in units]

@@ -1,0 +1,107 @@
+"""GPU parity of kvr_prefill with KVR_PREFILL_SKIP_PREFIX_CACHE: the attention
+gathers the prefix keys and values straight from the pool (re-rotating the
+keys on chip) and leaves the cache's prefix rows alone.
+
+Checked against the oracle (attention output, appended query rows, position
+ids and source map) and, bit for bit, against the stitched path: the key
+rotation is the same arithmetic and the MMAs run in the same order, so the
+outputs must be identical.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from parity import Case, run_parity_case
+from rag_precomputed_kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+EDGE = W.Config("edge", 2, 8, 2, 128, "bf16", 1e4, 4, 96, 5, 7, 1, 77, "random")
+
+
+def _custom(cfg, span_lists):
+    reqs = [W.Request(np.asarray(rows, np.int32).reshape(-1, 3), 0) for rows in span_lists]
+    return dataclasses.replace(cfg, batch=len(reqs)), reqs
+
+
+def _bits(t):
+    import torch
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+
+def _case(name):
+    if name == "cfg2":
+        return W.CONFIGS[2], None, {}
+    if name == "cfg2_composite":
+        return W.CONFIGS[2], None, {"composite": True}
+    if name == "cfg3":
+        return W.CONFIGS[3], None, {"sample_units": 6, "requests": [0, 7, 15]}
+    if name == "cfg5":
+        return W.CONFIGS[5], None, {"sample_units": 3, "requests": [0, 31, 63]}
+    if name == "edges":
+        # a request without prefix, a prompt-only one, length-1 spans, a span
+        # ending at the chunk end, overlapping spans
+        pid = EDGE.n_chunks
+        cfg, reqs = _custom(dataclasses.replace(EDGE, query_len=21),
+                            [[], [[pid, 0, 5]], [[0, 95, 96], [1, 0, 1], [2, 10, 96]],
+                             [[3, 3, 50], [3, 20, 60], [pid, 0, 5]]])
+        return cfg, reqs, {}
+    if name == "many_requests":
+        base = dataclasses.replace(EDGE, prompt_len=0, query_len=3)
+        rng = np.random.default_rng(3)
+        lists = [[[int(rng.integers(0, base.n_chunks)), 4, 4 + int(rng.integers(1, 70))]
+                  for _ in range(int(rng.integers(1, 4)))] for _ in range(70)]
+        cfg, reqs = _custom(base, lists)
+        return cfg, reqs, {"requests": [0, 1, 35, 68, 69]}
+    raise ValueError(name)
+
+
+@pytest.mark.parametrize("name", ["cfg2", "cfg2_composite", "cfg3", "cfg5", "edges", "many_requests"])
+def test_gathering_prefill_matches_oracle_and_stitched_path(name):
+    import torch
+    cfg, reqs, kw = _case(name)
+    composite = kw.pop("composite", False)
+    case = Case(cfg, reqs=reqs, composite=composite)
+    res = run_parity_case(cfg=cfg, case=case, prefill=True, skip_prefix=True, composite=composite, **kw)
+    assert res["ok"], res
+    got = [case.out.clone(), case.pos_ids.clone(), case.src_map.clone()]
+    # the query rows of every block, appended by the query prologue
+    qrows = []
+    for b in range(len(case.reqs)):
+        P, lq = int(case.prefix[b]), cfg.query_len
+        qrows.append((case.cache_block("k", b)[:, P:P + lq].clone(), case.cache_block("v", b)[:, P:P + lq].clone()))
+    for x in (case.out, case.cache_k, case.cache_v):
+        x.fill_(float("nan"))
+    case.pos_ids.fill_(-1)
+    case.src_map.fill_(-1)
+    case.run(prefill=True)
+    want = [case.out, case.pos_ids, case.src_map]
+    for g_, w_ in zip(got, want):
+        assert torch.equal(_bits(g_), _bits(w_))
+    for b, (k, v) in enumerate(qrows):
+        P, lq = int(case.prefix[b]), cfg.query_len
+        assert torch.equal(_bits(k), _bits(case.cache_block("k", b)[:, P:P + lq]))
+        assert torch.equal(_bits(v), _bits(case.cache_block("v", b)[:, P:P + lq]))
+
+
+def test_gathering_prefill_is_deterministic():
+    import torch
+    case = Case(W.CONFIGS[2], prerotate=False)
+    case.run(prefill=True, skip_prefix=True)
+    first = case.out.clone()
+    for _ in range(3):
+        case.run(prefill=True, skip_prefix=True)
+        assert torch.equal(_bits(case.out), _bits(first))
+
+
+def test_gathering_prefill_refuses_what_it_cannot_gather():
+    """fp32 pools and request-local sources take the stitched path only."""
+    from rag_precomputed_kv_gb300 import kvr
+    F = W.LOCAL_FLAG
+    reqs = [W.Request(np.asarray([[0, 0, 96], [F | 0, 0, 8]], np.int32), 8)]
+    for cfg, rq in ((W.CONFIGS[1], None), (dataclasses.replace(EDGE, prompt_len=0, batch=1), reqs)):
+        case = Case(cfg, reqs=rq)
+        with pytest.raises(kvr.KvrError) as e:
+            case.run(prefill=True, skip_prefix=True)
+        assert e.value.status == 3, cfg.name
