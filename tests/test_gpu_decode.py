@@ -1,0 +1,105 @@
+"""Decode over the stitched cache (the step after prefill): each step is one
+query token per request, appended at row n_b (position n_b) of its cache
+block and attending to rows 0..n_b -- kvr_query_attention with one token per
+request.  Several steps in a row after a kvr_prefill, checked against the
+oracle, which builds its own cache (stitched prefix, query rows, earlier
+decoded rows) from the same seeded inputs and never reads the GPU's.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+from parity import Case, attn_within_tolerance, k_within_tolerance, to_np64
+from rag_precomputed_kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+STEPS = 3
+
+
+def _run(cfg, reqs, sample_units=None):
+    import torch
+    case = Case(cfg, reqs=reqs, spare_rows=STEPS + 2)
+    case.run(prefill=True)
+    L, H, Hq, D = cfg.n_layers, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
+    G, lq, B = Hq // H, cfg.query_len, len(case.reqs)
+    dev = case.cache_k.device
+    rng = np.random.default_rng(7)
+    units = list(range(case.LH)) if sample_units is None else sorted(
+        rng.choice(case.LH, size=sample_units, replace=False).tolist())
+    li = [u // H for u in units]
+    hi = [u % H for u in units]
+    # the oracle's cache of every sampled unit: stitched prefix + query rows
+    kc, vc = [], []
+    for b in range(B):
+        spans = case.spans[b]
+        srcs = {int(s): case.source(int(s), units) for s in np.unique(spans[:, 0])}
+        if srcs:
+            K, V, pz = oracle.assemble(srcs, spans, cfg.rope_theta)
+            K, V = K[0], V[0]
+        else:
+            K = V = np.zeros((len(units), 0, D))
+        P = K.shape[1]
+        qo = int(case.q_offsets[b])
+        kq = to_np64(case.t.kq[:, qo:qo + lq])
+        vq = to_np64(case.t.vq[:, qo:qo + lq])
+        kqu = np.stack([kq[l, :, h, :] for l, h in zip(li, hi)])
+        vqu = np.stack([vq[l, :, h, :] for l, h in zip(li, hi)])
+        kc.append(np.concatenate([K, oracle.rope(kqu, (P + np.arange(lq, dtype=np.float64))[None, :],
+                                                  cfg.rope_theta)], axis=1))
+        vc.append(np.concatenate([V, vqu], axis=1))
+    g = torch.Generator(device=dev)
+    g.manual_seed(99)
+    dt = case.t.q.dtype
+    qoffs = np.arange(B + 1, dtype=np.int32)
+    worst = (0.0, 0.0)
+    for step in range(STEPS):
+        n = np.array([kc[b].shape[1] for b in range(B)], np.int32)   # rows before this step
+        q1 = torch.randn((L, B, Hq, D), generator=g, device=dev).to(dt)
+        k1 = torch.randn((L, B, H, D), generator=g, device=dev).to(dt)
+        v1 = torch.randn((L, B, H, D), generator=g, device=dev).to(dt)
+        o1 = torch.full_like(q1, float("nan"))
+        case.pool.query_attention(case.cache_offsets, n, qoffs, q1, k1, v1, case.cache_k, case.cache_v, o1)
+        torch.cuda.synchronize()
+        case.pool.check()
+        q1n, k1n, v1n, o1n = (to_np64(x) for x in (q1, k1, v1, o1))
+        for b in range(B):
+            qu = np.stack([q1n[l, b, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])   # [U, 1, G, D]
+            ku = np.stack([k1n[l, b, h][None] for l, h in zip(li, hi)])                    # [U, 1, D]
+            vu = np.stack([v1n[l, b, h][None] for l, h in zip(li, hi)])
+            o_ref = oracle.query_attention(kc[b], vc[b], qu, ku, vu, cfg.rope_theta)
+            o_gpu = np.stack([o1n[l, b, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])
+            ok, mx, rel = attn_within_tolerance(o_gpu, o_ref, cfg.dtype)
+            assert ok, (step, b, mx, rel)
+            worst = (max(worst[0], mx), max(worst[1], rel))
+            # the appended row: K rotated at n_b, V copied
+            blk_k = to_np64(case.cache_block("k", b)[units])
+            blk_v = to_np64(case.cache_block("v", b)[units])
+            k_new = oracle.rope(ku, float(n[b]), cfg.rope_theta)
+            okk, _ = k_within_tolerance(blk_k[:, n[b]:n[b] + 1], k_new, cfg.dtype)
+            assert okk, (step, b)
+            assert np.array_equal(blk_v[:, n[b]:n[b] + 1], vu), (step, b)
+            kc[b] = np.concatenate([kc[b], k_new], axis=1)
+            vc[b] = np.concatenate([vc[b], vu], axis=1)
+    return worst
+
+
+EDGE = W.Config("edge", 2, 8, 2, 128, "bf16", 1e4, 4, 96, 5, 7, 1, 77, "random")
+
+
+def test_decode_steps_after_prefill_bf16_tensor_cores():
+    pid = EDGE.n_chunks
+    reqs = [W.Request(np.asarray(r, np.int32).reshape(-1, 3), 0) for r in
+            ([[pid, 0, 5], [0, 0, 96], [2, 10, 60]], [[1, 3, 90]], [])]
+    cfg = dataclasses.replace(EDGE, batch=len(reqs), query_len=9)
+    _run(cfg, reqs)
+
+
+def test_decode_steps_fp32_cuda_cores():
+    _run(W.CONFIGS[1], None)
+
+
+def test_decode_steps_default_workload_sampled():
+    _run(W.CONFIGS[2], None, sample_units=6)
