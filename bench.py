@@ -195,6 +195,12 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def asm_bytes_of(cfg, wl) -> int:
+    """Algorithmic bytes of one stitch: every stitched K and V row read once
+    and written once."""
+    return W.assemble_bytes(cfg, wl.reqs)
+
+
 def job_throughput(units_per_rank: float, seconds: float, world: int) -> float:
     """Whole-job throughput: every rank's units over the slowest rank's time."""
     return units_per_rank * world / max_over_ranks(seconds, world)
@@ -322,6 +328,37 @@ def run_kvr(args):
               "what": "kvr_query_attention with one token per request (append at P_b + Lq, attend to "
                       "all rows); bytes = K and V rows read once"}
 
+    # ---- the stitch from a pool kept in pinned host memory (read over the
+    # CPU-GPU link through its unified address) ----
+    host_pool = None
+    try:
+        hk, hv = wl.t.pool_k.cpu().pin_memory(), wl.t.pool_v.cpu().pin_memory()
+    except RuntimeError:
+        hk = hv = None
+    if hk is not None:
+        hp = K.Pool(hk, hv, cfg.n_q_heads, cfg.rope_theta)
+        n_h = min(args.steps, 200)
+        h0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
+        h1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
+        for k in range(args.warmup + n_h):
+            flush.zero_()
+            if k >= args.warmup:
+                h0[k - args.warmup].record(stream)
+            hp.assemble(wl.span_offsets, wl.spans, wl.cache_offsets, wl.cache_k, wl.cache_v,
+                        locals_=wl.locals)
+            if k >= args.warmup:
+                h1[k - args.warmup].record(stream)
+        torch.cuda.synchronize()
+        hp.check()
+        h_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(h0, h1))
+        host_read = asm_bytes_of(cfg, wl) // 2
+        host_pool = {"assemble_us": round(h_ms * 1e3, 2), "steps": n_h,
+                     "host_read_gbs": round(host_read / (h_ms * 1e-3) / 1e9, 1),
+                     "what": "kvr_assemble from a pool in pinned host memory: K/V rows read over the "
+                             "CPU-GPU link, stitched cache written to HBM"}
+        hp.close()
+        del hk, hv
+
     # ---- end to end through the public API with host buffers ----
     q_h = wl.t.q.cpu().pin_memory()
     kq_h = wl.t.kq.cpu().pin_memory()
@@ -402,6 +439,7 @@ def run_kvr(args):
         "gpu_launches": 3 * args.steps,
         "skip_prefix_cache": gather,
         "decode": decode,
+        "host_pool": host_pool,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -70,6 +70,14 @@ enum { KVR_DTYPE_BF16 = 0, KVR_DTYPE_FP32 = 1 };
  * TurboRAG blog, "Position ID", Figure 5. */
 #define KVR_POSITIONS_COMPOSITE 1u
 
+/* kvr_pool_desc flag: the pool keeps its keys before RoPE (the raw key
+ * projections), and stitching applies RoPE at each token's new position
+ * instead of turning stored keys by delta = position - start (TurboRAG blog,
+ * "Position ID": keep the un-rotated K, re-apply RoPE at the new position
+ * when stitching).  Applies to pool entries; request-local sources keep
+ * their keys rotated at local positions 0..len-1. */
+#define KVR_POOL_KEYS_UNROTATED 1u
+
 /* kvr_prefill flag: no decode follows, so the stitched prefix is not kept.
  * The prefix rows [0, P_b) of the cache blocks are left as they are; the
  * attention gathers the prefix keys and values straight from the pool and
@@ -93,10 +101,12 @@ typedef struct {
     int32_t n_kv_heads;
     int32_t head_dim;     /* 64 or 128 (128 for the tensor-core attention path) */
     int32_t dtype;        /* KVR_DTYPE_BF16 or KVR_DTYPE_FP32                   */
-    int32_t reserved;     /* must be 0                                          */
+    int32_t flags;        /* 0 or KVR_POOL_KEYS_UNROTATED                       */
     int64_t n_entries;    /* chunks (plus prompt entries) in the pool           */
     int64_t entry_len;    /* tokens per entry                                   */
-    const void *k;        /* device, caller-owned, valid until unregister       */
+    const void *k;        /* caller-owned, valid until unregister: device memory,
+                           * or pinned host memory the GPU reads through its
+                           * unified address (over NVLink-C2C on Grace boards) */
     const void *v;
     int64_t stride[4];    /* elements: entry, layer, head, token; multiples of 8 */
     double rope_theta;    /* RoPE base (e.g. 1e6 for Qwen2)                     */
@@ -216,7 +226,7 @@ KVR_API kvr_status kvr_query_attention(kvr_pool_t pool, int32_t batch, const int
  * overlaps it.  The timing hook (kvr_set_timing_events) serializes them.
  *
  * flags: KVR_POSITIONS_COMPOSITE as in kvr_assemble; KVR_PREFILL_SKIP_PREFIX_CACHE
- * (above) needs a bf16 pool with head_dim 128, laid out contiguously
+ * (above) needs a bf16 pool in device memory with head_dim 128, laid out contiguously
  * ([entries][L][H_kv][entry_len][D], fewer than 2^31 rows), spans from the
  * pool only (n_locals = 0) and the tensor-core attention; otherwise the call
  * returns KVR_ERR_UNSUPPORTED before any work.

@@ -153,7 +153,8 @@ def rope(x, shift, theta: float) -> np.ndarray:
     return out.reshape(x.shape)
 
 
-def assemble(sources, spans, theta: float, first_pos: int = 0, composite: bool = False):
+def assemble(sources, spans, theta: float, first_pos: int = 0, composite: bool = False,
+             unrotated=()):
     """Stitch one request's prefix.
 
     ``sources`` maps a source id to a pair ``(k, v)`` of arrays
@@ -161,6 +162,10 @@ def assemble(sources, spans, theta: float, first_pos: int = 0, composite: bool =
     positions 0..n_tokens-1 (any float dtype; converted exactly to fp64).
     Returns ``(K, V, Positions)`` with K, V fp64 ``[L, H_kv, P, D]``: span i's
     keys rotated by ``delta_i``, its values copied.
+
+    Sources named in ``unrotated`` hold their keys before RoPE (TurboRAG
+    blog, "Position ID": keep the un-rotated K and apply RoPE at the new
+    position when stitching): their tokens are rotated at their positions.
     """
     pz = positions(spans, first_pos, composite)
     sp = np.asarray(spans, dtype=np.int64).reshape(-1, 3)
@@ -174,8 +179,12 @@ def assemble(sources, spans, theta: float, first_pos: int = 0, composite: bool =
         if n <= 0:
             continue
         k_src, v_src = sources[int(src)]
-        K[:, :, row:row + n, :] = rope(np.asarray(k_src[:, :, s:e, :], dtype=np.float64),
-                                       float(pz.delta[i]), theta)
+        k_rows = np.asarray(k_src[:, :, s:e, :], dtype=np.float64)
+        if int(src) in unrotated:
+            at = pz.pos[row:row + n].astype(np.float64)
+            K[:, :, row:row + n, :] = rope(k_rows, np.broadcast_to(at, k_rows.shape[:-1]), theta)
+        else:
+            K[:, :, row:row + n, :] = rope(k_rows, float(pz.delta[i]), theta)
         V[:, :, row:row + n, :] = np.asarray(v_src[:, :, s:e, :], dtype=np.float64)
         row += n
     return K, V, pz

@@ -163,8 +163,8 @@ extern "C" kvr_status kvr_pool_register(const kvr_pool_desc *desc, kvr_pool_t *o
     if (d.n_entries < 1 || d.entry_len < 1 || d.entry_len > kMaxPosition)
         return fail(KVR_ERR_INVALID_ARG, "n_entries %lld, entry_len %lld",
                     (long long)d.n_entries, (long long)d.entry_len);
-    if (d.reserved != 0)
-        return fail(KVR_ERR_INVALID_ARG, "reserved field must be 0");
+    if (d.flags & ~KVR_POOL_KEYS_UNROTATED)
+        return fail(KVR_ERR_INVALID_ARG, "unknown pool flags 0x%x", (unsigned)d.flags);
     if (!d.k || !d.v)
         return fail(KVR_ERR_INVALID_ARG, "pool k / v is NULL");
     if (!aligned16(d.k) || !aligned16(d.v))
@@ -392,6 +392,10 @@ static kvr_status asm_validate(const kvr_pool &p, int32_t batch, const int32_t *
                 d.delta = (int32_t)(pos0 - s.start);
                 d.cap = (int32_t)cap;
                 d.dstep = 0;
+                if (!(s.src & KVR_SRC_LOCAL) && (p.d.flags & KVR_POOL_KEYS_UNROTATED)) {
+                    d.delta = (int32_t)pos0;   // token t turns by its position pos0 + t
+                    d.dstep = 1;
+                }
                 pl.ds.push_back(d);
             }
             row += len;
@@ -893,6 +897,11 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
         // the attention gathers the prefix from the pool; nothing stitched
         if (!use_tensor_cores(*p))
             return fail(KVR_ERR_UNSUPPORTED, "KVR_PREFILL_SKIP_PREFIX_CACHE needs the tensor-core attention");
+        cudaPointerAttributes pa{};
+        if (cudaPointerGetAttributes(&pa, p->d.k) != cudaSuccess || pa.type != cudaMemoryTypeDevice) {
+            cudaGetLastError();
+            return fail(KVR_ERR_UNSUPPORTED, "KVR_PREFILL_SKIP_PREFIX_CACHE needs the pool in device memory");
+        }
         if (qp.T == 0)
             return KVR_OK;
         GatherLaunch gl;

@@ -763,7 +763,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                                 const DevSpan &sp = spans[cur];
                                 const int off = rr - sp.row;
                                 rows[k] = (int)((int64_t)sp.src * e_rows + lh_row + sp.start + off);
-                                d = sp.delta;
+                                d = sp.dstep ? sp.delta + off : sp.delta;
                                 if (maps) {
                                     if (g.pos_ids)
                                         g.pos_ids[sp.flat0 + off] = sp.pos0 + off;

@@ -68,7 +68,7 @@ extern "C" kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t ba
     if (d.head_dim != 64 && d.head_dim != 128)
         return na_fail(KVR_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
     if (d.n_layers < 1 || d.n_kv_heads < 1 || d.n_q_heads < 1 || d.n_q_heads % d.n_kv_heads ||
-        d.n_entries < 1 || d.entry_len < 1 || d.entry_len > kMaxPosition || d.reserved != 0 || !d.k ||
+        d.n_entries < 1 || d.entry_len < 1 || d.entry_len > kMaxPosition || (d.flags & ~KVR_POOL_KEYS_UNROTATED) != 0 || !d.k ||
         !d.v || !na_aligned16(d.k) || !na_aligned16(d.v) || !(d.rope_theta > 1.0) ||
         !std::isfinite(d.rope_theta))
         return na_fail(KVR_ERR_INVALID_ARG, "invalid pool descriptor");
@@ -147,6 +147,10 @@ extern "C" kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t ba
                 t.delta = (int32_t)(pos0 - s.start);
                 t.cap = (int32_t)cap;
                 t.dstep = 0;
+                if (!(s.src & KVR_SRC_LOCAL) && (d.flags & KVR_POOL_KEYS_UNROTATED)) {
+                    t.delta = (int32_t)pos0;   // token t turns by its position pos0 + t
+                    t.dstep = 1;
+                }
             }
             row += len;
             flat += len;

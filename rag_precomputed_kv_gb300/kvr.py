@@ -22,6 +22,7 @@ KVR_DTYPE_FP32 = 1
 KVR_SRC_LOCAL = 1 << 30
 KVR_POSITIONS_COMPOSITE = 1
 KVR_PREFILL_SKIP_PREFIX_CACHE = 2
+KVR_POOL_KEYS_UNROTATED = 1
 
 STATUS = {0: "KVR_OK", 1: "KVR_ERR_INVALID_ARG", 2: "KVR_ERR_OUT_OF_RANGE", 3: "KVR_ERR_UNSUPPORTED",
           4: "KVR_ERR_CUDA", 5: "KVR_ERR_TIMEOUT", 6: "KVR_ERR_DEVICE_CHECK"}
@@ -41,7 +42,7 @@ class KvrError(RuntimeError):
 class PoolDesc(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("n_entries", ctypes.c_int64), ("entry_len", ctypes.c_int64),
                 ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("stride", ctypes.c_int64 * 4), ("rope_theta", ctypes.c_double)]
@@ -133,17 +134,19 @@ class Pool:
 
     ``k``, ``v``: device tensors ``[entries, layers, kv_heads, entry_len, head_dim]``
     (any strides with head_dim contiguous), keys rotated at entry-local
-    positions.  The tensors must outlive the pool.
+    positions (or, with ``keys_unrotated``, before RoPE).  The tensors must
+    outlive the pool.
     """
 
-    def __init__(self, k, v, n_q_heads: int, rope_theta: float):
+    def __init__(self, k, v, n_q_heads: int, rope_theta: float, keys_unrotated: bool = False):
         import torch
         lib = load()
         assert k.shape == v.shape and k.stride() == v.stride() and k.dtype == v.dtype
         assert k.stride(-1) == 1
         dt = {torch.bfloat16: KVR_DTYPE_BF16, torch.float32: KVR_DTYPE_FP32}[k.dtype]
         E, L, H, T, D = k.shape
-        d = PoolDesc(L, n_q_heads, H, D, dt, 0, E, T, _ptr(k), _ptr(v),
+        d = PoolDesc(L, n_q_heads, H, D, dt, KVR_POOL_KEYS_UNROTATED if keys_unrotated else 0, E, T,
+                     _ptr(k), _ptr(v),
                      (ctypes.c_int64 * 4)(*k.stride()[:4]), float(rope_theta))
         h = ctypes.c_void_p()
         _raise(lib.kvr_pool_register(ctypes.byref(d), ctypes.byref(h)))

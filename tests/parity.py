@@ -68,16 +68,17 @@ class Case:
     """Inputs, layout and GPU results of one configuration."""
 
     def __init__(self, cfg: W.Config, device="cuda:0", prerotate=None, reqs=None, composite=False,
-                 spare_rows=0):
+                 spare_rows=0, keys_unrotated=False):
         import torch
         from rag_precomputed_kv_gb300 import kvr
         self.cfg, self.device, self.composite = cfg, device, composite
+        self.keys_unrotated = keys_unrotated   # pool keys kept before RoPE
         self.reqs = reqs if reqs is not None else W.draw_spans(cfg)
         self.t = W.make_tensors(cfg, self.reqs, device=device)
         # explicit pre-rotation of the pool keys at chunk-local positions (the
         # offline forward pass of CoinRAG 2.1), done by the oracle in fp64
         if prerotate is None:
-            prerotate = cfg.pool_bytes() < 2e9
+            prerotate = cfg.pool_bytes() < 2e9 and not keys_unrotated
         self.raw_pool_k = None
         if prerotate:
             raw = to_np64(self.t.pool_k)
@@ -115,7 +116,8 @@ class Case:
         self.pos_ids = torch.full((max(tot, 1),), -1, dtype=torch.int32, device=device)
         self.src_map = torch.full((max(tot, 1), 2), -1, dtype=torch.int32, device=device)
         self.out = torch.full_like(self.t.q, float("nan"))
-        self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta)
+        self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta,
+                             keys_unrotated=keys_unrotated)
 
     def run(self, attention=True, prefill=False, skip_prefix=False):
         """The hot path through the C ABI: kvr_assemble then
@@ -188,7 +190,9 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
         spans = case.spans[b]
         srcs = {int(s): case.source(int(s), units) for s in np.unique(spans[:, 0])}
         if srcs:
-            K_ref, V_ref, pz = oracle.assemble(srcs, spans, cfg.rope_theta, composite=composite)
+            unrot = {s for s in srcs if not (s & W.LOCAL_FLAG)} if case.keys_unrotated else ()
+            K_ref, V_ref, pz = oracle.assemble(srcs, spans, cfg.rope_theta, composite=composite,
+                                               unrotated=unrot)
         else:   # a request without any prefix
             K_ref = V_ref = np.zeros((1, len(units), 0, D))
             pz = oracle.positions(spans, 0, composite)

@@ -48,7 +48,7 @@ def test_status_strings(lib):
 def _desc(**kw):
     from rag_precomputed_kv_gb300 import kvr
     d = dict(n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128, dtype=kvr.KVR_DTYPE_BF16,
-             reserved=0, n_entries=4, entry_len=512, k=0x10000, v=0x20000,
+             flags=0, n_entries=4, entry_len=512, k=0x10000, v=0x20000,
              stride=(2 * 2 * 512 * 128, 2 * 512 * 128, 512 * 128, 128), rope_theta=1e6)
     d.update(kw)
     s = d.pop("stride")
@@ -65,7 +65,7 @@ def _register(lib, desc):
 
 @pytest.mark.parametrize("bad,status", [
     (dict(dtype=7), 3), (dict(head_dim=96), 3), (dict(n_q_heads=7), 1), (dict(n_layers=0), 1),
-    (dict(n_entries=0), 1), (dict(reserved=1), 1), (dict(k=0), 1), (dict(k=0x10008), 1),
+    (dict(n_entries=0), 1), (dict(flags=2), 1), (dict(k=0), 1), (dict(k=0x10008), 1),
     (dict(rope_theta=0.5), 1), (dict(stride=(8, 8, 8, 12)), 1), (dict(stride=(-8, 8, 8, 8)), 1),
 ])
 def test_register_rejects_bad_descriptors(lib, bad, status):

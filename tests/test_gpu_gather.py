@@ -105,3 +105,18 @@ def test_gathering_prefill_refuses_what_it_cannot_gather():
         with pytest.raises(kvr.KvrError) as e:
             case.run(prefill=True, skip_prefix=True)
         assert e.value.status == 3, cfg.name
+
+
+def test_gathering_prefill_with_pool_keys_kept_before_rope():
+    """The gathering attention turns each pool row by its position when the
+    pool keeps its keys before RoPE; output still bit-identical to the
+    stitched path."""
+    import torch
+    cfg = W.CONFIGS[2]
+    case = Case(cfg, keys_unrotated=True)
+    res = run_parity_case(cfg=cfg, case=case, prefill=True, skip_prefix=True)
+    assert res["ok"], res
+    got = case.out.clone()
+    case.out.fill_(float("nan"))
+    case.run(prefill=True)
+    assert torch.equal(_bits(got), _bits(case.out))

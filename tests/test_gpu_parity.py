@@ -217,3 +217,45 @@ def test_config4_inline_docs_sampled():
 
 def test_config5_serving_pool_sampled():
     _ok(run_parity_case(5, sample_units=3, requests=[0, 31, 63]))
+
+
+@pytest.mark.parametrize("variant", ["fp32", "fp32_composite", "bf16_with_locals", "cfg2_prefill"])
+def test_pool_keys_kept_before_rope(variant):
+    """A pool registered with KVR_POOL_KEYS_UNROTATED: stitching applies RoPE
+    at each token's position (request-local sources stay rotated at their
+    local positions)."""
+    if variant.startswith("fp32"):
+        cfg, reqs, composite = W.CONFIGS[1], None, variant.endswith("composite")
+    elif variant == "bf16_with_locals":
+        base = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, prompt_len=0, query_len=11)
+        F = W.LOCAL_FLAG
+        cfg, reqs = _custom(base, [[[0, 3, 90], [F | 0, 0, 8], [2, 0, 40]], [[3, 10, 96], [1, 0, 5]]],
+                            local_lens={0: 8})
+        composite = False
+    else:
+        cfg, reqs, composite = W.CONFIGS[2], None, False
+    case = Case(cfg, reqs=reqs, composite=composite, keys_unrotated=True)
+    _ok(run_parity_case(cfg=cfg, case=case, composite=composite, prefill=variant == "cfg2_prefill"))
+
+
+def test_pool_in_pinned_host_memory():
+    """A pool kept in pinned host memory (read by the stitch kernel through
+    its unified address): same results, bit for bit, as the device pool."""
+    import torch
+    from rag_precomputed_kv_gb300 import kvr
+    cfg = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=13)
+    pid = cfg.n_chunks
+    cfg, reqs = _custom(cfg, [[[pid, 0, 5], [0, 3, 90], [2, 0, 96]], [[1, 7, 60], [3, 0, 96]]])
+    case = Case(cfg, reqs=reqs)
+    case.run(prefill=True)
+    want = [x.clone() for x in (case.out, case.cache_k, case.cache_v)]
+    hk, hv = case.t.pool_k.cpu().pin_memory(), case.t.pool_v.cpu().pin_memory()
+    case.pool = kvr.Pool(hk, hv, cfg.n_q_heads, cfg.rope_theta)
+    for x in (case.out, case.cache_k, case.cache_v):
+        x.fill_(float("nan"))
+    _ok(run_parity_case(cfg=cfg, case=case, prefill=True))
+    for g_, w_ in zip((case.out, case.cache_k, case.cache_v), want):
+        assert torch.equal(g_.view(torch.int16), w_.view(torch.int16))
+    with pytest.raises(kvr.KvrError) as e:      # the gathering attention wants device memory
+        case.run(prefill=True, skip_prefix=True)
+    assert e.value.status == 3

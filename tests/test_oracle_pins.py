@@ -192,6 +192,34 @@ def pin_assemble_is_rope_at_target():
     assert row == pz.total
 
 
+def pin_unrotated_sources_take_rope_at_their_positions():
+    """Keys kept before RoPE and rotated at the stitched positions equal the
+    same keys cached at chunk-local positions and re-rotated by delta (the
+    rotation composes: R(target) k = R(delta) R(local) k), in both position
+    schemes; values are untouched."""
+    rng = np.random.default_rng(9)
+    L, H, n, D, theta = 2, 2, 20, 16, 1e4
+    raw = {c: rng.standard_normal((L, H, n, D)) for c in range(3)}
+    vals = {c: rng.standard_normal((L, H, n, D)) for c in range(3)}
+    local = np.arange(n, dtype=np.float64)
+    cached = {c: rot_complex(raw[c], local[None, None, :], theta) for c in raw}
+    spans = np.array([[1, 4, 12], [0, 0, 20], [2, 19, 20], [1, 0, 3]])
+    for composite in (False, True):
+        Kr, Vr, pz = oracle.assemble({c: (raw[c], vals[c]) for c in raw}, spans, theta, first_pos=3,
+                                     composite=composite, unrotated=set(raw))
+        Kc, Vc, _ = oracle.assemble({c: (cached[c], vals[c]) for c in raw}, spans, theta, first_pos=3,
+                                    composite=composite)
+        np.testing.assert_allclose(Kr, Kc, atol=1e-12)
+        assert np.array_equal(Vr, Vc)
+        # and, written out: each token's raw key rotated at its position id
+        row = 0
+        for c, s, e in spans:
+            for t in range(s, e):
+                np.testing.assert_allclose(Kr[:, :, row], rot_complex(raw[c][:, :, t], float(pz.pos[row]), theta),
+                                           atol=1e-12)
+                row += 1
+
+
 # ----------------------------------------------------------------------------
 # attention
 # ----------------------------------------------------------------------------
@@ -254,7 +282,8 @@ def pin_attention_zero_query_is_mean():
 PINS = [pin_fig5_worked_example, pin_delta_formula_and_brute_force, pin_composite_positions,
         pin_rope_identity, pin_rope_vs_complex, pin_rope_closed_form,
         pin_rope_composition_and_norm, pin_rope_relative_position,
-        pin_assemble_is_rope_at_target, pin_attention_single_chunk_is_causal_attention,
+        pin_assemble_is_rope_at_target, pin_unrotated_sources_take_rope_at_their_positions,
+        pin_attention_single_chunk_is_causal_attention,
         pin_attention_single_visible_key, pin_attention_zero_query_is_mean]
 
 
