@@ -93,6 +93,7 @@ struct kvr_pool {
     size_t q_rot_cap = 0;
     cudaEvent_t q_rot_done = nullptr;
     bool q_rot_used = false;
+    float *part = nullptr;      // half-unit states of the attention's last wave (ordered like q_rot)
     cudaEvent_t timing[6] = {};  // optional kernel timing events (caller-owned)
     bool timed = false;
 
@@ -243,6 +244,8 @@ extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
     }
     if (p->q_rot)
         cudaFree(p->q_rot);
+    if (p->part)
+        cudaFree(p->part);
     if (p->rope)
         cudaFree(p->rope);
     if (p->err)
@@ -784,6 +787,22 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         p->mark(3, s);
         if (e == cudaSuccess) {
             TcAttnArgs ta{pl.at, &rt, &pl.mq, &pl.mk, &pl.mv, pl.m_blocks, p->n_sms};
+            // the last wave's units split in two halves of their keys when two
+            // halves of each fit one wave
+            const int64_t units = (int64_t)pl.m_blocks * p->d.n_layers * p->d.n_kv_heads;
+            const int64_t tail = units % p->n_sms;
+            ta.base.n_full = (int32_t)units;
+            if (tail > 0 && 2 * tail <= p->n_sms) {
+                if (!p->part &&
+                    cudaMalloc(&p->part, sizeof(float) * 2 * (size_t)p->n_sms * kAttnPartFloats) != cudaSuccess) {
+                    cudaGetLastError();
+                    p->part = nullptr;
+                }
+                if (p->part) {
+                    ta.base.n_full = (int32_t)(units - tail);
+                    ta.base.part = p->part;
+                }
+            }
             if (gl) {
                 ta.gather = true;
                 ta.tmap_pk = &gl->mpk;

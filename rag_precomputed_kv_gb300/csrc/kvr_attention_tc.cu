@@ -457,6 +457,26 @@ __device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, i
     return w;
 }
 
+// Work item `it` of the persistent loop: units 0..n_full-1 whole, then two
+// halves of each remaining unit (key tiles [0, h) and [h, n), h = ceil(n/2)).
+struct Item {
+    Unit w;
+    int half;           // -1: the whole unit
+    int jb, je;         // key tiles of the item
+};
+
+__device__ __forceinline__ Item item_at(const AttnArgs &a, const DevReq *reqs, int n_blocks, int it)
+{
+    Item t;
+    const int u = it < a.n_full ? it : a.n_full + ((it - a.n_full) >> 1);
+    t.half = it < a.n_full ? -1 : ((it - a.n_full) & 1);
+    t.w = unit_at(a, reqs, n_blocks, u);
+    const int hs = (t.w.n_tiles + 1) >> 1;
+    t.jb = t.half == 1 ? hs : 0;
+    t.je = t.half == 0 ? hs : t.w.n_tiles;
+    return t;
+}
+
 }  // namespace
 
 template <bool kG>
@@ -480,6 +500,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n_units = n_blocks * a.n_layers * a.n_kv_heads;
+    const int n_items = 2 * n_units - a.n_full;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
@@ -507,13 +528,14 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float sc = a.scale_log2;
         const int G = a.n_q_heads / a.n_kv_heads;
-        int s_cnt = 0, o_cnt = 0, tt = 0;
+        int s_cnt = 0, o_cnt = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit w = unit_at(a, reqs, n_blocks, u);
-            tt += 2 * w.n_tiles;
-            const int nx = w.n_t[x];
-            if (nx == 0)
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const Item itm = item_at(a, reqs, n_blocks, it);
+            const Unit &w = itm.w;
+            const int jb = itm.jb;
+            const int nx = min(itm.je, w.n_t[x]);   // this tile's key tiles in the item: [jb, nx)
+            if (jb >= nx)
                 continue;
             const int rr = w.row0[x] + r;          // packed row in the request
             const bool row_ok = rr < w.m_rows;
@@ -521,7 +543,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             const int g = row_ok ? rr - (rr / G) * G : 0;
             const int pos = w.rq.prefix + t;
             float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < nx; ++j) {
+            for (int j = jb; j < nx; ++j) {
                 if (!mbar_wait(bar(kBarSFull + x), s_cnt & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -552,13 +574,15 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 // lazy max: keep m_run unless this tile's max exceeds it by more than
                 // the threshold; O_x and l are rescaled after P_x is written (S is dead)
                 float corr = 1.f;
-                if (j == 0) {
+                if (j == jb) {
                     m_run = mxs;
                 } else if (mxs > m_run + kRescaleThreshold) {
                     corr = ex2(m_run - mxs);
                     m_run = mxs;
                 }
-                const float nm = -m_run;
+                // a row that sees no key of the item's first tile sees none of
+                // the item (p = 0 throughout, m stays -inf)
+                const float nm = m_run == -INFINITY ? 0.f : -m_run;
                 const uint64_t sc2 = pk2(sc, sc), nm2 = pk2(nm, nm);
                 uint64_t acc[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
 #pragma unroll
@@ -615,7 +639,17 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(kBarOEmpty + x));      // O_x may now take the next unit's PV
-            {
+            if (itm.half >= 0) {
+                // half a unit: its state (O unnormalized, running max, sum) for
+                // the merge kernel, 16-byte pieces laid out [piece][row]
+                float *pp = a.part + ((size_t)(it - a.n_full) * 2 + x) * kAttnPartFloats;
+                float4 *po = reinterpret_cast<float4 *>(pp);
+#pragma unroll
+                for (int c = 0; c < kD / 4; ++c)
+                    po[c * kTileM + r] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                pp[kTileM * kD + r] = m_run;
+                pp[kTileM * kD + kTileM + r] = l_run;
+            } else {
                 const float inv = row_ok ? 1.f / l_run : 0.f;
                 const int64_t orow = row_ok ? (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD
                                             : -1;
@@ -651,8 +685,11 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             if (lane == 0) {
                 int tt = 0, nq = 0;
                 bool ok = true;
-                for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                    const Unit w = unit_at(a, reqs, n_blocks, u);
+                for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+                    const Item itm = item_at(a, reqs, n_blocks, it);
+                    const Unit &w = itm.w;
+                    if (itm.je <= itm.jb)
+                        continue;
                     if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
                         ok = false;
                         break;
@@ -665,14 +702,14 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                         tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
                     }
                     ++nq;
-                    if (u + (int)gridDim.x < n_units) {
-                        const Unit wn = unit_at(a, reqs, n_blocks, u + gridDim.x);
+                    if (it + (int)gridDim.x < n_items) {
+                        const Unit wn = item_at(a, reqs, n_blocks, it + gridDim.x).w;
                         for (int x = 0; x < (wn.n_t[1] > 0 ? 2 : 1); ++x) {
                             tma_prefetch_2d(&tmq, 0, wn.q_row0 + x * kTileM);
                             tma_prefetch_2d(&tmq, 64, wn.q_row0 + x * kTileM);
                         }
                     }
-                    for (int i = 0; i < 2 * w.n_tiles; ++i, ++tt) {
+                    for (int i = 0; i < 2 * (itm.je - itm.jb); ++i, ++tt) {
                         const int slot = tt % kSlots;
                         if (tt >= kSlots && !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag)) {
                             ok = false;
@@ -680,7 +717,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                         }
                         const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
                         const CUtensorMap *map = (i & 1) ? &tmv : &tmk;
-                        const int row = (int)(w.kv_row0 + (int64_t)(i >> 1) * kTileN);
+                        const int row = (int)(w.kv_row0 + (int64_t)(itm.jb + (i >> 1)) * kTileN);
                         mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
                         tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
                         tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
@@ -707,8 +744,11 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             const DevSpan *spans = g.spans ? g.spans : st.spans;
             int *meta = reinterpret_cast<int *>(smem + kOffMeta);
             const int64_t e_rows = (int64_t)a.n_layers * a.n_kv_heads * g.entry_len;   // pool rows per entry
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit w = unit_at(a, reqs, n_blocks, u);
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+                const Item itm = item_at(a, reqs, n_blocks, it);
+                const Unit &w = itm.w;
+                if (itm.je <= itm.jb)
+                    continue;
                 if (lane == 0) {
                     if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
                         ok = false;
@@ -720,8 +760,8 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                             tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
                             tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
                         }
-                        if (u + (int)gridDim.x < n_units) {
-                            const Unit wn = unit_at(a, reqs, n_blocks, u + gridDim.x);
+                        if (it + (int)gridDim.x < n_items) {
+                            const Unit wn = item_at(a, reqs, n_blocks, it + gridDim.x).w;
                             for (int x = 0; x < (wn.n_t[1] > 0 ? 2 : 1); ++x) {
                                 tma_prefetch_2d(&tmq, 0, wn.q_row0 + x * kTileM);
                                 tma_prefetch_2d(&tmq, 64, wn.q_row0 + x * kTileM);
@@ -740,7 +780,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 int cur = w.rq.span0;
                 int rows[4] = {0, 0, 0, 0};
                 bool run32 = false;   // this lane's 32-row group is 32 consecutive pool rows
-                for (int i = 0; i < 2 * w.n_tiles; ++i, ++tt) {
+                for (int i = 0; i < 2 * (itm.je - itm.jb); ++i, ++tt) {
                     const int slot = tt % kSlots;
                     bool okw = true;
                     if (tt >= kSlots)
@@ -751,7 +791,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                     }
                     if ((i & 1) == 0) {
                         // K tile j: resolve its rows (the V tile that follows reuses them)
-                        const int j = i >> 1;
+                        const int j = itm.jb + (i >> 1);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const int rr = j * kTileN + 4 * lane + k;
@@ -850,25 +890,31 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 tc_fence_after();
                 return true;
             };
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit w = unit_at(a, reqs, n_blocks, u);
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+                const Item itm = item_at(a, reqs, n_blocks, it);
+                const Unit &w = itm.w;
+                const int jb = itm.jb, je = itm.je;
+                if (je <= jb)
+                    continue;
+                const int jx[2] = {min(je, w.n_t[0]), min(je, w.n_t[1])};   // tile x's key tiles: [jb, jx[x])
                 if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag) || !wait_kv(tt)) {
                     ok = false;
                     break;
                 }
                 ++nq;
                 for (int x = 0; x < 2; ++x)
-                    if (w.n_t[x] > 0)
+                    if (jb < jx[x])
                         issue_s(x, tt % kSlots);
-                if (w.n_tiles == 1)
+                if (je - jb == 1)
                     umma_commit(lead, bar(kBarQEmpty));
                 umma_commit(lead, bar(kBarEmpty + tt % kSlots));
-                for (int j = 0; j < w.n_tiles && ok; ++j) {
-                    const int tv = tt + 2 * j + 1, tk = tt + 2 * j + 2;
+                for (int j = jb; j < je && ok; ++j) {
+                    const int i = j - jb;
+                    const int tv = tt + 2 * i + 1, tk = tt + 2 * i + 2;
                     const uint32_t vb = lo_v + ((kOffKV + (tv % kSlots) * kTileBytes) >> 4);
                     bool v_ready = false, k_ready = false;
                     for (int x = 0; x < 2; ++x) {
-                        if (j >= w.n_t[x])
+                        if (j >= jx[x])
                             continue;
                         if (!mbar_wait(bar(kBarPFull + x), p_cnt[x] & 1, abort_flag)) {
                             ok = false;
@@ -879,7 +925,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                             ok = false;
                             break;
                         }
-                        if (j == 0 && o_used[x]) {   // O_x still holds the last unit until read
+                        if (j == jb && o_used[x]) {   // O_x still holds the last item until read
                             if (!mbar_wait(bar(kBarOEmpty + x), oe_cnt[x] & 1, abort_flag)) {
                                 ok = false;
                                 break;
@@ -888,12 +934,12 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t d = tmem + col_o(x), pa = tmem + col_s(x);
-                        const uint32_t acc0 = j > 0;
+                        const uint32_t acc0 = j > jb;
 #pragma unroll
                         for (int k = 0; k < kTileN / 16; ++k)
                             mma_ts(lead, d, pa + 8 * k, desc_with_lo(vb + ((k * 2048) >> 4), hi_v), kIdescPV,
                                    k > 0 ? 1u : acc0);
-                        if (j + 1 == w.n_t[x]) {
+                        if (j + 1 == jx[x]) {
                             umma_commit(lead, bar(kBarOFull + x));
                             o_used[x] = true;
                         } else {
@@ -906,13 +952,13 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                     }
                     if (!ok)
                         break;
-                    if (k_ready && j + 2 == w.n_tiles)
-                        umma_commit(lead, bar(kBarQEmpty));   // the unit's last S MMAs are issued
+                    if (k_ready && j + 2 == je)
+                        umma_commit(lead, bar(kBarQEmpty));   // the item's last S MMAs are issued
                     umma_commit(lead, bar(kBarEmpty + tv % kSlots));
                     if (k_ready)
                         umma_commit(lead, bar(kBarEmpty + tk % kSlots));
                 }
-                tt += 2 * w.n_tiles;
+                tt += 2 * (je - jb);
             }
             if (!ok)
                 flag_timeout(a.err, abort_flag);
@@ -937,9 +983,10 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         const __nv_bfloat16 *cv = static_cast<const __nv_bfloat16 *>(a.cache_v);
         int tt = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit w = unit_at(a, reqs, n_blocks, u);
-            for (int j = 0; j < w.n_tiles; ++j, tt += 2) {
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const Item itm = item_at(a, reqs, n_blocks, it);
+            const Unit &w = itm.w;
+            for (int j = itm.jb; j < itm.je; ++j, tt += 2) {
                 const int sk = tt % kSlots, sv = (tt + 1) % kSlots;
                 if (!mbar_wait(bar(kBarFull + sk), (tt / kSlots) & 1, abort_flag)) {
                     ok = false;
@@ -1034,6 +1081,62 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     }
 }
 
+// The units that ran as two halves (n_full..): combine each row's two
+// online-softmax states (m, l, unnormalized O) in a fixed order and write the
+// normalized bf16 row.  Four CTAs per (unit, 128-row tile), 256 threads:
+// thread (row, k) takes 16-byte pieces 8 * blockIdx % 4 + 4k .. +3 of its row
+// (reads of consecutive rows are consecutive).
+constexpr int kMergeThreads = 256;
+__global__ void __launch_bounds__(kMergeThreads)
+    k_attention_merge(const __grid_constant__ AttnArgs a, const __grid_constant__ ReqTable rt, const int n_blocks)
+{
+    // the halves are written by the attention kernel just before
+    pdl_wait_prerequisites();
+    const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
+    const int tile = blockIdx.x >> 2, grp = blockIdx.x & 3;
+    const int tail = tile >> 1, x = tile & 1;
+    const Unit w = unit_at(a, reqs, n_blocks, a.n_full + tail);
+    const int r = threadIdx.x & (kTileM - 1), k = threadIdx.x >> 7, rr = w.row0[x] + r;
+    if (w.n_t[x] == 0 || rr >= w.m_rows)
+        return;
+    const bool two = (w.n_tiles + 1) / 2 < w.n_t[x];   // the second half reached this tile
+    const float *p0 = a.part + ((size_t)(2 * tail) * 2 + x) * kAttnPartFloats;
+    const float *p1 = a.part + ((size_t)(2 * tail + 1) * 2 + x) * kAttnPartFloats;
+    const float m0 = p0[kTileM * kD + r];
+    float w0 = 1.f, w1 = 0.f, L = p0[kTileM * kD + kTileM + r];
+    if (two) {
+        const float m1 = p1[kTileM * kD + r];
+        const float M = fmaxf(m0, m1);   // m0 is finite: every row sees key 0
+        w0 = ex2(m0 - M);
+        w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+        L = L * w0 + p1[kTileM * kD + kTileM + r] * w1;
+    }
+    const float inv = 1.f / L;
+    const int G = a.n_q_heads / a.n_kv_heads;
+    const int t = rr / G, g = rr - t * G;
+    uint2 *dst = reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.out) +
+                                           (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD);
+    const float4 *o0 = reinterpret_cast<const float4 *>(p0);
+    const float4 *o1 = reinterpret_cast<const float4 *>(p1);
+    float4 v[4], u[4];
+    const int c0 = 8 * grp + 4 * k;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = o0[(c0 + i) * kTileM + r];
+        if (two)
+            u[i] = o1[(c0 + i) * kTileM + r];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float4 q = v[i];
+        q.x *= w0, q.y *= w0, q.z *= w0, q.w *= w0;
+        if (two) {
+            q.x += u[i].x * w1, q.y += u[i].y * w1, q.z += u[i].z * w1, q.w += u[i].w * w1;
+        }
+        dst[c0 + i] = make_uint2(pack_bf16(q.x * inv, q.y * inv), pack_bf16(q.z * inv, q.w * inv));
+    }
+}
+
 bool attention_tc_supported(int dtype, int head_dim) { return dtype == KVR_DTYPE_BF16 && head_dim == kD; }
 
 template <bool kG>
@@ -1082,8 +1185,22 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
     const int64_t units = (int64_t)ta.n_m_blocks * ta.base.n_layers * ta.base.n_kv_heads;
     if (units > 0x7fffffff)
         return cudaErrorInvalidValue;
-    const int grid = (int)(units < ta.n_sms ? units : ta.n_sms);
-    return ta.gather ? launch_variant<true>(ta, grid, pdl, s) : launch_variant<false>(ta, grid, pdl, s);
+    const int64_t items = 2 * units - ta.base.n_full;
+    const int grid = (int)(items < ta.n_sms ? items : ta.n_sms);
+    cudaError_t e = ta.gather ? launch_variant<true>(ta, grid, pdl, s) : launch_variant<false>(ta, grid, pdl, s);
+    if (e != cudaSuccess || ta.base.n_full == units)
+        return e;
+    // the split units' halves, merged right after
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(8 * (units - ta.base.n_full)));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_attention_merge, ta.base, *ta.rt, ta.n_m_blocks);
 }
 
 }  // namespace kvr

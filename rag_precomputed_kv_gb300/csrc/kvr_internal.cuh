@@ -152,7 +152,14 @@ struct AttnArgs {
     int32_t total_q;            // T
     float scale_log2;           // softmax scale * log2(e)
     int *err;
+    // tensor-core kernel: units n_full.. (the last wave's, when two halves of
+    // each fit one wave) run as two halves of their key range, leaving their
+    // online-softmax state in part for the merge kernel
+    int32_t n_full;
+    float *part;
 };
+// fp32 words of one half-unit partial (one 128-row tile): O, then m, then l
+constexpr int kAttnPartFloats = 128 * 128 + 2 * 128;
 
 struct QueryPrologueArgs {
     const DevReq *reqs;         // NULL: the ReqTable parameter holds the requests
