@@ -78,6 +78,12 @@ enum { KVR_DTYPE_BF16 = 0, KVR_DTYPE_FP32 = 1 };
  * their keys rotated at local positions 0..len-1. */
 #define KVR_POOL_KEYS_UNROTATED 1u
 
+/* kvr_pool_desc flag: RoPE pairs adjacent elements (x_2i, x_2i+1) (the
+ * interleaved convention) instead of (x_i, x_i+D/2); pair i still turns at
+ * frequency theta^(-2i/D).  Applies to every rotation the library makes for
+ * this pool: stored keys, query keys and query heads. */
+#define KVR_POOL_ROPE_INTERLEAVED 2u
+
 /* kvr_prefill flag: no decode follows, so the stitched prefix is not kept.
  * The prefix rows [0, P_b) of the cache blocks are left as they are; the
  * attention gathers the prefix keys and values straight from the pool and
@@ -101,7 +107,7 @@ typedef struct {
     int32_t n_kv_heads;
     int32_t head_dim;     /* 64 or 128 (128 for the tensor-core attention path) */
     int32_t dtype;        /* KVR_DTYPE_BF16 or KVR_DTYPE_FP32                   */
-    int32_t flags;        /* 0 or KVR_POOL_KEYS_UNROTATED                       */
+    int32_t flags;        /* KVR_POOL_KEYS_UNROTATED | KVR_POOL_ROPE_INTERLEAVED */
     int64_t n_entries;    /* chunks (plus prompt entries) in the pool           */
     int64_t entry_len;    /* tokens per entry                                   */
     const void *k;        /* caller-owned, valid until unregister: device memory,

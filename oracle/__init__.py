@@ -11,9 +11,10 @@ What each function follows (page titles and sections):
   ``C_ctx = C_p (+) Rot(C_b1[s1:e1]; D1) (+) ...`` with the new position of
   span i given by the prompt length plus the lengths of the spans before it;
   TurboRAG blog, "Position ID": reordered vs composite positions (Figure 5).
-* :func:`rope` -- RoPE rotation R(shift) on half-split pairs.  CoinRAG blog
-  section 2.3 (``Rot``), TurboRAG blog ("RoPE only cares about relative
-  position"; "re-apply RoPE at the new position").
+* :func:`rope` -- RoPE rotation R(shift) on half-split pairs (or, with
+  ``interleaved``, on adjacent pairs).  CoinRAG blog section 2.3 (``Rot``),
+  TurboRAG blog ("RoPE only cares about relative position"; "re-apply RoPE at
+  the new position").
 * :func:`assemble` -- gather + re-rotate + stitch of one request (CoinRAG
   blog section 2.3; SemPIC page, hit path: re-rotate RoPE keys at the final
   logical positions and interleave request-side inline tokens).
@@ -66,10 +67,12 @@ def _bind(lib):
                                   p, p, p, p, p]
     lib.kvo_rope_rows.restype = None
     lib.kvo_rope_rows.argtypes = [ctypes.c_int64, ctypes.c_int, p, p, ctypes.c_double, p]
+    lib.kvo_rope_rows_interleaved.restype = None
+    lib.kvo_rope_rows_interleaved.argtypes = lib.kvo_rope_rows.argtypes
     lib.kvo_query_attention_units.restype = ctypes.c_int
     lib.kvo_query_attention_units.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                                              ctypes.c_double, p, p, p, p, p, p]
+                                              ctypes.c_int, ctypes.c_double, p, p, p, p, p, p]
     return lib
 
 
@@ -141,20 +144,25 @@ def positions(spans, first_pos: int = 0, composite: bool = False) -> Positions:
     return Positions(target[:k], delta[:k], pos[:got], sid[:got], stok[:got], int(got))
 
 
-def rope(x, shift, theta: float) -> np.ndarray:
-    """Rotate rows ``x[..., D]`` by ``shift`` (scalar, or one value per row)."""
+def rope(x, shift, theta: float, interleaved: bool = False) -> np.ndarray:
+    """Rotate rows ``x[..., D]`` by ``shift`` (scalar, or one value per row).
+
+    Pairs are (x_i, x_{i+D/2}), or (x_{2i}, x_{2i+1}) with ``interleaved``.
+    """
     x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
     D = x.shape[-1]
     rows = x.reshape(-1, D)
     sh = np.ascontiguousarray(np.broadcast_to(np.asarray(shift, dtype=np.float64),
                                               x.shape[:-1]).reshape(-1))
     out = np.empty_like(rows)
-    _load().kvo_rope_rows(rows.shape[0], D, _ptr(rows), _ptr(sh), float(theta), _ptr(out))
+    lib = _load()
+    fn = lib.kvo_rope_rows_interleaved if interleaved else lib.kvo_rope_rows
+    fn(rows.shape[0], D, _ptr(rows), _ptr(sh), float(theta), _ptr(out))
     return out.reshape(x.shape)
 
 
 def assemble(sources, spans, theta: float, first_pos: int = 0, composite: bool = False,
-             unrotated=()):
+             unrotated=(), interleaved: bool = False):
     """Stitch one request's prefix.
 
     ``sources`` maps a source id to a pair ``(k, v)`` of arrays
@@ -166,6 +174,7 @@ def assemble(sources, spans, theta: float, first_pos: int = 0, composite: bool =
     Sources named in ``unrotated`` hold their keys before RoPE (TurboRAG
     blog, "Position ID": keep the un-rotated K and apply RoPE at the new
     position when stitching): their tokens are rotated at their positions.
+    ``interleaved`` selects the adjacent-pair RoPE layout.
     """
     pz = positions(spans, first_pos, composite)
     sp = np.asarray(spans, dtype=np.int64).reshape(-1, 3)
@@ -182,26 +191,31 @@ def assemble(sources, spans, theta: float, first_pos: int = 0, composite: bool =
         k_rows = np.asarray(k_src[:, :, s:e, :], dtype=np.float64)
         if int(src) in unrotated:
             at = pz.pos[row:row + n].astype(np.float64)
-            K[:, :, row:row + n, :] = rope(k_rows, np.broadcast_to(at, k_rows.shape[:-1]), theta)
+            K[:, :, row:row + n, :] = rope(k_rows, np.broadcast_to(at, k_rows.shape[:-1]), theta,
+                                           interleaved)
         else:
-            K[:, :, row:row + n, :] = rope(k_rows, float(pz.delta[i]), theta)
+            K[:, :, row:row + n, :] = rope(k_rows, float(pz.delta[i]), theta, interleaved)
         V[:, :, row:row + n, :] = np.asarray(v_src[:, :, s:e, :], dtype=np.float64)
         row += n
     return K, V, pz
 
 
-def query_attention(kc, vc, q, kq, vq, theta: float, scale: float = 0.0) -> np.ndarray:
+def query_attention(kc, vc, q, kq, vq, theta: float, scale: float = 0.0,
+                    interleaved: bool = False) -> np.ndarray:
     """Query prefill over stitched prefixes of ``U`` independent units.
 
     kc, vc: [U, P, D]; q: [U, Lq, G, D]; kq, vq: [U, Lq, D] (query-side
-    arrays un-rotated).  Returns o: [U, Lq, G, D] fp64.
+    arrays un-rotated).  ``interleaved``: the RoPE layout of the query-side
+    rotations (kc is rotated the same way by the caller).  Returns o:
+    [U, Lq, G, D] fp64.
     """
     c = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.float64))
     kc, vc, q, kq, vq = c(kc), c(vc), c(q), c(kq), c(vq)
     U, P, D = kc.shape
     _, Lq, G, _ = q.shape
     o = np.zeros((U, Lq, G, D), np.float64)
-    rc = _load().kvo_query_attention_units(U, P, Lq, G, D, float(theta), float(scale),
+    rc = _load().kvo_query_attention_units(U, P, Lq, G, D, float(theta), int(bool(interleaved)),
+                                           float(scale),
                                            _ptr(kc), _ptr(vc), _ptr(q), _ptr(kq), _ptr(vq),
                                            _ptr(o))
     if rc != 0:

@@ -19,6 +19,9 @@
  *                      blog, "TurboRAG's two key observations" (RoPE only
  *                      depends on relative position) and "Position ID"
  *                      (re-apply RoPE at the new position).
+ *   kvo_rope_rows_interleaved
+ *                   -- the same rotation on adjacent pairs (x_2i, x_2i+1),
+ *                      the other RoPE layout in use; the pages fix no layout.
  *   kvo_query_attention_units
  *                   -- query prefill over a stitched prefix: every query
  *                      token sees the whole prefix and the query tokens
@@ -33,6 +36,8 @@
  *     the cached key already carries its chunk-local position start + t;
  *   - RoPE pairs element i with element i + D/2 (half-split), frequency
  *     theta^(-2i/D), x' = x cos(a) - y sin(a), y' = x sin(a) + y cos(a);
+ *     the interleaved layout pairs elements 2i and 2i+1 at the same
+ *     frequency theta^(-2i/D);
  *   - query tokens (and their keys) are rotated at P + t, P = prefix length;
  *   - attention scale defaults to 1/sqrt(D); masked keys get weight 0.
  */
@@ -129,6 +134,37 @@ void kvo_rope_rows(int64_t n_rows, int D, const double *x, const double *shift,
 }
 
 /*
+ * Rotate each row r of x by shift[r] with the interleaved pairing: pair i is
+ * (x_{2i}, x_{2i+1}) and turns by angle shift[r] * theta^(-2i/D).  out may
+ * alias x.
+ */
+void kvo_rope_rows_interleaved(int64_t n_rows, int D, const double *x, const double *shift,
+                               double theta, double *out)
+{
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const double *xr = x + r * D;
+        double *yr = out + r * D;
+        for (int i = 0; i < D / 2; ++i) {
+            const double ang = shift[r] * inv_freq(theta, D, i);
+            const double cs = cos(ang), sn = sin(ang);
+            const double ev = xr[2 * i], od = xr[2 * i + 1];
+            yr[2 * i] = ev * cs - od * sn;
+            yr[2 * i + 1] = ev * sn + od * cs;
+        }
+    }
+}
+
+/* One row through the rotation of the chosen layout. */
+static void rope_row(int interleaved, int D, const double *x, double shift, double theta,
+                     double *out)
+{
+    if (interleaved)
+        kvo_rope_rows_interleaved(1, D, x, &shift, theta, out);
+    else
+        kvo_rope_rows(1, D, x, &shift, theta, out);
+}
+
+/*
  * Query prefill attention for n_units independent (request, layer, kv-head)
  * units that share the prefix length P and the query length Lq.
  *
@@ -143,10 +179,11 @@ void kvo_rope_rows(int64_t n_rows, int D, const double *x, const double *shift,
  * the P prefix rows plus query rows 0..t:
  *     s_j = scale * <R(P+t) q_{t,g}, k_j>,  o = sum_j softmax(s)_j v_j
  * (softmax with the maximum subtracted).  scale <= 0 means 1/sqrt(D).
- * Returns 0, or -1 if memory runs out.
+ * interleaved != 0 rotates with kvo_rope_rows_interleaved (kc must then be
+ * rotated that way too).  Returns 0, or -1 if memory runs out.
  */
 int kvo_query_attention_units(int64_t n_units, int64_t P, int64_t Lq, int G,
-                              int D, double theta, double scale,
+                              int D, double theta, int interleaved, double scale,
                               const double *kc, const double *vc,
                               const double *q, const double *kq,
                               const double *vq, double *o)
@@ -172,14 +209,14 @@ int kvo_query_attention_units(int64_t n_units, int64_t P, int64_t Lq, int G,
         memcpy(V, vc + u * P * D, sizeof(double) * (size_t)(P * D));
         for (int64_t t = 0; t < Lq; ++t) {
             const double sh = (double)(P + t);
-            kvo_rope_rows(1, D, kq + (u * Lq + t) * D, &sh, theta, K + (P + t) * D);
+            rope_row(interleaved, D, kq + (u * Lq + t) * D, sh, theta, K + (P + t) * D);
             memcpy(V + (P + t) * D, vq + (u * Lq + t) * D, sizeof(double) * (size_t)D);
         }
         for (int64_t t = 0; t < Lq; ++t) {
             const double sh = (double)(P + t);
             const int64_t n_vis = P + t + 1; /* prefix + query rows 0..t */
             for (int g = 0; g < G; ++g) {
-                kvo_rope_rows(1, D, q + ((u * Lq + t) * G + g) * D, &sh, theta, qr);
+                rope_row(interleaved, D, q + ((u * Lq + t) * G + g) * D, sh, theta, qr);
                 double m = -INFINITY;
                 for (int64_t j = 0; j < n_vis; ++j) {
                     double dot = 0.0;

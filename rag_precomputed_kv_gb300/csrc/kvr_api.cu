@@ -164,7 +164,7 @@ extern "C" kvr_status kvr_pool_register(const kvr_pool_desc *desc, kvr_pool_t *o
     if (d.n_entries < 1 || d.entry_len < 1 || d.entry_len > kMaxPosition)
         return fail(KVR_ERR_INVALID_ARG, "n_entries %lld, entry_len %lld",
                     (long long)d.n_entries, (long long)d.entry_len);
-    if (d.flags & ~KVR_POOL_KEYS_UNROTATED)
+    if (d.flags & ~(KVR_POOL_KEYS_UNROTATED | KVR_POOL_ROPE_INTERLEAVED))
         return fail(KVR_ERR_INVALID_ARG, "unknown pool flags 0x%x", (unsigned)d.flags);
     if (!d.k || !d.v)
         return fail(KVR_ERR_INVALID_ARG, "pool k / v is NULL");
@@ -445,6 +445,7 @@ static kvr_status asm_stage(kvr_pool *p, AsmPlan &pl, cudaStream_t s)
     a.n_layers = p->d.n_layers;
     a.n_heads = p->d.n_kv_heads;
     a.upc = units_per_cta(LH, pl.flat, (int64_t)pl.ds.size());
+    a.interleaved = (p->d.flags & KVR_POOL_ROPE_INTERLEAVED) ? 1 : 0;
     const int n_locals = pl.n_locals;
     const kvr_local_src *locals = pl.locals;
     pl.inl = (int)pl.ds.size() <= kInlineEntries && n_locals <= kInlineEntries;
@@ -757,6 +758,7 @@ static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
     at.total_q = T;
     at.scale_log2 = (pl.scale > 0.f ? pl.scale : 1.f / std::sqrt((float)D)) * 1.4426950408889634f;
     at.err = p->err;
+    at.interleaved = (p->d.flags & KVR_POOL_ROPE_INTERLEAVED) ? 1 : 0;
     // CUDA-core path: the query keys / values are appended by the assemble
     // kernel (un-rotated source, token t turned by P + t); the query heads
     // are rotated inside the CUDA-core attention kernel
@@ -766,6 +768,7 @@ static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
     a.n_layers = L;
     a.n_heads = Hkv;
     a.upc = 1;
+    a.interleaved = at.interleaved;
     return KVR_OK;
 }
 
@@ -781,7 +784,8 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
     cudaError_t e;
     if (pl.tc) {
         QueryPrologueArgs qp{pl.at.reqs, p->rope, pl.q, pl.kq, pl.vq, pl.cache_k, pl.cache_v, p->q_rot,
-                             p->d.n_layers, p->d.n_q_heads, p->d.n_kv_heads, pl.T, pl.max_lq, pl.batch};
+                             p->d.n_layers, p->d.n_q_heads, p->d.n_kv_heads, pl.T, pl.max_lq, pl.batch,
+                             pl.at.interleaved};
         p->mark(2, s);
         e = launch_query_prologue(qp, rt, p->n_sms, after_assemble && !p->timed, s);
         p->mark(3, s);

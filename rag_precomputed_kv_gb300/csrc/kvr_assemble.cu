@@ -54,19 +54,37 @@ struct Vec;
 template <>
 struct Vec<__nv_bfloat16> {
     static constexpr int E = 8;
-    __device__ static void rotate(uint4 &lo, uint4 &hi, const float *c, const float *s)
+    __device__ static void rotate(uint4 &lo, uint4 &hi, const float *c, const float *s, bool il)
     {
-        rotate_bf16x8(lo, hi, c, s);
+        if (il)
+            rotate_bf16x8_il(lo, hi, c, s);
+        else
+            rotate_bf16x8(lo, hi, c, s);
     }
 };
 
 template <>
 struct Vec<float> {
     static constexpr int E = 4;
-    __device__ static void rotate(uint4 &lo, uint4 &hi, const float *c, const float *s)
+    __device__ static void rotate(uint4 &lo, uint4 &hi, const float *c, const float *s, bool il)
     {
         float *x = reinterpret_cast<float *>(&lo);
         float *y = reinterpret_cast<float *>(&hi);
+        if (il) {
+            // pairs (x0, x1), (x2, x3) of lo with c[0], c[1]; of hi with c[2], c[3]
+            float *v[2] = {x, y};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const float a0 = v[h][2 * p], a1 = v[h][2 * p + 1];
+                    const float cc = c[2 * h + p], ss = s[2 * h + p];
+                    v[h][2 * p] = fmaf(a0, cc, -a1 * ss);
+                    v[h][2 * p + 1] = fmaf(a0, ss, a1 * cc);
+                }
+            }
+            return;
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float xo = fmaf(x[e], c[e], -y[e] * s[e]);
@@ -118,7 +136,7 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
     float c[E], s[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        const float2 cs = rope_cs(a.rope, H2, sp.delta, j * E + e);
+        const float2 cs = rope_cs(a.rope, H2, sp.delta, rope_pair(a.interleaved, D, E, j, e));
         c[e] = cs.x;
         s[e] = cs.y;
     }
@@ -175,12 +193,12 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
                     const int row = r - (r / sp.len) * sp.len;
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
-                        const float2 cs = rope_cs(a.rope, H2, sp.delta + row, j * E + e);
+                        const float2 cs = rope_cs(a.rope, H2, sp.delta + row, rope_pair(a.interleaved, D, E, j, e));
                         c[e] = cs.x;
                         s[e] = cs.y;
                     }
                 }
-                Vec<T>::rotate(klo[u], khi[u], c, s);
+                Vec<T>::rotate(klo[u], khi[u], c, s, a.interleaved);
                 st_vec(ck + dst[u], klo[u]);
                 st_vec(ck + dst[u] + H2, khi[u]);
                 st_vec(cv + dst[u], vlo[u]);

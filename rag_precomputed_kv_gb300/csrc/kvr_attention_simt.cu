@@ -61,12 +61,22 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int k = 0; k < PL; ++k)
         qv[k] = to_f(qp[lane + 32 * k]);
+    if (a.interleaved) {
+        // pairs (x_2i, x_2i+1): element lane + 32k and its neighbour lane ^ 1
 #pragma unroll
-    for (int k = 0; k < PL / 2; ++k) {
-        const float2 cs = rope_cs(a.rope, D / 2, pos, lane + 32 * k);
-        const float x = qv[k], y = qv[k + PL / 2];
-        qv[k] = fmaf(x, cs.x, -y * cs.y);
-        qv[k + PL / 2] = fmaf(x, cs.y, y * cs.x);
+        for (int k = 0; k < PL; ++k) {
+            const float2 cs = rope_cs(a.rope, D / 2, pos, (lane + 32 * k) >> 1);
+            const float other = __shfl_xor_sync(0xffffffffu, qv[k], 1);
+            qv[k] = (lane & 1) ? fmaf(other, cs.y, qv[k] * cs.x) : fmaf(qv[k], cs.x, -other * cs.y);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < PL / 2; ++k) {
+            const float2 cs = rope_cs(a.rope, D / 2, pos, lane + 32 * k);
+            const float x = qv[k], y = qv[k + PL / 2];
+            qv[k] = fmaf(x, cs.x, -y * cs.y);
+            qv[k + PL / 2] = fmaf(x, cs.y, y * cs.x);
+        }
     }
 
     const int64_t blk = rq.cache_row0 + (int64_t)(l * a.n_kv_heads + kvh) * rq.cap;

@@ -1025,12 +1025,15 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                             d_cur = dd[q];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                const float2 cs = rope_cs(a.rope, kD / 2, d_cur, 8 * p + e);
+                                const float2 cs = rope_cs(a.rope, kD / 2, d_cur, rope_pair(a.interleaved, kD, 8, p, e));
                                 c[e] = cs.x;
                                 sn[e] = cs.y;
                             }
                         }
-                        rotate_bf16x8(lo[q], hi[q], c, sn);
+                        if (a.interleaved)
+                            rotate_bf16x8_il(lo[q], hi[q], c, sn);
+                        else
+                            rotate_bf16x8(lo[q], hi[q], c, sn);
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {

@@ -71,6 +71,35 @@ __device__ __forceinline__ void rotate_bf16x8(uint4 &lo, uint4 &hi, const float 
         ph[w] = *reinterpret_cast<uint32_t *>(&yb);
     }
 }
+
+// The same rotation for the interleaved pairing: every bf16 word of lo and
+// hi is a pair (x_2i, x_2i+1); c[w], s[w] belong to lo's word w and c[4 + w],
+// s[4 + w] to hi's.
+__device__ __forceinline__ void rotate_bf16x8_il(uint4 &lo, uint4 &hi, const float *c, const float *s)
+{
+    uint32_t *pw[2] = {reinterpret_cast<uint32_t *>(&lo), reinterpret_cast<uint32_t *>(&hi)};
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float2 xy = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&pw[v][w]));
+            const float cc = c[4 * v + w], ss = s[4 * v + w];
+            __nv_bfloat162 o = __floats2bfloat162_rn(fmaf(xy.x, cc, -xy.y * ss), fmaf(xy.x, ss, xy.y * cc));
+            pw[v][w] = *reinterpret_cast<uint32_t *>(&o);
+        }
+    }
+}
+
+// Pair index of the e-th (cos, sin) of a thread that owns 16-byte chunk j of
+// both row halves (E elements per chunk, head dim D): half-split pairs are
+// elements (jE + e, D/2 + jE + e); interleaved pairs are whole inside a
+// chunk, E/2 of them in the chunk of each half.
+__device__ __forceinline__ int rope_pair(bool interleaved, int D, int E, int j, int e)
+{
+    if (!interleaved)
+        return j * E + e;
+    return e < E / 2 ? (E / 2) * j + e : D / 4 + (E / 2) * j + (e - E / 2);
+}
 #endif
 
 // Device copy of one span (48 bytes).
@@ -124,6 +153,7 @@ struct AssembleArgs {
     int32_t *src_map;
     int32_t n_layers, n_heads;  // kv heads
     int32_t upc;                // (layer, head) units per CTA
+    int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
 };
 
 // Span / local-source tables passed inside the kernel parameters (no upload)
@@ -157,6 +187,7 @@ struct AttnArgs {
     // online-softmax state in part for the merge kernel
     int32_t n_full;
     float *part;
+    int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
 };
 // fp32 words of one half-unit partial (one 128-row tile): O, then m, then l
 constexpr int kAttnPartFloats = 128 * 128 + 2 * 128;
@@ -174,6 +205,7 @@ struct QueryPrologueArgs {
     int32_t total_q;            // T
     int32_t max_q_len;          // longest query of the batch
     int32_t n_reqs;
+    int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
 };
 
 // ---- launchers (each returns the cudaGetLastError of its launch) ----

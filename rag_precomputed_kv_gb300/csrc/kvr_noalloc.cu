@@ -68,7 +68,7 @@ extern "C" kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t ba
     if (d.head_dim != 64 && d.head_dim != 128)
         return na_fail(KVR_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
     if (d.n_layers < 1 || d.n_kv_heads < 1 || d.n_q_heads < 1 || d.n_q_heads % d.n_kv_heads ||
-        d.n_entries < 1 || d.entry_len < 1 || d.entry_len > kMaxPosition || (d.flags & ~KVR_POOL_KEYS_UNROTATED) != 0 || !d.k ||
+        d.n_entries < 1 || d.entry_len < 1 || d.entry_len > kMaxPosition || (d.flags & ~(KVR_POOL_KEYS_UNROTATED | KVR_POOL_ROPE_INTERLEAVED)) != 0 || !d.k ||
         !d.v || !na_aligned16(d.k) || !na_aligned16(d.v) || !(d.rope_theta > 1.0) ||
         !std::isfinite(d.rope_theta))
         return na_fail(KVR_ERR_INVALID_ARG, "invalid pool descriptor");
@@ -225,6 +225,7 @@ extern "C" kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t ba
     a.n_heads = d.n_kv_heads;
     const int64_t avg = flat / n > 0 ? flat / n : 1;
     a.upc = (int)(256 / avg > LH ? LH : (256 / avg < 1 ? 1 : 256 / avg));
+    a.interleaved = (d.flags & KVR_POOL_ROPE_INTERLEAVED) ? 1 : 0;
     if ((e = launch_assemble(a, d.dtype, d.head_dim, n, s)) != cudaSuccess)
         return na_fail(KVR_ERR_CUDA, cudaGetErrorString(e));
     return KVR_OK;

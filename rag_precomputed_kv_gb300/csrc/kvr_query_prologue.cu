@@ -24,8 +24,12 @@ namespace {
 constexpr int kQpTokens = 16;                 // query tokens per CTA
 constexpr int kQpThreads = 8 * kQpTokens;     // 8 threads per token
 
-__device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float *c, const float *s)
+__device__ __forceinline__ void rotate8(uint4 &lo, uint4 &hi, const float *c, const float *s, bool il)
 {
+    if (il) {
+        rotate_bf16x8_il(lo, hi, c, s);
+        return;
+    }
     uint32_t *pl = reinterpret_cast<uint32_t *>(&lo);
     uint32_t *ph = reinterpret_cast<uint32_t *>(&hi);
 #pragma unroll
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(kQpThreads)
             float c[E], s[E];
 #pragma unroll
             for (int e = 0; e < E; ++e) {
-                const float2 cs = rope_cs(a.rope, H2, rq.prefix + t, j * E + e);
+                const float2 cs = rope_cs(a.rope, H2, rq.prefix + t, rope_pair(a.interleaved, D, E, j, e));
                 c[e] = cs.x;
                 s[e] = cs.y;
             }
@@ -86,7 +90,7 @@ __global__ void __launch_bounds__(kQpThreads)
             uint4 khi = *reinterpret_cast<const uint4 *>(kq + kv_src + H2);
             const uint4 vlo = *reinterpret_cast<const uint4 *>(vq + kv_src);
             const uint4 vhi = *reinterpret_cast<const uint4 *>(vq + kv_src + H2);
-            rotate8(klo, khi, c, s);
+            rotate8(klo, khi, c, s, a.interleaved);
             const int64_t dst = (rq.cache_row0 + (int64_t)lh * rq.cap + rq.prefix + t) * D + j * E;
             *reinterpret_cast<uint4 *>(ck + dst) = klo;
             *reinterpret_cast<uint4 *>(ck + dst + H2) = khi;
@@ -97,7 +101,7 @@ __global__ void __launch_bounds__(kQpThreads)
             for (int g = 0; g < G; ++g) {
                 uint4 lo = *reinterpret_cast<const uint4 *>(q + q_src + (int64_t)g * D);
                 uint4 hi = *reinterpret_cast<const uint4 *>(q + q_src + (int64_t)g * D + H2);
-                rotate8(lo, hi, c, s);
+                rotate8(lo, hi, c, s, a.interleaved);
                 *reinterpret_cast<uint4 *>(qr + q_dst + (int64_t)g * D) = lo;
                 *reinterpret_cast<uint4 *>(qr + q_dst + (int64_t)g * D + H2) = hi;
             }

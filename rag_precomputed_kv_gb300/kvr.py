@@ -23,6 +23,7 @@ KVR_SRC_LOCAL = 1 << 30
 KVR_POSITIONS_COMPOSITE = 1
 KVR_PREFILL_SKIP_PREFIX_CACHE = 2
 KVR_POOL_KEYS_UNROTATED = 1
+KVR_POOL_ROPE_INTERLEAVED = 2
 
 STATUS = {0: "KVR_OK", 1: "KVR_ERR_INVALID_ARG", 2: "KVR_ERR_OUT_OF_RANGE", 3: "KVR_ERR_UNSUPPORTED",
           4: "KVR_ERR_CUDA", 5: "KVR_ERR_TIMEOUT", 6: "KVR_ERR_DEVICE_CHECK"}
@@ -134,18 +135,23 @@ class Pool:
 
     ``k``, ``v``: device tensors ``[entries, layers, kv_heads, entry_len, head_dim]``
     (any strides with head_dim contiguous), keys rotated at entry-local
-    positions (or, with ``keys_unrotated``, before RoPE).  The tensors must
-    outlive the pool.
+    positions (or, with ``keys_unrotated``, before RoPE).  ``rope_interleaved``:
+    RoPE pairs are (x_2i, x_2i+1) instead of (x_i, x_i+D/2), for the stored
+    keys and every rotation the library makes.  The tensors must outlive the
+    pool.
     """
 
-    def __init__(self, k, v, n_q_heads: int, rope_theta: float, keys_unrotated: bool = False):
+    def __init__(self, k, v, n_q_heads: int, rope_theta: float, keys_unrotated: bool = False,
+                 rope_interleaved: bool = False):
         import torch
         lib = load()
         assert k.shape == v.shape and k.stride() == v.stride() and k.dtype == v.dtype
         assert k.stride(-1) == 1
         dt = {torch.bfloat16: KVR_DTYPE_BF16, torch.float32: KVR_DTYPE_FP32}[k.dtype]
         E, L, H, T, D = k.shape
-        d = PoolDesc(L, n_q_heads, H, D, dt, KVR_POOL_KEYS_UNROTATED if keys_unrotated else 0, E, T,
+        flags = ((KVR_POOL_KEYS_UNROTATED if keys_unrotated else 0)
+                 | (KVR_POOL_ROPE_INTERLEAVED if rope_interleaved else 0))
+        d = PoolDesc(L, n_q_heads, H, D, dt, flags, E, T,
                      _ptr(k), _ptr(v),
                      (ctypes.c_int64 * 4)(*k.stride()[:4]), float(rope_theta))
         h = ctypes.c_void_p()

@@ -35,16 +35,20 @@ def to_np64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def pair_norm(x):
+def pair_norm(x, interleaved=False):
+    """Norm of the RoPE pair each element belongs to."""
+    if interleaved:
+        n = np.sqrt(x[..., 0::2] ** 2 + x[..., 1::2] ** 2)
+        return np.repeat(n, 2, axis=-1)
     h = x.shape[-1] // 2
     n = np.sqrt(x[..., :h] ** 2 + x[..., h:] ** 2)
     return np.concatenate([n, n], axis=-1)
 
 
-def k_within_tolerance(gpu, ref, dtype):
+def k_within_tolerance(gpu, ref, dtype, interleaved=False):
     """Returns (ok, worst ratio of |err| to the allowed error)."""
     err = np.abs(gpu - ref)
-    nrm = pair_norm(ref)
+    nrm = pair_norm(ref, interleaved)
     if dtype == "bf16":
         mag = np.maximum(np.abs(ref), 2.0 ** -14 * nrm)
         mag = np.where(mag > 0, mag, 2.0 ** -126)
@@ -68,11 +72,12 @@ class Case:
     """Inputs, layout and GPU results of one configuration."""
 
     def __init__(self, cfg: W.Config, device="cuda:0", prerotate=None, reqs=None, composite=False,
-                 spare_rows=0, keys_unrotated=False):
+                 spare_rows=0, keys_unrotated=False, rope_interleaved=False):
         import torch
         from rag_precomputed_kv_gb300 import kvr
         self.cfg, self.device, self.composite = cfg, device, composite
         self.keys_unrotated = keys_unrotated   # pool keys kept before RoPE
+        self.il = rope_interleaved             # RoPE pairs (x_2i, x_2i+1)
         self.reqs = reqs if reqs is not None else W.draw_spans(cfg)
         self.t = W.make_tensors(cfg, self.reqs, device=device)
         # explicit pre-rotation of the pool keys at chunk-local positions (the
@@ -84,7 +89,7 @@ class Case:
             raw = to_np64(self.t.pool_k)
             self.raw_pool_k = raw
             pos = np.arange(cfg.chunk_len, dtype=np.float64)[None, None, None, :]
-            rot = oracle.rope(raw, np.broadcast_to(pos, raw.shape[:-1]), cfg.rope_theta)
+            rot = oracle.rope(raw, np.broadcast_to(pos, raw.shape[:-1]), cfg.rope_theta, self.il)
             self.t.pool_k.copy_(torch.from_numpy(rot).to(self.t.pool_k.dtype))
         L, H, D = cfg.n_layers, cfg.n_kv_heads, cfg.head_dim
         self.LH = L * H
@@ -117,7 +122,7 @@ class Case:
         self.src_map = torch.full((max(tot, 1), 2), -1, dtype=torch.int32, device=device)
         self.out = torch.full_like(self.t.q, float("nan"))
         self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta,
-                             keys_unrotated=keys_unrotated)
+                             keys_unrotated=keys_unrotated, rope_interleaved=rope_interleaved)
 
     def run(self, attention=True, prefill=False, skip_prefix=False):
         """The hot path through the C ABI: kvr_assemble then
@@ -192,7 +197,7 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
         if srcs:
             unrot = {s for s in srcs if not (s & W.LOCAL_FLAG)} if case.keys_unrotated else ()
             K_ref, V_ref, pz = oracle.assemble(srcs, spans, cfg.rope_theta, composite=composite,
-                                               unrotated=unrot)
+                                               unrotated=unrot, interleaved=case.il)
         else:   # a request without any prefix
             K_ref = V_ref = np.zeros((1, len(units), 0, D))
             pz = oracle.positions(spans, 0, composite)
@@ -214,7 +219,7 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
             if not np.array_equal(cv[:, :P], V_ref[0]):
                 res["ok"] = False
                 res["v"] = f"request {b}: gathered V differs"
-            okk, ratio = k_within_tolerance(ck[:, :P], K_ref[0], cfg.dtype)
+            okk, ratio = k_within_tolerance(ck[:, :P], K_ref[0], cfg.dtype, case.il)
             res["k_ratio"] = max(res["k_ratio"], ratio)
             res["ok"] &= okk
         if attention:
@@ -227,7 +232,8 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
             qu = np.stack([q[l, :, h * G:(h + 1) * G, :] for l, h in zip(li, hi)])
             kqu = np.stack([kq[l, :, h, :] for l, h in zip(li, hi)])
             vqu = np.stack([vq[l, :, h, :] for l, h in zip(li, hi)])
-            o_ref = oracle.query_attention(K_ref[0], V_ref[0], qu, kqu, vqu, cfg.rope_theta)
+            o_ref = oracle.query_attention(K_ref[0], V_ref[0], qu, kqu, vqu, cfg.rope_theta,
+                                           interleaved=case.il)
             og = to_np64(case.out[:, qo:qo + lq])
             o_gpu = np.stack([og[l, :, h * G:(h + 1) * G, :] for l, h in zip(li, hi)])
             oka, mx, rel = attn_within_tolerance(o_gpu, o_ref, cfg.dtype)
@@ -235,8 +241,9 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
             res["attn_mean_rel"] = max(res["attn_mean_rel"], rel)
             res["ok"] &= oka
             # appended query rows: K rotated at P + t, V copied
-            kq_ref = oracle.rope(kqu, (P + np.arange(lq, dtype=np.float64))[None, :], cfg.rope_theta)
-            okq, rq = k_within_tolerance(ck[:, P:P + lq], kq_ref, cfg.dtype)
+            kq_ref = oracle.rope(kqu, (P + np.arange(lq, dtype=np.float64))[None, :], cfg.rope_theta,
+                                 case.il)
+            okq, rq = k_within_tolerance(ck[:, P:P + lq], kq_ref, cfg.dtype, case.il)
             res["k_ratio"] = max(res["k_ratio"], rq)
             res["ok"] &= okq
             if not np.array_equal(cv[:, P:P + lq], vqu):

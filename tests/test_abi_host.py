@@ -65,7 +65,7 @@ def _register(lib, desc):
 
 @pytest.mark.parametrize("bad,status", [
     (dict(dtype=7), 3), (dict(head_dim=96), 3), (dict(n_q_heads=7), 1), (dict(n_layers=0), 1),
-    (dict(n_entries=0), 1), (dict(flags=2), 1), (dict(k=0), 1), (dict(k=0x10008), 1),
+    (dict(n_entries=0), 1), (dict(flags=4), 1), (dict(flags=-1), 1), (dict(k=0), 1), (dict(k=0x10008), 1),
     (dict(rope_theta=0.5), 1), (dict(stride=(8, 8, 8, 12)), 1), (dict(stride=(-8, 8, 8, 8)), 1),
 ])
 def test_register_rejects_bad_descriptors(lib, bad, status):

@@ -238,6 +238,44 @@ def test_pool_keys_kept_before_rope(variant):
     _ok(run_parity_case(cfg=cfg, case=case, composite=composite, prefill=variant == "cfg2_prefill"))
 
 
+@pytest.mark.parametrize("variant", ["bf16_two_calls", "cfg2_prefill", "fp32_cuda_cores", "d64_cuda_cores",
+                                     "unrotated_with_locals", "cfg2_gathering"])
+def test_pool_with_interleaved_rope_pairs(variant):
+    """A pool registered with KVR_POOL_ROPE_INTERLEAVED: every rotation
+    (stitched keys, query keys, query heads; in the stitch kernel, the query
+    prologue, the CUDA-core attention and the gathering attention's rotator)
+    pairs (x_2i, x_2i+1)."""
+    import torch
+    pid = EDGE_BASE.n_chunks
+    lists = [[[pid, 0, 5], [0, 0, 1], [1, 95, 96], [2, 10, 50], [2, 30, 70]], [],
+             [[3, 0, 96], [1, 5, 40]]]
+    kw, unrot, prefill, skip = {}, False, False, False
+    if variant == "bf16_two_calls":
+        cfg, reqs = _custom(dataclasses.replace(EDGE_BASE, query_len=29), lists)
+    elif variant == "cfg2_prefill":
+        cfg, reqs, prefill = W.CONFIGS[2], None, True
+    elif variant == "fp32_cuda_cores":
+        cfg, reqs = W.CONFIGS[1], None
+    elif variant == "d64_cuda_cores":
+        cfg, reqs = _custom(dataclasses.replace(EDGE_BASE, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                                                query_len=17, rope_theta=5e5), lists)
+    elif variant == "unrotated_with_locals":
+        base = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, prompt_len=0, query_len=11)
+        F = W.LOCAL_FLAG
+        cfg, reqs = _custom(base, [[[0, 3, 90], [F | 0, 0, 8], [2, 0, 40]], [[3, 10, 96], [1, 0, 5]]],
+                            local_lens={0: 8})
+        unrot = True
+    else:
+        cfg, reqs, prefill, skip = W.CONFIGS[2], None, True, True
+    case = Case(cfg, reqs=reqs, keys_unrotated=unrot, rope_interleaved=True)
+    _ok(run_parity_case(cfg=cfg, case=case, prefill=prefill, skip_prefix=skip, **kw))
+    if skip:    # the gathering attention rotates like the stitch kernel: same bits
+        got = case.out.clone()
+        case.out.fill_(float("nan"))
+        case.run(prefill=True)
+        assert torch.equal(got.view(torch.int16), case.out.view(torch.int16))
+
+
 def test_pool_in_pinned_host_memory():
     """A pool kept in pinned host memory (read by the stitch kernel through
     its unified address): same results, bit for bit, as the device pool."""

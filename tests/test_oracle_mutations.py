@@ -25,14 +25,20 @@ MUTANTS = {
     "composite_from_zero": ("target[i] = composite ? s.start : next;", "target[i] = composite ? 0 : next;"),
     "mask_drops_self": ("const int64_t n_vis = P + t + 1;", "const int64_t n_vis = P + t;"),
     "no_causal_mask": ("const int64_t n_vis = P + t + 1;", "const int64_t n_vis = N;"),
-    "query_key_position": ("const double sh = (double)(P + t);\n            kvo_rope_rows(1, D, kq",
-                           "const double sh = (double)(P + t + 1);\n            kvo_rope_rows(1, D, kq"),
-    "query_not_rotated": ("kvo_rope_rows(1, D, q + ((u * Lq + t) * G + g) * D, &sh, theta, qr);",
+    "query_key_position": ("const double sh = (double)(P + t);\n            rope_row(interleaved, D, kq",
+                           "const double sh = (double)(P + t + 1);\n            rope_row(interleaved, D, kq"),
+    "query_not_rotated": ("rope_row(interleaved, D, q + ((u * Lq + t) * G + g) * D, sh, theta, qr);",
                           "memcpy(qr, q + ((u * Lq + t) * G + g) * D, sizeof(double) * (size_t)D);"),
     "scale": ("scale = 1.0 / sqrt((double)D);", "scale = 1.0 / (double)D;"),
     "query_head_layout": ("q + ((u * Lq + t) * G + g) * D", "q + ((u * G + g) * Lq + t) * D"),
     "values_from_keys": ("acc += sc[j] * V[j * D + d];", "acc += sc[j] * K[j * D + d];"),
     "missing_normaliser": ("orow[d] = acc / z;", "orow[d] = acc;"),
+    "interleaved_sign": ("yr[2 * i] = ev * cs - od * sn;", "yr[2 * i] = ev * cs + od * sn;"),
+    "interleaved_frequency": ("shift[r] * inv_freq(theta, D, i);\n            const double cs",
+                              "shift[r] * inv_freq(theta, D, 2 * i);\n            const double cs"),
+    "interleaved_partner": ("const double ev = xr[2 * i], od = xr[2 * i + 1];",
+                            "const double ev = xr[i], od = xr[i + D / 2];"),
+    "interleaved_ignored": ("    if (interleaved)\n        kvo_rope_rows_interleaved", "    if (0)\n        kvo_rope_rows_interleaved"),
     "value_row_shift": ("memcpy(V + (P + t) * D, vq + (u * Lq + t) * D", "memcpy(V + (P + t) * D, vq + (u * Lq + (t + 1) % Lq) * D"),
 }
 

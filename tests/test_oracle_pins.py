@@ -6,8 +6,9 @@ against an independent fact:
 * the worked position example of TurboRAG's Figure 5 (golden fixture);
 * the span-position formula as the CoinRAG blog prints it (inclusive ends,
   section 2.3) and a brute-force concatenation of token lists;
-* RoPE as complex multiplication (numpy complex128), closed forms on unit
-  vectors, and the group properties the pages rely on (identity at 0,
+* RoPE as complex multiplication (numpy complex128) in both pair layouts,
+  closed forms on unit vectors, the adjacent layout as a relabelling of the
+  half-split one, and the group properties the pages rely on (identity at 0,
   composition, relative-position invariance, re-rotating a cached key equals
   rotating the raw key at its target);
 * attention against torch's scaled_dot_product_attention (a library routine)
@@ -170,6 +171,79 @@ def pin_rope_relative_position():
     assert abs(d1 - d2) < 1e-10
 
 
+def rot_complex_adjacent(x, shift, theta):
+    """The interleaved layout by complex numbers: pair (x_2i, x_2i+1) is
+    z = x_2i + 1j*x_2i+1, multiplied by exp(1j * shift * theta**(-2i/D))."""
+    x = np.asarray(x, np.float64)
+    D = x.shape[-1]
+    z = x[..., 0::2] + 1j * x[..., 1::2]
+    ang = np.asarray(shift, np.float64)[..., None] * theta ** (-2.0 * np.arange(D // 2) / D)
+    w = z * np.exp(1j * ang)
+    out = np.empty_like(x)
+    out[..., 0::2] = w.real
+    out[..., 1::2] = w.imag
+    return out
+
+
+def half_split_to_adjacent(D):
+    """Index map: element 2i of the adjacent layout is element i of the
+    half-split one, element 2i+1 is element i + D/2."""
+    idx = np.empty(D, np.int64)
+    idx[0::2] = np.arange(D // 2)
+    idx[1::2] = np.arange(D // 2) + D // 2
+    return idx
+
+
+def pin_rope_interleaved():
+    """Adjacent pairs: complex multiplication, unit-vector closed forms, and
+    the same rotation as the half-split layout up to the index map above."""
+    rng = np.random.default_rng(11)
+    for D, theta in ((64, 1e4), (128, 1e6), (8, 10.0)):
+        x = rng.standard_normal((7, D))
+        sh = rng.integers(-40000, 40000, 7).astype(np.float64)
+        y = oracle.rope(x, sh, theta, interleaved=True)
+        np.testing.assert_allclose(y, rot_complex_adjacent(x, sh, theta), rtol=0, atol=1e-9)
+        m = half_split_to_adjacent(D)
+        np.testing.assert_allclose(y, oracle.rope(x[:, np.argsort(m)], sh, theta)[:, m],
+                                   rtol=0, atol=1e-12)
+    D, theta = 16, 100.0
+    for i in range(D // 2):
+        w = theta ** (-2.0 * i / D)
+        e = np.zeros(D)
+        e[2 * i] = 1.0
+        expect = np.zeros(D)
+        expect[2 * i], expect[2 * i + 1] = np.cos(w), np.sin(w)
+        np.testing.assert_allclose(oracle.rope(e, 1.0, theta, interleaved=True), expect, atol=1e-15)
+
+
+def pin_interleaved_layout_is_a_relabelling():
+    """Attention scores are dot products, so storing every head in the
+    adjacent layout (keys, queries, query keys relabelled by the same index
+    map) and rotating with adjacent pairs gives the half-split result; the
+    values keep their layout.  The stitch, likewise, is the half-split stitch
+    relabelled."""
+    rng = np.random.default_rng(12)
+    U, P, Lq, G, D, theta = 3, 9, 5, 2, 16, 1e4
+    m = half_split_to_adjacent(D)
+    kc = rng.standard_normal((U, P, D))
+    vc = rng.standard_normal((U, P, D))
+    q = rng.standard_normal((U, Lq, G, D))
+    kq = rng.standard_normal((U, Lq, D))
+    vq = rng.standard_normal((U, Lq, D))
+    ref = oracle.query_attention(kc, vc, q, kq, vq, theta)
+    got = oracle.query_attention(kc[..., m], vc, q[..., m], kq[..., m], vq, theta, interleaved=True)
+    np.testing.assert_allclose(got, ref, atol=1e-12)
+    L, H, n = 2, 2, 12
+    raw = {c: rng.standard_normal((L, H, n, D)) for c in (4, 7)}
+    vals = {c: rng.standard_normal((L, H, n, D)) for c in raw}
+    spans = [(7, 2, 9), (4, 0, 5), (7, 10, 12)]
+    Kh, Vh, _ = oracle.assemble({c: (raw[c], vals[c]) for c in raw}, spans, theta, first_pos=3)
+    Ki, Vi, _ = oracle.assemble({c: (raw[c][..., m], vals[c]) for c in raw}, spans, theta,
+                                first_pos=3, interleaved=True)
+    np.testing.assert_allclose(Ki, Kh[..., m], atol=1e-12)
+    assert np.array_equal(Vi, Vh)
+
+
 def pin_assemble_is_rope_at_target():
     """A span cached at chunk-local positions and re-rotated equals the raw key
     rotated at its target position; values are copied bit-exactly."""
@@ -282,6 +356,7 @@ def pin_attention_zero_query_is_mean():
 PINS = [pin_fig5_worked_example, pin_delta_formula_and_brute_force, pin_composite_positions,
         pin_rope_identity, pin_rope_vs_complex, pin_rope_closed_form,
         pin_rope_composition_and_norm, pin_rope_relative_position,
+        pin_rope_interleaved, pin_interleaved_layout_is_a_relabelling,
         pin_assemble_is_rope_at_target, pin_unrotated_sources_take_rope_at_their_positions,
         pin_attention_single_chunk_is_causal_attention,
         pin_attention_single_visible_key, pin_attention_zero_query_is_mean]
