@@ -92,7 +92,8 @@ constexpr int kNumBars = kBarReady + kSlots;
 constexpr int kOffMeta = kOffBar + 8 * kNumBars;  // [2][128] int: rotation of each row of the K slots
 constexpr int kOffTmemAddr = kOffMeta + 2 * kTileN * 4;
 constexpr int kOffAbort = kOffTmemAddr + 4;
-constexpr int kSmemBytes = kOffAbort + 4 + 1024;   // + alignment slack
+constexpr int kOffArrival = kOffAbort + 4;        // [2] arrival rank of a half unit's tile x
+constexpr int kSmemBytes = kOffArrival + 8 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kNoRotation = INT32_MIN;            // meta value of a row that is not a pool row
 
@@ -177,6 +178,12 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
 
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (the tensor core reads its operands through it).
+// Fetch a tensor map (a kernel parameter) ahead of its first copy.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -399,6 +406,15 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return d;
 }
 
+// Named barrier of the 128 threads of a softmax warpgroup (ids 1 and 2).
+__device__ __forceinline__ void wg_sync(int x)
+{
+    if (x == 0)
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+    else
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -513,6 +529,17 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     }
     if (warp == 9)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    if (warp == 8 && lane == 0) {   // descriptors only: nothing the previous kernel writes
+        prefetch_tmap(&tmq);
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+        if constexpr (kG) {
+            prefetch_tmap(&tmpk);
+            prefetch_tmap(&tmpv);
+            prefetch_tmap(&tmbk);
+            prefetch_tmap(&tmbv);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -625,57 +652,110 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             }
             if (!ok)
                 break;
-            // epilogue: O / l -> bf16 -> out[l][q_off + t][h*G + g][:]
+            // epilogue: O / l -> bf16 -> out[l][q_off + t][h*G + g][:], read from
+            // TMEM 64 columns at a time (a whole row of O in registers spills)
             if (!mbar_wait(bar(kBarOFull + x), o_cnt & 1, abort_flag)) {
                 ok = false;
                 break;
             }
             ++o_cnt;
             tc_fence_after();
-            float o[kD];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                tmem_ld32(lane_base + col_o(x) + 32 * q, o + 32 * q);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(kBarOEmpty + x));      // O_x may now take the next unit's PV
-            if (itm.half >= 0) {
-                // half a unit: its state (O unnormalized, running max, sum) for
-                // the merge kernel, 16-byte pieces laid out [piece][row]
-                float *pp = a.part + ((size_t)(it - a.n_full) * 2 + x) * kAttnPartFloats;
+            const uint32_t o_tm = lane_base + col_o(x);
+            float l_fin = l_run;
+            // a split unit whose second half reaches this tile: both halves leave
+            // their state (O unnormalized, running max, sum; 16-byte pieces laid
+            // out [piece][row]) in part, and the second to finish merges the two
+            // in a fixed order (half 0 first), so the result does not depend on
+            // which finished first.  Nothing waits: the count decides.
+            const float4 *qo = nullptr;   // the other half's O, when this half merges
+            float w_self = 1.f, w_oth = 0.f;
+            const bool first = itm.half == 0;
+            if (itm.half >= 0 && (w.n_tiles + 1) / 2 < w.n_t[x]) {
+                const int tail = it - a.n_full;
+                float *pp = a.part + ((size_t)tail * 2 + x) * kAttnPartFloats;
                 float4 *po = reinterpret_cast<float4 *>(pp);
 #pragma unroll
-                for (int c = 0; c < kD / 4; ++c)
-                    po[c * kTileM + r] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                for (int hh = 0; hh < 2; ++hh) {
+                    float f[64];
+                    tmem_ld32(o_tm + 64 * hh, f);
+                    tmem_ld32(o_tm + 64 * hh + 32, f + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        po[(16 * hh + c) * kTileM + r] = make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
+                }
                 pp[kTileM * kD + r] = m_run;
                 pp[kTileM * kD + kTileM + r] = l_run;
-            } else {
-                const float inv = row_ok ? 1.f / l_run : 0.f;
-                const int64_t orow = row_ok ? (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD
-                                            : -1;
-                __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
-                const uint32_t stg = sbase + kOffStage + (uint32_t)warp * 32 * 128;
-                const int wr = r & 31;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float *f = o + 64 * hh + 8 * c;
-                        st_shared_v4(stg + wr * 128 + ((c ^ (wr & 7)) << 4), pack_bf16(f[0] * inv, f[1] * inv),
-                                     pack_bf16(f[2] * inv, f[3] * inv), pack_bf16(f[4] * inv, f[5] * inv),
-                                     pack_bf16(f[6] * inv, f[7] * inv));
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int row = 4 * i + (lane >> 3), c = lane & 7;
-                        const int64_t base = __shfl_sync(0xffffffffu, orow, row);
-                        const uint4 v = ld_shared_v4(stg + row * 128 + ((c ^ (row & 7)) << 4));
-                        if (base >= 0)
-                            *reinterpret_cast<uint4 *>(out + base + 64 * hh + 8 * c) = v;
-                    }
-                    __syncwarp();
+                __threadfence();
+                wg_sync(x);
+                volatile int *arrival = reinterpret_cast<volatile int *>(smem + kOffArrival);
+                if (r == 0) {
+                    const int rank = atomicAdd(a.part_ctr + (tail >> 1) * 2 + x, 1);
+                    __threadfence();
+                    arrival[x] = rank;
                 }
+                wg_sync(x);
+                if (arrival[x] == 0) {             // the other half merges
+                    tc_fence_before();
+                    mbar_arrive(bar(kBarOEmpty + x));
+                    continue;
+                }
+                const float *qp = a.part + ((size_t)(tail ^ 1) * 2 + x) * kAttnPartFloats;
+                qo = reinterpret_cast<const float4 *>(qp);
+                const float m_oth = __ldcg(qp + kTileM * kD + r), l_oth = __ldcg(qp + kTileM * kD + kTileM + r);
+                const float m0 = first ? m_run : m_oth, m1 = first ? m_oth : m_run;
+                const float M = fmaxf(m0, m1);     // m0 is finite: every row sees key 0
+                const float w0 = ex2(m0 - M), w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+                l_fin = __fmaf_rn(first ? l_oth : l_run, w1, __fmul_rn(first ? l_run : l_oth, w0));
+                w_self = first ? w0 : w1;
+                w_oth = first ? w1 : w0;
+            }
+            const float inv = row_ok ? 1.f / l_fin : 0.f;
+            const int64_t orow = row_ok ? (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD
+                                        : -1;
+            __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+            const uint32_t stg = sbase + kOffStage + (uint32_t)warp * 32 * 128;
+            const int wr = r & 31;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float f[64];
+                tmem_ld32(o_tm + 64 * hh, f);
+                tmem_ld32(o_tm + 64 * hh + 32, f + 32);
+                tmem_wait_ld();
+                if (hh == 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar(kBarOEmpty + x));   // O_x may now take the next unit's PV
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        v[e] = f[8 * c + e];
+                    if (qo) {
+                        // half-0 value times w0 plus half-1 value times w1, one rounding order
+                        const int pc = 16 * hh + 2 * c;
+                        const float4 u0 = __ldcg(qo + pc * kTileM + r), u1 = __ldcg(qo + (pc + 1) * kTileM + r);
+                        const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            v[e] = first ? __fmaf_rn(u[e], w_oth, __fmul_rn(v[e], w_self))
+                                         : __fmaf_rn(v[e], w_self, __fmul_rn(u[e], w_oth));
+                    }
+                    st_shared_v4(stg + wr * 128 + ((c ^ (wr & 7)) << 4), pack_bf16(v[0] * inv, v[1] * inv),
+                                 pack_bf16(v[2] * inv, v[3] * inv), pack_bf16(v[4] * inv, v[5] * inv),
+                                 pack_bf16(v[6] * inv, v[7] * inv));
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 4 * i + (lane >> 3), c = lane & 7;
+                    const int64_t base = __shfl_sync(0xffffffffu, orow, row);
+                    const uint4 v = ld_shared_v4(stg + row * 128 + ((c ^ (row & 7)) << 4));
+                    if (base >= 0)
+                        *reinterpret_cast<uint4 *>(out + base + 64 * hh + 8 * c) = v;
+                }
+                __syncwarp();
             }
         }
         if (!ok)
@@ -1084,62 +1164,6 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     }
 }
 
-// The units that ran as two halves (n_full..): combine each row's two
-// online-softmax states (m, l, unnormalized O) in a fixed order and write the
-// normalized bf16 row.  Four CTAs per (unit, 128-row tile), 256 threads:
-// thread (row, k) takes 16-byte pieces 8 * blockIdx % 4 + 4k .. +3 of its row
-// (reads of consecutive rows are consecutive).
-constexpr int kMergeThreads = 256;
-__global__ void __launch_bounds__(kMergeThreads)
-    k_attention_merge(const __grid_constant__ AttnArgs a, const __grid_constant__ ReqTable rt, const int n_blocks)
-{
-    // the halves are written by the attention kernel just before
-    pdl_wait_prerequisites();
-    const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
-    const int tile = blockIdx.x >> 2, grp = blockIdx.x & 3;
-    const int tail = tile >> 1, x = tile & 1;
-    const Unit w = unit_at(a, reqs, n_blocks, a.n_full + tail);
-    const int r = threadIdx.x & (kTileM - 1), k = threadIdx.x >> 7, rr = w.row0[x] + r;
-    if (w.n_t[x] == 0 || rr >= w.m_rows)
-        return;
-    const bool two = (w.n_tiles + 1) / 2 < w.n_t[x];   // the second half reached this tile
-    const float *p0 = a.part + ((size_t)(2 * tail) * 2 + x) * kAttnPartFloats;
-    const float *p1 = a.part + ((size_t)(2 * tail + 1) * 2 + x) * kAttnPartFloats;
-    const float m0 = p0[kTileM * kD + r];
-    float w0 = 1.f, w1 = 0.f, L = p0[kTileM * kD + kTileM + r];
-    if (two) {
-        const float m1 = p1[kTileM * kD + r];
-        const float M = fmaxf(m0, m1);   // m0 is finite: every row sees key 0
-        w0 = ex2(m0 - M);
-        w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
-        L = L * w0 + p1[kTileM * kD + kTileM + r] * w1;
-    }
-    const float inv = 1.f / L;
-    const int G = a.n_q_heads / a.n_kv_heads;
-    const int t = rr / G, g = rr - t * G;
-    uint2 *dst = reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.out) +
-                                           (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD);
-    const float4 *o0 = reinterpret_cast<const float4 *>(p0);
-    const float4 *o1 = reinterpret_cast<const float4 *>(p1);
-    float4 v[4], u[4];
-    const int c0 = 8 * grp + 4 * k;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[i] = o0[(c0 + i) * kTileM + r];
-        if (two)
-            u[i] = o1[(c0 + i) * kTileM + r];
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float4 q = v[i];
-        q.x *= w0, q.y *= w0, q.z *= w0, q.w *= w0;
-        if (two) {
-            q.x += u[i].x * w1, q.y += u[i].y * w1, q.z += u[i].z * w1, q.w += u[i].w * w1;
-        }
-        dst[c0 + i] = make_uint2(pack_bf16(q.x * inv, q.y * inv), pack_bf16(q.z * inv, q.w * inv));
-    }
-}
-
 bool attention_tc_supported(int dtype, int head_dim) { return dtype == KVR_DTYPE_BF16 && head_dim == kD; }
 
 template <bool kG>
@@ -1190,20 +1214,7 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
         return cudaErrorInvalidValue;
     const int64_t items = 2 * units - ta.base.n_full;
     const int grid = (int)(items < ta.n_sms ? items : ta.n_sms);
-    cudaError_t e = ta.gather ? launch_variant<true>(ta, grid, pdl, s) : launch_variant<false>(ta, grid, pdl, s);
-    if (e != cudaSuccess || ta.base.n_full == units)
-        return e;
-    // the split units' halves, merged right after
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(8 * (units - ta.base.n_full)));
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_attention_merge, ta.base, *ta.rt, ta.n_m_blocks);
+    return ta.gather ? launch_variant<true>(ta, grid, pdl, s) : launch_variant<false>(ta, grid, pdl, s);
 }
 
 }  // namespace kvr

@@ -183,10 +183,13 @@ struct AttnArgs {
     float scale_log2;           // softmax scale * log2(e)
     int *err;
     // tensor-core kernel: units n_full.. (the last wave's, when two halves of
-    // each fit one wave) run as two halves of their key range, leaving their
-    // online-softmax state in part for the merge kernel
+    // each fit one wave) run as two halves of their key range; each half
+    // leaves its online-softmax state in part, and the second half of a
+    // (unit, tile) to finish (counted in part_ctr, zeroed by the query
+    // prologue) merges the two
     int32_t n_full;
     float *part;
+    int32_t *part_ctr;
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
 };
 // fp32 words of one half-unit partial (one 128-row tile): O, then m, then l
@@ -206,6 +209,8 @@ struct QueryPrologueArgs {
     int32_t max_q_len;          // longest query of the batch
     int32_t n_reqs;
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
+    int32_t *zero;              // n_zero words set to 0 (the attention's half-unit counters)
+    int32_t n_zero;
 };
 
 // ---- launchers (each returns the cudaGetLastError of its launch) ----
