@@ -93,7 +93,6 @@ struct kvr_pool {
     size_t q_rot_cap = 0;
     cudaEvent_t q_rot_done = nullptr;
     bool q_rot_used = false;
-    float *part = nullptr;      // half-unit states of the attention's last wave (ordered like q_rot)
     cudaEvent_t timing[6] = {};  // optional kernel timing events (caller-owned)
     bool timed = false;
 
@@ -244,8 +243,6 @@ extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
     }
     if (p->q_rot)
         cudaFree(p->q_rot);
-    if (p->part)
-        cudaFree(p->part);
     if (p->rope)
         cudaFree(p->rope);
     if (p->err)
@@ -785,27 +782,15 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
     if (pl.tc) {
         TcAttnArgs ta{pl.at, &rt, &pl.mq, &pl.mk, &pl.mv, pl.m_blocks, p->n_sms};
         // the last wave's units split in two halves of their keys when two
-        // halves of each fit one wave: per half and tile a state of
-        // kAttnPartFloats floats, per split unit and tile one arrival counter
+        // halves of each fit one wave and the grid can run as two-CTA clusters
         const int64_t units = (int64_t)pl.m_blocks * p->d.n_layers * p->d.n_kv_heads;
         const int64_t tail = units % p->n_sms;
-        const size_t part_floats = 2 * (size_t)p->n_sms * kAttnPartFloats;
         ta.base.n_full = (int32_t)units;
-        if (tail > 0 && 2 * tail <= p->n_sms) {
-            if (!p->part &&
-                cudaMalloc(&p->part, sizeof(float) * part_floats + sizeof(int32_t) * (size_t)p->n_sms) != cudaSuccess) {
-                cudaGetLastError();
-                p->part = nullptr;
-            }
-            if (p->part) {
-                ta.base.n_full = (int32_t)(units - tail);
-                ta.base.part = p->part;
-                ta.base.part_ctr = reinterpret_cast<int32_t *>(p->part + part_floats);
-            }
-        }
+        if (tail > 0 && 2 * tail <= p->n_sms && attention_tc_pairs_fit(p->n_sms, gl != nullptr))
+            ta.base.n_full = (int32_t)(units - tail);
         QueryPrologueArgs qp{pl.at.reqs, p->rope, pl.q, pl.kq, pl.vq, pl.cache_k, pl.cache_v, p->q_rot,
                              p->d.n_layers, p->d.n_q_heads, p->d.n_kv_heads, pl.T, pl.max_lq, pl.batch,
-                             pl.at.interleaved, ta.base.part_ctr, (int32_t)(2 * (units - ta.base.n_full))};
+                             pl.at.interleaved};
         p->mark(2, s);
         e = launch_query_prologue(qp, rt, p->n_sms, after_assemble && !p->timed, s);
         p->mark(3, s);

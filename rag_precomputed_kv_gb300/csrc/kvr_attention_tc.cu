@@ -48,6 +48,7 @@
 // freed before the CTA exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kvr_internal.cuh"
 
@@ -88,12 +89,24 @@ constexpr int kBarQFull = kBarOEmpty + 2;         // Q tiles landed
 constexpr int kBarQEmpty = kBarQFull + 1;         // all S of the unit done with Q
 constexpr int kBarDrain = kBarQEmpty + 1;
 constexpr int kBarReady = kBarDrain + 1;          // [kSlots] gathered tile rotated / patched (64 arrivals)
-constexpr int kNumBars = kBarReady + kSlots;
+// split units (two-CTA cluster, half h on CTA rank h; rank x merges tile x):
+// the partner's half of this CTA's tile has landed in its shared memory (128
+// arrivals); the partner's MMAs are all done, so its K/V ring and Q tiles may
+// take this CTA's half of the partner's tile
+constexpr int kBarPeerData = kBarReady + kSlots;
+constexpr int kBarPeerFree = kBarPeerData + 1;
+constexpr int kNumBars = kBarPeerFree + 1;
 constexpr int kOffMeta = kOffBar + 8 * kNumBars;  // [2][128] int: rotation of each row of the K slots
 constexpr int kOffTmemAddr = kOffMeta + 2 * kTileN * 4;
 constexpr int kOffAbort = kOffTmemAddr + 4;
-constexpr int kOffArrival = kOffAbort + 4;        // [2] arrival rank of a half unit's tile x
-constexpr int kSmemBytes = kOffArrival + 8 + 1024;   // + alignment slack
+constexpr int kSmemBytes = kOffAbort + 4 + 1024;   // + alignment slack
+// where a split unit's partner CTA leaves its half of this CTA's tile: O as
+// fp16 with a power-of-two scale per row ([16-byte piece of 8][row]) over the
+// K/V ring; the running max, sum and scale (fp32 [3][128]) over the Q tiles
+constexpr int kOffPeerO = kOffKV;
+constexpr int kPeerOBytes = kTileM * kD * 2;
+constexpr int kOffPeerML = kOffQ;
+static_assert(kPeerOBytes <= kSlots * kTileBytes && 3 * kTileM * 4 <= 2 * kTileBytes, "peer state");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kNoRotation = INT32_MIN;            // meta value of a row that is not a pool row
 
@@ -406,13 +419,68 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return d;
 }
 
-// Named barrier of the 128 threads of a softmax warpgroup (ids 1 and 2).
-__device__ __forceinline__ void wg_sync(int x)
+// ---- the two CTAs of a cluster (split units) ----
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank)
 {
-    if (x == 0)
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-    else
-        asm volatile("bar.sync 2, 128;" ::: "memory");
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
+}
+
+// Arrive on a barrier of another CTA of the cluster, releasing this thread's
+// earlier writes to that CTA's shared memory.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+// Bounded wait that acquires at cluster scope (sees the writes another CTA
+// released before arriving).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag)
+{
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok)
+            return true;
+        if (*abort_flag)
+            return false;
+        if (globaltimer() - t0 > kWaitNs)
+            return false;
+    }
+}
+
+// All threads of both CTAs of the cluster (a launch without clusters is a
+// cluster of one CTA).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
@@ -520,7 +588,8 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const bool wg = (i >= kBarPFull && i < kBarPFull + 2) || (i >= kBarOEmpty && i < kBarOEmpty + 2);
+            const bool wg = (i >= kBarPFull && i < kBarPFull + 2) || (i >= kBarOEmpty && i < kBarOEmpty + 2) ||
+                            i == kBarPeerData;
             const bool rot = i >= kBarReady && i < kBarReady + kSlots;
             mbar_init(bar(i), wg ? 128u : rot ? (uint32_t)kRotThreads : 1u);
         }
@@ -543,6 +612,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    cluster_sync();   // the partner CTA's barriers are initialised before any remote arrive
     const uint32_t tmem = *tmem_slot;
     // setup above overlaps the previous kernel's tail; its outputs (the
     // stitched cache, the rotated queries) are read only from here on
@@ -662,18 +732,23 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             tc_fence_after();
             const uint32_t o_tm = lane_base + col_o(x);
             float l_fin = l_run;
-            // a split unit whose second half reaches this tile: both halves leave
-            // their state (O unnormalized, running max, sum; 16-byte pieces laid
-            // out [piece][row]) in part, and the second to finish merges the two
-            // in a fixed order (half 0 first), so the result does not depend on
-            // which finished first.  Nothing waits: the count decides.
-            const float4 *qo = nullptr;   // the other half's O, when this half merges
-            float w_self = 1.f, w_oth = 0.f;
-            const bool first = itm.half == 0;
-            if (itm.half >= 0 && (w.n_tiles + 1) / 2 < w.n_t[x]) {
-                const int tail = it - a.n_full;
-                float *pp = a.part + ((size_t)tail * 2 + x) * kAttnPartFloats;
-                float4 *po = reinterpret_cast<float4 *>(pp);
+            // a split unit whose second half reaches this tile: the two halves run
+            // on the two CTAs of a cluster (half h on rank h), and rank x merges
+            // tile x, half 0 first (one rounding order); the other CTA sends its
+            // half of tile x through distributed shared memory, O as fp16 with a
+            // power-of-two scale per row (exact to ~2^-12, below the output's bf16
+            // rounding, at half the bytes of fp32).  Nothing of it touches L2.
+            const bool split2 = itm.half >= 0 && (w.n_tiles + 1) / 2 < w.n_t[x];
+            const bool merger = split2 && itm.half == x;
+            const uint32_t peer_o = sbase + kOffPeerO, peer_ml = sbase + kOffPeerML;
+            if (split2 && !merger) {
+                // the partner's ring and Q tiles are free once its MMAs are done
+                if (!mbar_wait_cluster(bar(kBarPeerFree), 0, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t peer = (uint32_t)x;
+                float amax = 0.f;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     float f[64];
@@ -681,34 +756,54 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                     tmem_ld32(o_tm + 64 * hh + 32, f + 32);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        po[(16 * hh + c) * kTileM + r] = make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
+                    for (int e = 0; e < 64; ++e)
+                        amax = fmaxf(amax, fabsf(f[e]));
                 }
-                pp[kTileM * kD + r] = m_run;
-                pp[kTileM * kD + kTileM + r] = l_run;
-                __threadfence();
-                wg_sync(x);
-                volatile int *arrival = reinterpret_cast<volatile int *>(smem + kOffArrival);
-                if (r == 0) {
-                    const int rank = atomicAdd(a.part_ctr + (tail >> 1) * 2 + x, 1);
-                    __threadfence();
-                    arrival[x] = rank;
+                // scale 2^k with amax / 2^k in [2^14, 2^15): no fp16 overflow
+                const int be = (__float_as_int(amax) >> 23) & 0xff;
+                const int se = be >= 15 ? be - 14 : 1;
+                const float scale = __int_as_float(se << 23), inv_scale = __int_as_float((254 - se) << 23);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float f[64];
+                    tmem_ld32(o_tm + 64 * hh, f);
+                    tmem_ld32(o_tm + 64 * hh + 32, f + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t hw[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const __half2 h2 = __floats2half2_rn(f[8 * c + 2 * q] * inv_scale, f[8 * c + 2 * q + 1] * inv_scale);
+                            hw[q] = *reinterpret_cast<const uint32_t *>(&h2);
+                        }
+                        st_cluster_v4(mapa_rank(peer_o + (uint32_t)(((8 * hh + c) * kTileM + r) * 16), peer),
+                                      __uint_as_float(hw[0]), __uint_as_float(hw[1]), __uint_as_float(hw[2]),
+                                      __uint_as_float(hw[3]));
+                    }
                 }
-                wg_sync(x);
-                if (arrival[x] == 0) {             // the other half merges
-                    tc_fence_before();
-                    mbar_arrive(bar(kBarOEmpty + x));
-                    continue;
+                st_cluster_f32(mapa_rank(peer_ml + (uint32_t)r * 4, peer), m_run);
+                st_cluster_f32(mapa_rank(peer_ml + (uint32_t)(kTileM + r) * 4, peer), l_run);
+                st_cluster_f32(mapa_rank(peer_ml + (uint32_t)(2 * kTileM + r) * 4, peer), scale);
+                mbar_arrive_remote(mapa_rank(bar(kBarPeerData), peer));
+                tc_fence_before();
+                mbar_arrive(bar(kBarOEmpty + x));
+                continue;
+            }
+            float w0 = 1.f, w1 = 0.f, p_scale = 0.f;
+            if (merger) {
+                if (!mbar_wait_cluster(bar(kBarPeerData), 0, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                const float *qp = a.part + ((size_t)(tail ^ 1) * 2 + x) * kAttnPartFloats;
-                qo = reinterpret_cast<const float4 *>(qp);
-                const float m_oth = __ldcg(qp + kTileM * kD + r), l_oth = __ldcg(qp + kTileM * kD + kTileM + r);
-                const float m0 = first ? m_run : m_oth, m1 = first ? m_oth : m_run;
+                const float mp = ld_shared_f32(peer_ml + (uint32_t)r * 4);
+                const float lp = ld_shared_f32(peer_ml + (uint32_t)(kTileM + r) * 4);
+                p_scale = ld_shared_f32(peer_ml + (uint32_t)(2 * kTileM + r) * 4);
+                const float m0 = x == 0 ? m_run : mp, m1 = x == 0 ? mp : m_run;   // halves 0 and 1
                 const float M = fmaxf(m0, m1);     // m0 is finite: every row sees key 0
-                const float w0 = ex2(m0 - M), w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
-                l_fin = __fmaf_rn(first ? l_oth : l_run, w1, __fmul_rn(first ? l_run : l_oth, w0));
-                w_self = first ? w0 : w1;
-                w_oth = first ? w1 : w0;
+                w0 = ex2(m0 - M);
+                w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+                l_fin = __fmaf_rn(x == 0 ? lp : l_run, w1, __fmul_rn(x == 0 ? l_run : lp, w0));
             }
             const float inv = row_ok ? 1.f / l_fin : 0.f;
             const int64_t orow = row_ok ? (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD
@@ -732,15 +827,22 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         v[e] = f[8 * c + e];
-                    if (qo) {
-                        // half-0 value times w0 plus half-1 value times w1, one rounding order
-                        const int pc = 16 * hh + 2 * c;
-                        const float4 u0 = __ldcg(qo + pc * kTileM + r), u1 = __ldcg(qo + (pc + 1) * kTileM + r);
-                        const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                    if (merger) {
+                        // half-0 value times w0 plus half-1 value times w1
+                        const uint4 u = ld_shared_v4(peer_o + (uint32_t)(((8 * hh + c) * kTileM + r) * 16));
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            v[e] = first ? __fmaf_rn(u[e], w_oth, __fmul_rn(v[e], w_self))
-                                         : __fmaf_rn(v[e], w_self, __fmul_rn(u[e], w_oth));
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 pv = __half22float2(*reinterpret_cast<const __half2 *>(&uw[q]));
+                            const float p0 = pv.x * p_scale, p1 = pv.y * p_scale;
+                            if (x == 0) {
+                                v[2 * q] = __fmaf_rn(p0, w1, __fmul_rn(v[2 * q], w0));
+                                v[2 * q + 1] = __fmaf_rn(p1, w1, __fmul_rn(v[2 * q + 1], w0));
+                            } else {
+                                v[2 * q] = __fmaf_rn(v[2 * q], w1, __fmul_rn(p0, w0));
+                                v[2 * q + 1] = __fmaf_rn(v[2 * q + 1], w1, __fmul_rn(p1, w0));
+                            }
+                        }
                     }
                     st_shared_v4(stg + wr * 128 + ((c ^ (wr & 7)) << 4), pack_bf16(v[0] * inv, v[1] * inv),
                                  pack_bf16(v[2] * inv, v[3] * inv), pack_bf16(v[4] * inv, v[5] * inv),
@@ -943,6 +1045,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             int tt = 0, nq = 0;
             int p_cnt[2] = {0, 0}, oe_cnt[2] = {0, 0};
             bool o_used[2] = {false, false};
+            int peer_wait = -1;   // the last item is half h of a split unit whose tile h the other half reaches
             bool ok = true;
             // descriptors: K-major 128B-swizzled tiles (Q, K) and the MN-major V tile
             const uint64_t d_k_major = sdesc(sbase, 16, 1024);
@@ -977,6 +1080,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 if (je <= jb)
                     continue;
                 const int jx[2] = {min(je, w.n_t[0]), min(je, w.n_t[1])};   // tile x's key tiles: [jb, jx[x])
+                peer_wait = itm.half >= 0 && (w.n_tiles + 1) / 2 < w.n_t[itm.half] ? itm.half : -1;
                 if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag) || !wait_kv(tt)) {
                     ok = false;
                     break;
@@ -1045,8 +1149,13 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             // drain: all issued MMAs complete before TMEM is released
             umma_commit(lead, bar(kBarDrain));
             const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(bar(kBarDrain), 0) && globaltimer() - t0 < kWaitNs) {
+            bool drained = false;
+            while (!(drained = mbar_try_wait(bar(kBarDrain), 0)) && globaltimer() - t0 < kWaitNs) {
             }
+            // a split unit whose tile (this CTA's rank) the partner's half reaches:
+            // the partner may now write its half over this CTA's K/V ring and Q tiles
+            if (ok && drained && peer_wait >= 0 && lane == 0)
+                mbar_arrive_remote(mapa_rank(bar(kBarPeerFree), (uint32_t)(1 - peer_wait)));
         }
     } else if constexpr (kG) {
         // =================== rotator (gathering variant, warps 10-11) ===================
@@ -1158,6 +1267,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();   // no CTA leaves while its partner may still touch its shared memory
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -1167,7 +1277,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
 bool attention_tc_supported(int dtype, int head_dim) { return dtype == KVR_DTYPE_BF16 && head_dim == kD; }
 
 template <bool kG>
-static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, cudaStream_t s)
+static cudaError_t set_smem_attr()
 {
     // the shared-memory opt-in is per device and per kernel
     static bool attr_set[64] = {};
@@ -1182,6 +1292,49 @@ static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, cuda
         if (dev < 64)
             attr_set[dev] = true;
     }
+    return cudaSuccess;
+}
+
+template <bool kG>
+static bool pairs_fit(int n_sms)
+{
+    static int fit[64] = {};   // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || (n_sms & 1))
+        return false;
+    if (fit[dev] == 0) {
+        if (set_smem_attr<kG>() != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(n_sms);
+        cfg.blockDim = dim3(kG ? kThreadsG : kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_attention_tc<kG>, &cfg);
+        if (e != cudaSuccess)
+            cudaGetLastError();
+        fit[dev] = (e == cudaSuccess && 2 * n >= n_sms) ? 1 : 2;
+    }
+    return fit[dev] == 1;
+}
+
+bool attention_tc_pairs_fit(int n_sms, bool gather) { return gather ? pairs_fit<true>(n_sms) : pairs_fit<false>(n_sms); }
+
+template <bool kG>
+static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool pairs, cudaStream_t s)
+{
+    cudaError_t e = set_smem_attr<kG>();
+    if (e != cudaSuccess)
+        return e;
     static const CUtensorMap no_map{};
     static const GatherArgs no_gather{};
     static const SpanTable no_spans{};
@@ -1190,11 +1343,22 @@ static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, cuda
     cfg.blockDim = dim3(kG ? kThreadsG : kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchAttribute attr[2];
+    int n_attr = 0;
+    if (pdl) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
+    if (pairs) {   // split units: half 0 on the even CTA of a cluster, half 1 on the odd one
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 2;
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
     return cudaLaunchKernelEx(&cfg, k_attention_tc<kG>, *static_cast<const CUtensorMap *>(ta.tmap_q),
                               *static_cast<const CUtensorMap *>(ta.tmap_k),
                               *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base, *ta.rt, ta.n_m_blocks,
@@ -1214,7 +1378,12 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
         return cudaErrorInvalidValue;
     const int64_t items = 2 * units - ta.base.n_full;
     const int grid = (int)(items < ta.n_sms ? items : ta.n_sms);
-    return ta.gather ? launch_variant<true>(ta, grid, pdl, s) : launch_variant<false>(ta, grid, pdl, s);
+    const bool pairs = ta.base.n_full < units;
+    // the two halves of split unit i are items n_full + 2i and n_full + 2i + 1:
+    // CTAs 2i and 2i + 1 of the last round when n_full is a multiple of the grid
+    if (pairs && ((grid & 1) || ta.base.n_full % grid != 0))
+        return cudaErrorInvalidValue;
+    return ta.gather ? launch_variant<true>(ta, grid, pdl, pairs, s) : launch_variant<false>(ta, grid, pdl, pairs, s);
 }
 
 }  // namespace kvr

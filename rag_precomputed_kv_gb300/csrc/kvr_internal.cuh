@@ -183,17 +183,12 @@ struct AttnArgs {
     float scale_log2;           // softmax scale * log2(e)
     int *err;
     // tensor-core kernel: units n_full.. (the last wave's, when two halves of
-    // each fit one wave) run as two halves of their key range; each half
-    // leaves its online-softmax state in part, and the second half of a
-    // (unit, tile) to finish (counted in part_ctr, zeroed by the query
-    // prologue) merges the two
+    // each fit one wave) run as two halves of their key range on the two CTAs
+    // of a cluster, which merge them; n_full < units requires a launch in
+    // two-CTA clusters
     int32_t n_full;
-    float *part;
-    int32_t *part_ctr;
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
 };
-// fp32 words of one half-unit partial (one 128-row tile): O, then m, then l
-constexpr int kAttnPartFloats = 128 * 128 + 2 * 128;
 
 struct QueryPrologueArgs {
     const DevReq *reqs;         // NULL: the ReqTable parameter holds the requests
@@ -209,8 +204,6 @@ struct QueryPrologueArgs {
     int32_t max_q_len;          // longest query of the batch
     int32_t n_reqs;
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
-    int32_t *zero;              // n_zero words set to 0 (the attention's half-unit counters)
-    int32_t n_zero;
 };
 
 // ---- launchers (each returns the cudaGetLastError of its launch) ----
@@ -262,7 +255,11 @@ cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt
                                   cudaStream_t s);
 // `pdl`: the kernel before it on the stream is the query prologue of the
 // same call; the setup (barriers, TMEM) overlaps that kernel's tail.
+// Launched in two-CTA clusters when a.base.n_full < units.
 cudaError_t launch_attention_tc(const TcAttnArgs &a, bool pdl, cudaStream_t s);
 bool attention_tc_supported(int dtype, int head_dim);
+// Whether `n_sms` CTAs of the attention kernel (gathering variant or not) can
+// be resident at once as two-CTA clusters.
+bool attention_tc_pairs_fit(int n_sms, bool gather);
 
 }  // namespace kvr

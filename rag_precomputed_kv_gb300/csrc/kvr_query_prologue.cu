@@ -68,10 +68,6 @@ __global__ void __launch_bounds__(kQpThreads)
     __nv_bfloat16 *ck = static_cast<__nv_bfloat16 *>(a.cache_k);
     __nv_bfloat16 *cv = static_cast<__nv_bfloat16 *>(a.cache_v);
     __nv_bfloat16 *qr = static_cast<__nv_bfloat16 *>(a.q_rot);
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < a.n_zero; i += blockDim.x)
-            a.zero[i] = 0;
-
     for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int64_t rc = it % n_rc;
         const int lh = (int)(it / n_rc);
