@@ -794,7 +794,15 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         p->mark(2, s);
         e = launch_query_prologue(qp, rt, p->n_sms, after_assemble && !p->timed, s);
         p->mark(3, s);
-        if (e == cudaSuccess) {
+        // a decode step (one query token per request) streams each cache
+        // block with its own kernel
+        const bool decode = !gl && pl.max_lq == 1 &&
+                            decode_supported(p->d.dtype, D, p->d.n_q_heads / p->d.n_kv_heads);
+        if (e == cudaSuccess && decode) {
+            p->mark(4, s);
+            e = launch_decode_attention(pl.at, rt, &pl.mk, &pl.mv, p->q_rot, !p->timed, s);
+            p->mark(5, s);
+        } else if (e == cudaSuccess) {
             if (gl) {
                 ta.gather = true;
                 ta.tmap_pk = &gl->mpk;

@@ -258,6 +258,13 @@ cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt
 // Launched in two-CTA clusters when a.base.n_full < units.
 cudaError_t launch_attention_tc(const TcAttnArgs &a, bool pdl, cudaStream_t s);
 bool attention_tc_supported(int dtype, int head_dim);
+// Attention of a decode step (every request has one query token, or none):
+// one CTA per (request, layer, kv-head) streams the cache block.  Uses the
+// query prologue's rotated heads (q_rot) and the cache tensor maps of the
+// prefill attention.  `pdl`: launched right after the query prologue.
+bool decode_supported(int dtype, int head_dim, int group);
+cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const void *tmap_k, const void *tmap_v,
+                                    const void *q_rot, bool pdl, cudaStream_t s);
 // Whether `n_sms` CTAs of the attention kernel (gathering variant or not) can
 // be resident at once as two-CTA clusters.
 bool attention_tc_pairs_fit(int n_sms, bool gather);

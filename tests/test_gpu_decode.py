@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 STEPS = 3
 
 
-def _run(cfg, reqs, sample_units=None):
+def _run(cfg, reqs, sample_units=None, skip=()):
+    """`skip`: requests that take no token in the decode steps (q_len 0)."""
     import torch
     case = Case(cfg, reqs=reqs, spare_rows=STEPS + 2)
     case.run(prefill=True)
@@ -53,24 +54,28 @@ def _run(cfg, reqs, sample_units=None):
     g = torch.Generator(device=dev)
     g.manual_seed(99)
     dt = case.t.q.dtype
-    qoffs = np.arange(B + 1, dtype=np.int32)
+    act = [b for b in range(B) if b not in skip]
+    tok = {b: i for i, b in enumerate(act)}
+    qoffs = np.concatenate([[0], np.cumsum([0 if b in skip else 1 for b in range(B)])]).astype(np.int32)
     worst = (0.0, 0.0)
     for step in range(STEPS):
         n = np.array([kc[b].shape[1] for b in range(B)], np.int32)   # rows before this step
-        q1 = torch.randn((L, B, Hq, D), generator=g, device=dev).to(dt)
-        k1 = torch.randn((L, B, H, D), generator=g, device=dev).to(dt)
-        v1 = torch.randn((L, B, H, D), generator=g, device=dev).to(dt)
+        T = len(act)
+        q1 = torch.randn((L, T, Hq, D), generator=g, device=dev).to(dt)
+        k1 = torch.randn((L, T, H, D), generator=g, device=dev).to(dt)
+        v1 = torch.randn((L, T, H, D), generator=g, device=dev).to(dt)
         o1 = torch.full_like(q1, float("nan"))
         case.pool.query_attention(case.cache_offsets, n, qoffs, q1, k1, v1, case.cache_k, case.cache_v, o1)
         torch.cuda.synchronize()
         case.pool.check()
         q1n, k1n, v1n, o1n = (to_np64(x) for x in (q1, k1, v1, o1))
-        for b in range(B):
-            qu = np.stack([q1n[l, b, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])   # [U, 1, G, D]
-            ku = np.stack([k1n[l, b, h][None] for l, h in zip(li, hi)])                    # [U, 1, D]
-            vu = np.stack([v1n[l, b, h][None] for l, h in zip(li, hi)])
+        for b in act:
+            t = tok[b]
+            qu = np.stack([q1n[l, t, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])   # [U, 1, G, D]
+            ku = np.stack([k1n[l, t, h][None] for l, h in zip(li, hi)])                    # [U, 1, D]
+            vu = np.stack([v1n[l, t, h][None] for l, h in zip(li, hi)])
             o_ref = oracle.query_attention(kc[b], vc[b], qu, ku, vu, cfg.rope_theta)
-            o_gpu = np.stack([o1n[l, b, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])
+            o_gpu = np.stack([o1n[l, t, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])
             ok, mx, rel = attn_within_tolerance(o_gpu, o_ref, cfg.dtype)
             assert ok, (step, b, mx, rel)
             worst = (max(worst[0], mx), max(worst[1], rel))
@@ -103,3 +108,23 @@ def test_decode_steps_fp32_cuda_cores():
 
 def test_decode_steps_default_workload_sampled():
     _run(W.CONFIGS[2], None, sample_units=6)
+
+
+@pytest.mark.parametrize("variant", ["g1", "g16", "short_blocks_and_idle_requests"])
+def test_decode_kernel_edges(variant):
+    """The streaming decode kernel: one and sixteen query heads per kv head,
+    cache blocks shorter than one 128-key tile, and requests that take no
+    token in a step (their CTAs leave at once)."""
+    pid = EDGE.n_chunks
+    lists = ([[pid, 0, 5], [0, 0, 96], [2, 10, 60]], [[1, 3, 90], [3, 0, 96]], [])
+    skip = ()
+    if variant == "g1":
+        cfg = dataclasses.replace(EDGE, n_q_heads=2, n_kv_heads=2, query_len=4)
+    elif variant == "g16":
+        cfg = dataclasses.replace(EDGE, n_q_heads=32, n_kv_heads=2, query_len=3, rope_theta=1e6)
+    else:
+        cfg = dataclasses.replace(EDGE, query_len=2)
+        lists = ([[pid, 0, 5]], [[0, 10, 40]], [[1, 0, 96], [2, 0, 96]], [])
+        skip = (1,)
+    reqs = [W.Request(np.asarray(r, np.int32).reshape(-1, 3), 0) for r in lists]
+    _run(dataclasses.replace(cfg, batch=len(reqs)), reqs, skip=skip)
