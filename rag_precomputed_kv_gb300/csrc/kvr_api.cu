@@ -791,16 +791,20 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         QueryPrologueArgs qp{pl.at.reqs, p->rope, pl.q, pl.kq, pl.vq, pl.cache_k, pl.cache_v, p->q_rot,
                              p->d.n_layers, p->d.n_q_heads, p->d.n_kv_heads, pl.T, pl.max_lq, pl.batch,
                              pl.at.interleaved};
-        p->mark(2, s);
-        e = launch_query_prologue(qp, rt, p->n_sms, after_assemble && !p->timed, s);
-        p->mark(3, s);
-        // a decode step (one query token per request) streams each cache
-        // block with its own kernel
+        // a decode step (one query token per request): one kernel rotates,
+        // appends and streams each cache block
         const bool decode = !gl && pl.max_lq == 1 &&
                             decode_supported(p->d.dtype, D, p->d.n_q_heads / p->d.n_kv_heads);
+        p->mark(2, s);
+        if (!decode)
+            e = launch_query_prologue(qp, rt, p->n_sms, after_assemble && !p->timed, s);
+        else
+            e = cudaSuccess;
+        p->mark(3, s);
         if (e == cudaSuccess && decode) {
+            const DecodeIO io{pl.kq, pl.vq, pl.cache_k, pl.cache_v, pl.at.interleaved};
             p->mark(4, s);
-            e = launch_decode_attention(pl.at, rt, &pl.mk, &pl.mv, p->q_rot, !p->timed, s);
+            e = launch_decode_attention(pl.at, rt, &pl.mk, &pl.mv, io, s);
             p->mark(5, s);
         } else if (e == cudaSuccess) {
             if (gl) {

@@ -1,13 +1,14 @@
 // kvr_decode.cu -- attention of a decode step over the stitched cache.
 //
 // CoinRAG blog section 2.3: after the query prefill the model decodes
-// normally on top of KV_CoinRAG; each step appends one token at position
-// P_b + Lq_b + s and attends to every cache row before it.  The query
-// prologue has already rotated the step's query heads (packed q_rot rows
-// [layer][kv-head][token][G][D]) and appended its key / value row; this kernel
-// computes, for every (request, layer, kv-head),
-//     o_g = sum_j softmax_j(q_g . k_j * scale) v_j,  j < n_valid = P_b + Lq_b,
-// for the G query heads of the kv head.
+// normally on top of KV_CoinRAG; each step appends one token at the next
+// row and position P_b of every cache block and attends to rows 0..P_b.  For
+// every (request, layer, kv-head) this kernel rotates the step's key by P_b
+// and appends it and its value at row P_b (TurboRAG blog, "Position ID":
+// contiguous positions), rotates the G query heads of the kv head by P_b, and
+// computes
+//     o_g = sum_j softmax_j(q_g . k_j * scale) v_j,  j <= P_b,
+// all in one pass over the block.
 //
 // A decode step reads the whole cache block once and does only G (<= 16)
 // rows of arithmetic per key: it is bound by HBM, not by the tensor cores.
@@ -20,6 +21,12 @@
 // throughput the step can use.  Each warp keeps an online softmax in registers
 // (the score fragment of one MMA is the P operand of the next); at the end the
 // four warps' states are combined in shared memory in a fixed order.
+//
+// The appended row reaches the computation through the kernel itself: the
+// warp whose keys hold row P_b writes it into the last shared-memory tile
+// (whatever the tile's copy read from memory), and every warp zeroes the V
+// rows of that tile past P_b, so that masked keys (p = 0) never meet a
+// non-finite value.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -150,7 +157,7 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c)
 __global__ void __launch_bounds__(kDecThreads, 1)
     k_decode_attention(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ AttnArgs a, const __grid_constant__ ReqTable rt,
-                       const __nv_bfloat16 *__restrict__ q_rot)
+                       const __grid_constant__ DecodeIO io)
 {
     extern __shared__ uint8_t dec_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dec_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -204,8 +211,59 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (; n_issued < n_t && n_issued < kDecStages; ++n_issued)
             issue(n_issued);
 
-    // Q fragments (A operand, 16 x 128, rows >= G zero): rows lane/4 and lane/4 + 8
-    const __nv_bfloat16 *qp = q_rot + ((int64_t)lh * a.total_q + rq.q_off) * G * kDecD;
+    const int P = rq.prefix;   // the step's row and position
+    const int l_idx = lh / a.n_kv_heads, h_idx = lh - l_idx * a.n_kv_heads;
+    const int64_t tok = (int64_t)l_idx * a.total_q + rq.q_off;
+    const bool il = io.interleaved != 0;
+    auto rot = [](float &x, float &y, float2 cs) {
+        const float xo = fmaf(x, cs.x, -(y * cs.y));
+        y = fmaf(x, cs.y, y * cs.x);
+        x = xo;
+    };
+    auto unpk = [](uint32_t u, float &lo, float &hi) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+        lo = f.x;
+        hi = f.y;
+    };
+
+    // the step's key (rotated by P) and value: lane l holds RoPE pairs 2l and
+    // 2l + 1, i.e. elements (2l, 2l + 1) and (64 + 2l, 65 + 2l), or (4l .. 4l + 3)
+    // with adjacent pairs; the warp whose keys hold row P appends them
+    const int w_new = (P & (kDecTile - 1)) >> 5;
+    uint32_t kn[2] = {0u, 0u}, vn[2] = {0u, 0u};
+    const int d_a = il ? 4 * lane : 2 * lane, d_b = il ? 4 * lane + 2 : 64 + 2 * lane;
+    if (warp == w_new) {
+        const int64_t src = (tok * a.n_kv_heads + h_idx) * kDecD;
+        const __nv_bfloat16 *kq = static_cast<const __nv_bfloat16 *>(io.kq) + src;
+        const __nv_bfloat16 *vq = static_cast<const __nv_bfloat16 *>(io.vq) + src;
+        kn[0] = *reinterpret_cast<const uint32_t *>(kq + d_a);
+        kn[1] = *reinterpret_cast<const uint32_t *>(kq + d_b);
+        vn[0] = *reinterpret_cast<const uint32_t *>(vq + d_a);
+        vn[1] = *reinterpret_cast<const uint32_t *>(vq + d_b);
+        float x0, x1, y0, y1;
+        unpk(kn[0], x0, x1);
+        unpk(kn[1], y0, y1);
+        const float2 c0 = rope_cs(a.rope, kDecD / 2, P, 2 * lane), c1 = rope_cs(a.rope, kDecD / 2, P, 2 * lane + 1);
+        if (il) {   // pairs (x0, x1) and (y0, y1)
+            rot(x0, x1, c0);
+            rot(y0, y1, c1);
+        } else {    // pairs (x0, y0) and (x1, y1)
+            rot(x0, y0, c0);
+            rot(x1, y1, c1);
+        }
+        kn[0] = pack2(x0, x1);
+        kn[1] = pack2(y0, y1);
+        __nv_bfloat16 *ck = static_cast<__nv_bfloat16 *>(io.cache_k) + (kv_row0 + P) * kDecD;
+        __nv_bfloat16 *cv = static_cast<__nv_bfloat16 *>(io.cache_v) + (kv_row0 + P) * kDecD;
+        *reinterpret_cast<uint32_t *>(ck + d_a) = kn[0];
+        *reinterpret_cast<uint32_t *>(ck + d_b) = kn[1];
+        *reinterpret_cast<uint32_t *>(cv + d_a) = vn[0];
+        *reinterpret_cast<uint32_t *>(cv + d_b) = vn[1];
+    }
+
+    // Q fragments (A operand, 16 x 128, rows >= G zero), rotated by P: rows
+    // lane/4 and lane/4 + 8, elements kb*16 + cq + {0, 1} and + 8 + {0, 1}
+    const __nv_bfloat16 *qp = static_cast<const __nv_bfloat16 *>(a.q) + (tok * a.n_q_heads + h_idx * G) * kDecD;
     const int r0 = lane >> 2, r1 = r0 + 8, cq = (lane & 3) * 2;
     uint32_t qa[8][4];
 #pragma unroll
@@ -218,6 +276,36 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         qa[kb][1] = ld2(r1, c0);
         qa[kb][2] = ld2(r0, c0 + 8);
         qa[kb][3] = ld2(r1, c0 + 8);
+    }
+    if (il) {   // the two elements of each register are a pair
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int d = kb * 16 + cq + ((i & 2) ? 8 : 0);
+                const float2 cs = rope_cs(a.rope, kDecD / 2, P, d >> 1);
+                float x, y;
+                unpk(qa[kb][i], x, y);
+                rot(x, y, cs);
+                qa[kb][i] = pack2(x, y);
+            }
+        }
+    } else {    // element d pairs with d + 64: register i of block kb with that of block kb + 4
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int d = kb * 16 + cq + ((i & 2) ? 8 : 0);
+                const float2 cs0 = rope_cs(a.rope, kDecD / 2, P, d), cs1 = rope_cs(a.rope, kDecD / 2, P, d + 1);
+                float x0, x1, y0, y1;
+                unpk(qa[kb][i], x0, x1);
+                unpk(qa[kb + 4][i], y0, y1);
+                rot(x0, y0, cs0);
+                rot(x1, y1, cs1);
+                qa[kb][i] = pack2(x0, x1);
+                qa[kb + 4][i] = pack2(y0, y1);
+            }
+        }
     }
 
     const float sc = a.scale_log2;
@@ -236,6 +324,28 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         const uint32_t kt = sbase + (uint32_t)(s * kDecStageBytes), vt = kt + kDecTileBytes;
         const int key0 = 32 * warp;   // this warp's 32 keys of the tile
+        if (j == n_t - 1) {
+            // V rows past P are zero; row P is the step's own key and value
+            for (int idx = lane; idx < 32 * 16; idx += 32) {
+                const int row = key0 + (idx >> 4);
+                if (j * kDecTile + row > P) {
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt + sw_off(row, idx & 15)), "r"(0u)
+                                 : "memory");
+                }
+            }
+            if (warp == w_new) {
+                const int row = P & (kDecTile - 1);
+                auto put = [&](uint32_t tile, int d, uint32_t v) {
+                    const uint32_t addr = tile + sw_off(row, d >> 3) + (uint32_t)((d & 7) * 2);
+                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+                };
+                put(kt, d_a, kn[0]);
+                put(kt, d_b, kn[1]);
+                put(vt, d_a, vn[0]);
+                put(vt, d_b, vn[1]);
+            }
+            __syncwarp();
+        }
         // S = Q K^T for 32 keys: four 8-key column blocks
         float c[4][4];
 #pragma unroll
@@ -358,7 +468,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     __syncthreads();
     // thread t: row t / 8 (the G valid rows), columns 16 (t % 8) .. +15
-    const int l_idx = lh / a.n_kv_heads, h_idx = lh - l_idx * a.n_kv_heads;
     for (int rr = threadIdx.x >> 3; rr < G; rr += kDecThreads / 8) {
         float M = -INFINITY;
 #pragma unroll
@@ -394,7 +503,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 bool decode_supported(int dtype, int head_dim, int group) { return dtype == KVR_DTYPE_BF16 && head_dim == kDecD && group <= 16; }
 
 cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const void *tmap_k, const void *tmap_v,
-                                    const void *q_rot, bool pdl, cudaStream_t s)
+                                    const DecodeIO &io, cudaStream_t s)
 {
     const int64_t ctas = (int64_t)a.n_reqs * a.n_layers * a.n_kv_heads;
     if (ctas == 0)
@@ -413,19 +522,9 @@ cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const
         if (dev < 64)
             attr_set[dev] = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = kDecSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_decode_attention, *static_cast<const CUtensorMap *>(tmap_k),
-                              *static_cast<const CUtensorMap *>(tmap_v), a, rt,
-                              static_cast<const __nv_bfloat16 *>(q_rot));
+    k_decode_attention<<<(unsigned)ctas, kDecThreads, kDecSmem, s>>>(*static_cast<const CUtensorMap *>(tmap_k),
+                                                                     *static_cast<const CUtensorMap *>(tmap_v), a, rt, io);
+    return cudaGetLastError();
 }
 
 }  // namespace kvr

@@ -258,13 +258,20 @@ cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt
 // Launched in two-CTA clusters when a.base.n_full < units.
 cudaError_t launch_attention_tc(const TcAttnArgs &a, bool pdl, cudaStream_t s);
 bool attention_tc_supported(int dtype, int head_dim);
-// Attention of a decode step (every request has one query token, or none):
-// one CTA per (request, layer, kv-head) streams the cache block.  Uses the
-// query prologue's rotated heads (q_rot) and the cache tensor maps of the
-// prefill attention.  `pdl`: launched right after the query prologue.
+// A decode step (every request has one query token, or none): one CTA per
+// (request, layer, kv-head) rotates the step's key and query heads, appends
+// the key and value at row P_b and streams the cache block (the cache tensor
+// maps of the prefill attention).  Replaces the query prologue for the step.
+struct DecodeIO {
+    const void *kq;             // [L][T][Hkv][D], not rotated
+    const void *vq;
+    void *cache_k;
+    void *cache_v;
+    int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
+};
 bool decode_supported(int dtype, int head_dim, int group);
 cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const void *tmap_k, const void *tmap_v,
-                                    const void *q_rot, bool pdl, cudaStream_t s);
+                                    const DecodeIO &io, cudaStream_t s);
 // Whether `n_sms` CTAs of the attention kernel (gathering variant or not) can
 // be resident at once as two-CTA clusters.
 bool attention_tc_pairs_fit(int n_sms, bool gather);

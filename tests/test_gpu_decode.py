@@ -19,10 +19,11 @@ pytestmark = pytest.mark.gpu
 STEPS = 3
 
 
-def _run(cfg, reqs, sample_units=None, skip=()):
-    """`skip`: requests that take no token in the decode steps (q_len 0)."""
+def _run(cfg, reqs, sample_units=None, skip=(), il=False):
+    """`skip`: requests that take no token in the decode steps (q_len 0);
+    `il`: a pool with interleaved RoPE pairs."""
     import torch
-    case = Case(cfg, reqs=reqs, spare_rows=STEPS + 2)
+    case = Case(cfg, reqs=reqs, spare_rows=STEPS + 2, rope_interleaved=il)
     case.run(prefill=True)
     L, H, Hq, D = cfg.n_layers, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
     G, lq, B = Hq // H, cfg.query_len, len(case.reqs)
@@ -38,7 +39,7 @@ def _run(cfg, reqs, sample_units=None, skip=()):
         spans = case.spans[b]
         srcs = {int(s): case.source(int(s), units) for s in np.unique(spans[:, 0])}
         if srcs:
-            K, V, pz = oracle.assemble(srcs, spans, cfg.rope_theta)
+            K, V, pz = oracle.assemble(srcs, spans, cfg.rope_theta, interleaved=il)
             K, V = K[0], V[0]
         else:
             K = V = np.zeros((len(units), 0, D))
@@ -49,7 +50,7 @@ def _run(cfg, reqs, sample_units=None, skip=()):
         kqu = np.stack([kq[l, :, h, :] for l, h in zip(li, hi)])
         vqu = np.stack([vq[l, :, h, :] for l, h in zip(li, hi)])
         kc.append(np.concatenate([K, oracle.rope(kqu, (P + np.arange(lq, dtype=np.float64))[None, :],
-                                                  cfg.rope_theta)], axis=1))
+                                                  cfg.rope_theta, il)], axis=1))
         vc.append(np.concatenate([V, vqu], axis=1))
     g = torch.Generator(device=dev)
     g.manual_seed(99)
@@ -74,7 +75,7 @@ def _run(cfg, reqs, sample_units=None, skip=()):
             qu = np.stack([q1n[l, t, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])   # [U, 1, G, D]
             ku = np.stack([k1n[l, t, h][None] for l, h in zip(li, hi)])                    # [U, 1, D]
             vu = np.stack([v1n[l, t, h][None] for l, h in zip(li, hi)])
-            o_ref = oracle.query_attention(kc[b], vc[b], qu, ku, vu, cfg.rope_theta)
+            o_ref = oracle.query_attention(kc[b], vc[b], qu, ku, vu, cfg.rope_theta, interleaved=il)
             o_gpu = np.stack([o1n[l, t, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])
             ok, mx, rel = attn_within_tolerance(o_gpu, o_ref, cfg.dtype)
             assert ok, (step, b, mx, rel)
@@ -82,8 +83,8 @@ def _run(cfg, reqs, sample_units=None, skip=()):
             # the appended row: K rotated at n_b, V copied
             blk_k = to_np64(case.cache_block("k", b)[units])
             blk_v = to_np64(case.cache_block("v", b)[units])
-            k_new = oracle.rope(ku, float(n[b]), cfg.rope_theta)
-            okk, _ = k_within_tolerance(blk_k[:, n[b]:n[b] + 1], k_new, cfg.dtype)
+            k_new = oracle.rope(ku, float(n[b]), cfg.rope_theta, il)
+            okk, _ = k_within_tolerance(blk_k[:, n[b]:n[b] + 1], k_new, cfg.dtype, il)
             assert okk, (step, b)
             assert np.array_equal(blk_v[:, n[b]:n[b] + 1], vu), (step, b)
             kc[b] = np.concatenate([kc[b], k_new], axis=1)
@@ -110,14 +111,14 @@ def test_decode_steps_default_workload_sampled():
     _run(W.CONFIGS[2], None, sample_units=6)
 
 
-@pytest.mark.parametrize("variant", ["g1", "g16", "short_blocks_and_idle_requests"])
+@pytest.mark.parametrize("variant", ["g1", "g16", "short_blocks_and_idle_requests", "interleaved_rope"])
 def test_decode_kernel_edges(variant):
     """The streaming decode kernel: one and sixteen query heads per kv head,
-    cache blocks shorter than one 128-key tile, and requests that take no
-    token in a step (their CTAs leave at once)."""
+    cache blocks shorter than one 128-key tile, requests that take no token
+    in a step (their CTAs leave at once), interleaved RoPE pairs."""
     pid = EDGE.n_chunks
     lists = ([[pid, 0, 5], [0, 0, 96], [2, 10, 60]], [[1, 3, 90], [3, 0, 96]], [])
-    skip = ()
+    skip, il = (), False
     if variant == "g1":
         cfg = dataclasses.replace(EDGE, n_q_heads=2, n_kv_heads=2, query_len=4)
     elif variant == "g16":
@@ -126,5 +127,7 @@ def test_decode_kernel_edges(variant):
         cfg = dataclasses.replace(EDGE, query_len=2)
         lists = ([[pid, 0, 5]], [[0, 10, 40]], [[1, 0, 96], [2, 0, 96]], [])
         skip = (1,)
+    if variant == "interleaved_rope":
+        cfg, il = dataclasses.replace(EDGE, n_q_heads=8, n_kv_heads=2, query_len=5), True
     reqs = [W.Request(np.asarray(r, np.int32).reshape(-1, 3), 0) for r in lists]
-    _run(dataclasses.replace(cfg, batch=len(reqs)), reqs, skip=skip)
+    _run(dataclasses.replace(cfg, batch=len(reqs)), reqs, skip=skip, il=il)
