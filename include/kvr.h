@@ -205,6 +205,16 @@ KVR_API kvr_status kvr_assemble(kvr_pool_t pool, int32_t batch, const int32_t *s
  *   kq, vq        device [n_layers][T][n_kv_heads][head_dim], not rotated
  *   out           device [n_layers][T][n_q_heads][head_dim], pool dtype
  *   softmax_scale 0 means 1/sqrt(head_dim)
+ *
+ * A decode step -- every request with one query token, or none (CoinRAG
+ * blog section 2.3: decoding continues normally on top of the stitched
+ * cache) -- on a bf16 pool with head_dim 128 and at most 16 query heads per
+ * kv head runs as a single kernel that rotates, appends and attends, each
+ * (request, layer, kv-head) block streamed once.  Other calls on the
+ * tensor-core path (bf16, head_dim 128) also write zeros into the V rows
+ * between a block's last query row and the end of its last 128-row key tile
+ * (rows of the block, never past R_b); a decode step leaves those rows as
+ * they are.
  * Errors: KVR_ERR_INVALID_ARG, KVR_ERR_OUT_OF_RANGE, KVR_ERR_UNSUPPORTED,
  * KVR_ERR_CUDA.  A kernel whose bounded wait ran out records
  * KVR_ERR_TIMEOUT, reported by kvr_check.
