@@ -267,11 +267,27 @@ KVR_API int32_t kvr_attention_path(kvr_pool_t pool);
 
 /* Timing hook.  With events non-NULL, later calls on this pool record, on the
  * caller's stream, events[0] / events[1] right before / after the assemble
- * kernel, events[2] / events[3] around the query-append kernel and
+ * kernel, events[2] / events[3] around the query-append kernel (nothing
+ * between them for a decode step, whose one kernel appends) and
  * events[4] / events[5] around the attention kernel.  The handles are
  * cudaEvent_t created by the caller (timing enabled); the array is copied.
  * NULL turns the hook off. */
 KVR_API kvr_status kvr_set_timing_events(kvr_pool_t pool, void *const *events);
+
+/*
+ * kvr_selftest_wait -- exercise the bounded-wait error path.
+ *
+ * Every wait inside the library's kernels gives up after a time limit (2 s),
+ * records KVR_ERR_TIMEOUT in the pool's error word and lets the kernel end,
+ * so that a lost signal is reported by kvr_check rather than hanging the GPU.
+ * This call enqueues, on `stream`, a one-CTA kernel that waits the same way on
+ * a barrier that nothing completes, for limit_ns nanoseconds (1 us .. 2 s;
+ * other values are clamped), and records KVR_ERR_TIMEOUT like the hot path.
+ * The next kvr_check on the pool returns KVR_ERR_TIMEOUT and clears the word;
+ * the pool and the CUDA context stay usable.  For tests of the error path.
+ * Errors: KVR_ERR_INVALID_ARG (NULL pool), KVR_ERR_CUDA.
+ */
+KVR_API kvr_status kvr_selftest_wait(kvr_pool_t pool, uint64_t limit_ns, void *stream);
 
 /*
  * kvr_assemble_noalloc -- kvr_assemble for callers that cannot allocate.

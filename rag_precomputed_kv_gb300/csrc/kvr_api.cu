@@ -1018,6 +1018,21 @@ extern "C" kvr_status kvr_set_timing_events(kvr_pool_t p, void *const *events)
     return KVR_OK;
 }
 
+extern "C" kvr_status kvr_selftest_wait(kvr_pool_t p, uint64_t limit_ns, void *stream)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    kvr_status st;
+    if ((st = ensure_device(p)) != KVR_OK)
+        return st;
+    DeviceGuard g(p->device);
+    const unsigned long long lim = std::min<uint64_t>(std::max<uint64_t>(limit_ns, 1000ull), 2000000000ull);
+    const cudaError_t e = launch_wait_selftest(p->err, lim, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "self-test launch");
+    return KVR_OK;
+}
+
 extern "C" int32_t kvr_attention_path(kvr_pool_t p)
 {
     if (!p)

@@ -270,6 +270,9 @@ struct DecodeIO {
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
 };
 bool decode_supported(int dtype, int head_dim, int group);
+// One CTA whose only wait (bounded by limit_ns) is on a barrier nothing
+// completes: records kDevTimeout in *err when the limit runs out.
+cudaError_t launch_wait_selftest(int *err, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const void *tmap_k, const void *tmap_v,
                                     const DecodeIO &io, cudaStream_t s);
 // Whether `n_sms` CTAs of the attention kernel (gathering variant or not) can

@@ -30,7 +30,7 @@ STATUS = {0: "KVR_OK", 1: "KVR_ERR_INVALID_ARG", 2: "KVR_ERR_OUT_OF_RANGE", 3: "
 
 EXPORTED = ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
             "kvr_prefill", "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
-            "kvr_set_timing_events")
+            "kvr_set_timing_events", "kvr_selftest_wait")
 PATH_UNBOUND, PATH_CUDA_CORES, PATH_TCGEN05 = -1, 0, 1
 
 
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
     lib.kvr_prefill.argtypes = [vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_uint32,
                                 vp, vp, vp, vp, vp, ctypes.c_float, vp]
     lib.kvr_check.argtypes = [vp, vp]
+    lib.kvr_selftest_wait.argtypes = [vp, ctypes.c_uint64, vp]
     lib.kvr_status_string.restype = ctypes.c_char_p
     lib.kvr_status_string.argtypes = [ctypes.c_int]
     lib.kvr_last_error.restype = ctypes.c_char_p
@@ -223,6 +224,12 @@ class Pool:
             return
         arr = (ctypes.c_void_p * 6)(*[int(e.cuda_event) for e in events])
         _raise(load().kvr_set_timing_events(self._h, ctypes.cast(arr, ctypes.c_void_p)))
+
+    def selftest_wait(self, limit_ns: int, stream=None):
+        """Enqueue a kernel whose bounded wait runs out after ``limit_ns``
+        (the library's timeout path); the next :meth:`check` raises
+        KVR_ERR_TIMEOUT."""
+        _raise(load().kvr_selftest_wait(self._h, int(limit_ns), _stream_ptr(stream)))
 
     def check(self, stream=None):
         """kvr_check: synchronize and raise on a device-recorded error."""

@@ -82,6 +82,7 @@ def test_null_arguments(lib):
                                    ctypes.c_float(0), None) == 1
     assert lib.kvr_prefill(None, 1, None, None, None, 0, None, None, None, None, None, None, 0,
                            None, None, None, None, None, ctypes.c_float(0), None) == 1
+    assert lib.kvr_selftest_wait(None, 1000, None) == 1
     assert lib.kvr_pool_unregister(None) == 0
 
 

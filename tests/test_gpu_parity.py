@@ -297,3 +297,18 @@ def test_pool_in_pinned_host_memory():
     with pytest.raises(kvr.KvrError) as e:      # the gathering attention wants device memory
         case.run(prefill=True, skip_prefix=True)
     assert e.value.status == 3
+
+
+def test_bounded_wait_timeout_is_reported_and_the_pool_stays_usable():
+    """A kernel whose wait nothing completes gives up after its limit and
+    records KVR_ERR_TIMEOUT; kvr_check reports it once, and the pool and the
+    context then run the hot path as before."""
+    from rag_precomputed_kv_gb300 import kvr
+    cfg, reqs = _custom(dataclasses.replace(EDGE_BASE, query_len=9), [[[0, 0, 50], [1, 10, 96]], [[2, 0, 30]]])
+    case = Case(cfg, reqs=reqs)
+    case.pool.selftest_wait(20_000_000)   # 20 ms
+    with pytest.raises(kvr.KvrError) as e:
+        case.pool.check()
+    assert e.value.status == 5            # KVR_ERR_TIMEOUT
+    case.pool.check()                     # reported once
+    _ok(run_parity_case(cfg=cfg, case=case, prefill=True))
