@@ -957,6 +957,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 }
                 ++nq;
                 const int s_end = w.b + 1 < a.n_reqs ? reqs[w.b + 1].span0 : g.n_spans;
+                const int prefix = w.rq.prefix;   // per-row reads stay in a register
                 const int64_t lh_row = (int64_t)w.lh * g.entry_len;    // (layer, kv-head) block inside an entry
                 const bool maps = w.lh == 0 && w.row0[0] == 0 && (g.pos_ids || g.src_map);
                 int cur = w.rq.span0;
@@ -979,7 +980,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                             const int rr = j * kTileN + 4 * lane + k;
                             int d = kNoRotation;
                             rows[k] = 0;   // rows past the prefix: any pool row (patched on chip)
-                            if (rr < w.rq.prefix) {
+                            if (rr < prefix) {
                                 while (cur + 1 < s_end && spans[cur].row + spans[cur].len <= rr)
                                     ++cur;
                                 const DevSpan &sp = spans[cur];
@@ -1000,7 +1001,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                         // a group of 8 lanes whose 32 rows are consecutive pool rows takes
                         // one 32-row box load per panel instead of eight gather4s
                         const int last = __shfl_up_sync(0xffffffffu, rows[3], 1);
-                        const bool mine = (j * kTileN + 4 * lane + 3 < w.rq.prefix) && rows[1] == rows[0] + 1 &&
+                        const bool mine = (j * kTileN + 4 * lane + 3 < prefix) && rows[1] == rows[0] + 1 &&
                                           rows[2] == rows[0] + 2 && rows[3] == rows[0] + 3 &&
                                           ((lane & 7) == 0 || rows[0] == last + 1);
                         const unsigned ball = __ballot_sync(0xffffffffu, mine);
@@ -1172,18 +1173,30 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         const __nv_bfloat16 *cv = static_cast<const __nv_bfloat16 *>(a.cache_v);
         int tt = 0;
         bool ok = true;
+        // (cos, sin) of the rotation last used: a span's rows share one delta,
+        // so the tables are read again only where the delta changes
+        int d_cur = kNoRotation;
+        float c[8], sn[8];
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-            const Item itm = item_at(a, reqs, n_blocks, it);
-            const Unit &w = itm.w;
-            for (int j = itm.jb; j < itm.je; ++j, tt += 2) {
+            // the few fields the loop needs, as scalars (the item struct would
+            // otherwise be read from the stack frame on every row)
+            int jb, je, prefix, n_valid;
+            int64_t kv_row0;
+            {
+                const Item itm = item_at(a, reqs, n_blocks, it);
+                jb = itm.jb;
+                je = itm.je;
+                prefix = itm.w.rq.prefix;
+                n_valid = itm.w.n_valid;
+                kv_row0 = itm.w.kv_row0;
+            }
+            for (int j = jb; j < je; ++j, tt += 2) {
                 const int sk = tt % kSlots, sv = (tt + 1) % kSlots;
                 if (!mbar_wait(bar(kBarFull + sk), (tt / kSlots) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 const uint32_t kb = sbase + kOffKV + sk * kTileBytes;
-                int d_cur = kNoRotation;
-                float c[8], sn[8];
                 // four rows at a time: all loads first, then the rotations, then the stores
                 for (int k0 = 0; k0 < kTileN / 8; k0 += 4) {
                     uint4 lo[4], hi[4];
@@ -1193,12 +1206,12 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                         const int r = r0 + 8 * (k0 + q), rr = j * kTileN + r;
                         const uint32_t lo_a = kb + r * 128 + ((p ^ (r & 7)) << 4);
                         dd[q] = kNoRotation;
-                        if (rr < w.rq.prefix) {
+                        if (rr < prefix) {
                             dd[q] = meta[(sk >> 1) * kTileN + r];
                             lo[q] = ld_shared_v4(lo_a);
                             hi[q] = ld_shared_v4(lo_a + kPanelBytes);
-                        } else if (rr < w.n_valid) {
-                            const __nv_bfloat16 *src = ck + (w.kv_row0 + rr) * kD + 8 * p;
+                        } else if (rr < n_valid) {
+                            const __nv_bfloat16 *src = ck + (kv_row0 + rr) * kD + 8 * p;
                             lo[q] = __ldg(reinterpret_cast<const uint4 *>(src));
                             hi[q] = __ldg(reinterpret_cast<const uint4 *>(src + kD / 2));
                         } else {
@@ -1239,14 +1252,14 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                     break;
                 }
                 const uint32_t vb = sbase + kOffKV + sv * kTileBytes;
-                if ((j + 1) * kTileN > w.rq.prefix) {
+                if ((j + 1) * kTileN > prefix) {
                     for (int k = 0; k < kTileN / 8; ++k) {
                         const int r = r0 + 8 * k, rr = j * kTileN + r;
-                        if (rr < w.rq.prefix)
+                        if (rr < prefix)
                             continue;
                         const uint32_t lo_a = vb + r * 128 + ((p ^ (r & 7)) << 4), hi_a = lo_a + kPanelBytes;
-                        if (rr < w.n_valid) {
-                            const __nv_bfloat16 *src = cv + (w.kv_row0 + rr) * kD + 8 * p;
+                        if (rr < n_valid) {
+                            const __nv_bfloat16 *src = cv + (kv_row0 + rr) * kD + 8 * p;
                             const uint4 lo = __ldg(reinterpret_cast<const uint4 *>(src));
                             const uint4 hi = __ldg(reinterpret_cast<const uint4 *>(src + kD / 2));
                             st_shared_v4(lo_a, lo.x, lo.y, lo.z, lo.w);
