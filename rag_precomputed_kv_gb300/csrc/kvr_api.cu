@@ -649,7 +649,8 @@ static kvr_status qa_validate(const kvr_pool &p, int32_t batch, const int64_t *c
         r.prefix = P;
         r.q_off = q_offsets[b];
         r.q_len = Lq;
-        r.m_block0 = pl.m_blocks;
+        r.unit0 = 0;   // set by the schedule (tensor-core path)
+        r.span0 = r.span_end = 0;
         pl.m_blocks += (int32_t)((int64_t(G) * Lq + 255) / 256);
         if (Lq > 0) {
             // the query tokens' keys / values become cache rows P..P+Lq-1;
@@ -712,6 +713,22 @@ static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
         // the previous call's attention must be done with the query scratch
         if (p->q_rot_used && (e = cudaStreamWaitEvent(s, p->q_rot_done, 0)) != cudaSuccess)
             return cuda_fail(e, "query scratch ordering");
+    }
+
+    if (pl.tc) {
+        // schedule: requests with the longest key range first (requests
+        // without query tokens last), each request's units numbered after the
+        // previous one's; the table goes up in this order
+        std::stable_sort(pl.rq.begin(), pl.rq.end(), [](const DevReq &x, const DevReq &y) {
+            if ((x.q_len > 0) != (y.q_len > 0))
+                return x.q_len > 0;
+            return x.prefix + x.q_len > y.prefix + y.q_len;
+        });
+        int64_t u0 = 0;
+        for (DevReq &r : pl.rq) {
+            r.unit0 = (int32_t)u0;
+            u0 += ((int64_t)(Hq / Hkv) * r.q_len + 255) / 256 * LH;
+        }
     }
 
     pl.inl = batch <= kInlineEntries;   // then ap, al have <= batch entries too
@@ -933,8 +950,10 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
             (st = encode_gather_map(*p, p->d.k, &gl.mbk, 32)) != KVR_OK ||
             (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK)
             return st;
-        for (int b = 0; b < batch; ++b)
+        for (int b = 0; b < batch; ++b) {
             qp.rq[b].span0 = ap.span0[b];
+            qp.rq[b].span_end = b + 1 < batch ? ap.span0[b + 1] : (int32_t)ap.ds.size();
+        }
         if ((stitch && (st = asm_stage(p, ap, s)) != KVR_OK) || (st = qa_stage(p, qp, s)) != KVR_OK)
             return st;
         gl.inl = !stitch || ap.inl;

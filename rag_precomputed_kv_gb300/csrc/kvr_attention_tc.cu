@@ -503,15 +503,20 @@ struct Unit {
     int q_row0;         // first row of tile A in the packed rotated Q
 };
 
+// Units are numbered request by request in the table's (schedule) order, and
+// inside a request (layer, kv-head)-major, so that the 256-row blocks of one
+// (layer, kv-head) are neighbours: in the persistent loop they run at the
+// same time on neighbouring SMs and read the same K/V tiles (the second read
+// hits L2).  With the longest requests first, every round of units is of
+// even length and the last, partial round holds the shortest.
 __device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, int n_blocks, int u)
 {
     Unit w;
-    const int mb = u % n_blocks;
-    w.lh = u / n_blocks;
+    (void)n_blocks;
     int lo = 0, hi = a.n_reqs - 1;
-    while (lo < hi) {
+    while (lo < hi) {   // the last request whose first unit is <= u
         const int mid = (lo + hi + 1) >> 1;
-        if (reqs[mid].m_block0 <= mb)
+        if (reqs[mid].unit0 <= u)
             lo = mid;
         else
             hi = mid - 1;
@@ -519,10 +524,14 @@ __device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, i
     w.rq = reqs[lo];
     w.b = lo;
     const int G = a.n_q_heads / a.n_kv_heads;
+    const int nb = (G * w.rq.q_len + 2 * kTileM - 1) / (2 * kTileM);   // 256-row blocks of the request
+    const int local = u - w.rq.unit0;
+    w.lh = local / nb;
+    const int mb = local - w.lh * nb;
     w.l = w.lh / a.n_kv_heads;
     w.h = w.lh - w.l * a.n_kv_heads;
     w.m_rows = G * w.rq.q_len;
-    const int base = (mb - w.rq.m_block0) * 2 * kTileM;
+    const int base = mb * 2 * kTileM;
     w.row0[0] = base;
     w.row0[1] = base + kTileM;
 #pragma unroll
@@ -956,7 +965,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                     break;
                 }
                 ++nq;
-                const int s_end = w.b + 1 < a.n_reqs ? reqs[w.b + 1].span0 : g.n_spans;
+                const int s_end = w.rq.span_end;
                 const int prefix = w.rq.prefix;   // per-row reads stay in a register
                 const int64_t lh_row = (int64_t)w.lh * g.entry_len;    // (layer, kv-head) block inside an entry
                 const bool maps = w.lh == 0 && w.row0[0] == 0 && (g.pos_ids || g.src_map);

@@ -126,16 +126,21 @@ struct alignas(16) DevLocal {
     int64_t len;
 };
 
-// Per-request data for the attention kernels (32 bytes).
+// Per-request data for the attention kernels (48 bytes).  On the tensor-core
+// path the table is in schedule order (longest prefix first) and unit0 is the
+// request's first work unit; elsewhere it is in request order.
 struct alignas(16) DevReq {
     int64_t cache_row0;  // cache_offsets[b] * L * H_kv
     int32_t cap;         // R_b
     int32_t prefix;      // P_b
     int32_t q_off;       // first query token (token axis of q / out)
     int32_t q_len;       // Lq_b
-    int32_t m_block0;    // first 256-row block of this request (tensor-core path)
+    int32_t unit0;       // first (layer, kv-head, 256-row block) unit (tensor-core path)
     int32_t span0;       // first non-empty span of this request (gathering attention)
+    int32_t span_end;    // one past its last
+    int32_t pad_[3];
 };
+static_assert(sizeof(DevReq) == 48, "request table layout");
 
 // Device error word codes (first error wins).
 enum : int { kDevOk = 0, kDevTimeout = 1, kDevBadInput = 2 };
