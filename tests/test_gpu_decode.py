@@ -19,11 +19,13 @@ pytestmark = pytest.mark.gpu
 STEPS = 3
 
 
-def _run(cfg, reqs, sample_units=None, skip=(), il=False):
+def _run(cfg, reqs, sample_units=None, skip=(), il=False, turn=0):
     """`skip`: requests that take no token in the decode steps (q_len 0);
-    `il`: a pool with interleaved RoPE pairs."""
+    `il`: a pool with interleaved RoPE pairs; `turn`: after the decode steps,
+    a further query of that many tokens per request on the same cache (the
+    next turn of a conversation)."""
     import torch
-    case = Case(cfg, reqs=reqs, spare_rows=STEPS + 2, rope_interleaved=il)
+    case = Case(cfg, reqs=reqs, spare_rows=STEPS + 2 + turn, rope_interleaved=il)
     case.run(prefill=True)
     L, H, Hq, D = cfg.n_layers, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
     G, lq, B = Hq // H, cfg.query_len, len(case.reqs)
@@ -89,6 +91,26 @@ def _run(cfg, reqs, sample_units=None, skip=(), il=False):
             assert np.array_equal(blk_v[:, n[b]:n[b] + 1], vu), (step, b)
             kc[b] = np.concatenate([kc[b], k_new], axis=1)
             vc[b] = np.concatenate([vc[b], vu], axis=1)
+    if turn:
+        n = np.array([kc[b].shape[1] for b in range(B)], np.int32)
+        qo2 = (np.arange(B + 1) * turn).astype(np.int32)
+        q2 = torch.randn((L, B * turn, Hq, D), generator=g, device=dev).to(dt)
+        k2 = torch.randn((L, B * turn, H, D), generator=g, device=dev).to(dt)
+        v2 = torch.randn((L, B * turn, H, D), generator=g, device=dev).to(dt)
+        o2 = torch.full_like(q2, float("nan"))
+        case.pool.query_attention(case.cache_offsets, n, qo2, q2, k2, v2, case.cache_k, case.cache_v, o2)
+        torch.cuda.synchronize()
+        case.pool.check()
+        q2n, k2n, v2n, o2n = (to_np64(x) for x in (q2, k2, v2, o2))
+        for b in range(B):
+            sl = slice(b * turn, (b + 1) * turn)
+            qu = np.stack([q2n[l, sl, h * G:(h + 1) * G] for l, h in zip(li, hi)])
+            ku = np.stack([k2n[l, sl, h] for l, h in zip(li, hi)])
+            vu = np.stack([v2n[l, sl, h] for l, h in zip(li, hi)])
+            o_ref = oracle.query_attention(kc[b], vc[b], qu, ku, vu, cfg.rope_theta, interleaved=il)
+            o_gpu = np.stack([o2n[l, sl, h * G:(h + 1) * G] for l, h in zip(li, hi)])
+            ok, mx, rel = attn_within_tolerance(o_gpu, o_ref, cfg.dtype)
+            assert ok, ("turn", b, mx, rel)
     return worst
 
 
@@ -131,3 +153,15 @@ def test_decode_kernel_edges(variant):
         cfg, il = dataclasses.replace(EDGE, n_q_heads=8, n_kv_heads=2, query_len=5), True
     reqs = [W.Request(np.asarray(r, np.int32).reshape(-1, 3), 0) for r in lists]
     _run(dataclasses.replace(cfg, batch=len(reqs)), reqs, skip=skip, il=il)
+
+
+def test_next_turn_after_decode_steps():
+    """Prefill, three decode steps, then a five-token query on the same cache
+    (the next turn): the decode steps leave the V rows past their token as
+    they are, and the query prologue pads them again for the tensor-core
+    attention."""
+    pid = EDGE.n_chunks
+    reqs = [W.Request(np.asarray(r, np.int32).reshape(-1, 3), 0) for r in
+            ([[pid, 0, 5], [0, 0, 96], [2, 10, 60]], [[1, 3, 90]], [[3, 0, 40]])]
+    cfg = dataclasses.replace(EDGE, batch=len(reqs), query_len=9)
+    _run(cfg, reqs, turn=5)
