@@ -57,8 +57,14 @@ namespace kvr {
 namespace {
 
 constexpr int kThreads = 320;           // stitched-cache variant
-constexpr int kThreadsG = 384;          // gathering variant: + 2 rotator warps
-constexpr int kRotThreads = 64;
+// gathering variant: + 4 rotator warps (10-13, one per SM sub-partition) and
+// 2 idle warps completing the fourth warpgroup; launched at 128 registers a
+// thread, the softmax warpgroups take 168 and the other two give up to 88
+// (setmaxnreg): 2 x 128 x 168 + 2 x 128 x 88 = 512 x 128
+constexpr int kThreadsG = 512;
+constexpr int kRotThreads = 128;
+constexpr int kRegsLaunchG = 128, kRegsSoftmaxG = 168, kRegsOtherG = 88;
+static_assert(2 * 128 * kRegsSoftmaxG + 2 * 128 * kRegsOtherG <= kThreadsG * kRegsLaunchG, "register split");
 constexpr int kTileM = 128;      // query rows per tile (two tiles per CTA)
 constexpr int kTileN = 128;      // keys per K/V tile
 constexpr int kD = 128;          // head dim
@@ -623,11 +629,23 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     tc_fence_after();
     cluster_sync();   // the partner CTA's barriers are initialised before any remote arrive
     const uint32_t tmem = *tmem_slot;
+    // gathering variant: each role's branch starts by setting its warp's
+    // register count, for whole warpgroups (0-1: softmax; 2: producer, MMA,
+    // rotators; 3: rotators and the two idle warps)
+    auto regs_softmax = [] {
+        if constexpr (kG)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmaxG));
+    };
+    auto regs_other = [] {
+        if constexpr (kG)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOtherG));
+    };
     // setup above overlaps the previous kernel's tail; its outputs (the
     // stitched cache, the rotated queries) are read only from here on
     pdl_wait_prerequisites();
 
     if (warp < 8) {
+        regs_softmax();
         // =================== softmax / epilogue warpgroup of tile x ===================
         const int x = warp >> 2;
         const int r = threadIdx.x & 127;           // row of the tile = TMEM lane
@@ -872,6 +890,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         if (!ok)
             flag_timeout(a.err, abort_flag);
     } else if (warp == 8) {
+        regs_other();
         if constexpr (!kG) {
             if (lane == 0) {
                 int tt = 0, nq = 0;
@@ -1049,6 +1068,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             }
         }
     } else if (warp == 9) {
+        regs_other();
         // =================== MMA issuer ===================
         {
             const uint32_t lead = elect_one();
@@ -1167,10 +1187,11 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             if (ok && drained && peer_wait >= 0 && lane == 0)
                 mbar_arrive_remote(mapa_rank(bar(kBarPeerFree), (uint32_t)(1 - peer_wait)));
         }
-    } else if constexpr (kG) {
-        // =================== rotator (gathering variant, warps 10-11) ===================
+    } else if (kG && warp < 14) {
+        regs_other();
+        // =================== rotator (gathering variant, warps 10-13) ===================
         // Thread t owns 16-byte chunk p = t % 8 of each row half (elements
-        // [8p, 8p+8) and their RoPE partners [64 + 8p, ...)) in rows t / 8 + 8k.
+        // [8p, 8p+8) and their RoPE partners [64 + 8p, ...)) in rows t / 8 + 16k.
         // Pool rows of a K tile are turned by their span's delta (the same
         // arithmetic as the stitch kernel); rows past the prefix are the query
         // rows (already rotated and appended to the cache by the query
@@ -1207,12 +1228,12 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 }
                 const uint32_t kb = sbase + kOffKV + sk * kTileBytes;
                 // four rows at a time: all loads first, then the rotations, then the stores
-                for (int k0 = 0; k0 < kTileN / 8; k0 += 4) {
+                for (int k0 = 0; k0 < kTileN / 16; k0 += 4) {
                     uint4 lo[4], hi[4];
                     int dd[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int r = r0 + 8 * (k0 + q), rr = j * kTileN + r;
+                        const int r = r0 + 16 * (k0 + q), rr = j * kTileN + r;
                         const uint32_t lo_a = kb + r * 128 + ((p ^ (r & 7)) << 4);
                         dd[q] = kNoRotation;
                         if (rr < prefix) {
@@ -1248,7 +1269,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                     }
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int r = r0 + 8 * (k0 + q);
+                        const int r = r0 + 16 * (k0 + q);
                         const uint32_t lo_a = kb + r * 128 + ((p ^ (r & 7)) << 4);
                         st_shared_v4(lo_a, lo[q].x, lo[q].y, lo[q].z, lo[q].w);
                         st_shared_v4(lo_a + kPanelBytes, hi[q].x, hi[q].y, hi[q].z, hi[q].w);
@@ -1262,8 +1283,8 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 }
                 const uint32_t vb = sbase + kOffKV + sv * kTileBytes;
                 if ((j + 1) * kTileN > prefix) {
-                    for (int k = 0; k < kTileN / 8; ++k) {
-                        const int r = r0 + 8 * k, rr = j * kTileN + r;
+                    for (int k = 0; k < kTileN / 16; ++k) {
+                        const int r = r0 + 16 * k, rr = j * kTileN + r;
                         if (rr < prefix)
                             continue;
                         const uint32_t lo_a = vb + r * 128 + ((p ^ (r & 7)) << 4), hi_a = lo_a + kPanelBytes;
@@ -1285,6 +1306,8 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         }
         if (!ok)
             flag_timeout(a.err, abort_flag);
+    } else {
+        regs_other();   // warps 14-15 of the gathering variant: no role
     }
 
     tc_fence_before();
@@ -1308,6 +1331,15 @@ static cudaError_t set_smem_attr()
     if (e != cudaSuccess)
         return e;
     if (dev >= 64 || !attr_set[dev]) {
+        if constexpr (kG) {
+            // the register split (setmaxnreg) must fit what the CTA is launched
+            // with, or the softmax warpgroups' increase would wait forever
+            cudaFuncAttributes fa{};
+            if ((e = cudaFuncGetAttributes(&fa, k_attention_tc<kG>)) != cudaSuccess)
+                return e;
+            if (fa.numRegs != kRegsLaunchG)
+                return cudaErrorInvalidConfiguration;
+        }
         e = cudaFuncSetAttribute(k_attention_tc<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess)
             return e;
