@@ -59,11 +59,12 @@ namespace {
 constexpr int kThreads = 320;           // stitched-cache variant
 // gathering variant: + 4 rotator warps (10-13, one per SM sub-partition) and
 // 2 idle warps completing the fourth warpgroup; launched at 128 registers a
-// thread, the softmax warpgroups take 168 and the other two give up to 88
-// (setmaxnreg): 2 x 128 x 168 + 2 x 128 x 88 = 512 x 128
+// thread, the softmax warpgroups take 152 and the other two give up to 104
+// (setmaxnreg): 2 x 128 x 152 + 2 x 128 x 104 = 512 x 128 (of the splits
+// measured, 168/88 .. 144/112, the fastest)
 constexpr int kThreadsG = 512;
 constexpr int kRotThreads = 128;
-constexpr int kRegsLaunchG = 128, kRegsSoftmaxG = 168, kRegsOtherG = 88;
+constexpr int kRegsLaunchG = 128, kRegsSoftmaxG = 152, kRegsOtherG = 104;
 static_assert(2 * 128 * kRegsSoftmaxG + 2 * 128 * kRegsOtherG <= kThreadsG * kRegsLaunchG, "register split");
 constexpr int kTileM = 128;      // query rows per tile (two tiles per CTA)
 constexpr int kTileN = 128;      // keys per K/V tile
