@@ -200,10 +200,14 @@ KVR_API kvr_status kvr_assemble(kvr_pool_t pool, int32_t batch, const int32_t *s
  *   prefix_len    host [batch] (P_b, e.g. from kvr_assemble)
  *   q_offsets     host [batch+1]: request b's query tokens are rows
  *                 q_offsets[b] .. q_offsets[b+1]-1 of the token axis
- *   q             device [n_layers][T][n_q_heads][head_dim], T = q_offsets[batch],
+ *   q             [n_layers][T][n_q_heads][head_dim], T = q_offsets[batch],
  *                 not rotated
- *   kq, vq        device [n_layers][T][n_kv_heads][head_dim], not rotated
- *   out           device [n_layers][T][n_q_heads][head_dim], pool dtype
+ *   kq, vq        [n_layers][T][n_kv_heads][head_dim], not rotated
+ *   out           [n_layers][T][n_q_heads][head_dim], pool dtype
+ *                 q, kq, vq and out are device memory or pinned host memory
+ *                 (read, or written, once by the library's kernels through the
+ *                 unified address, over the CPU-GPU link): a host `out` spares
+ *                 the caller a copy back after the call.
  *   softmax_scale 0 means 1/sqrt(head_dim)
  *
  * A decode step -- every request with one query token, or none (CoinRAG

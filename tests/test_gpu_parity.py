@@ -312,3 +312,28 @@ def test_bounded_wait_timeout_is_reported_and_the_pool_stays_usable():
     assert e.value.status == 5            # KVR_ERR_TIMEOUT
     case.pool.check()                     # reported once
     _ok(run_parity_case(cfg=cfg, case=case, prefill=True))
+
+
+def test_query_side_buffers_in_pinned_host_memory():
+    """q, kq, vq and out in pinned host memory (read and written by the
+    kernels through their unified addresses): the same bits as with device
+    buffers, on the tensor-core, decode and CUDA-core paths."""
+    import torch
+    for cfg, reqs in (_custom(dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=13),
+                              [[[0, 3, 90], [2, 0, 96]], [[1, 7, 60]]]),
+                      _custom(dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=1),
+                              [[[0, 3, 90]], [[1, 7, 60], [3, 0, 96]]]),
+                      (W.CONFIGS[1], None)):
+        case = Case(cfg, reqs=reqs)
+        case.run(prefill=True)
+        want_out, want_k = case.out.clone(), case.cache_k.clone()
+        hq, hkq, hvq = (x.cpu().pin_memory() for x in (case.t.q, case.t.kq, case.t.vq))
+        hout = torch.full(case.out.shape, float("nan"), dtype=case.out.dtype, pin_memory=True)
+        case.cache_k.fill_(float("nan"))
+        case.pool.prefill(case.span_offsets, np.concatenate(case.spans), case.cache_offsets, case.cache_k,
+                          case.cache_v, case.q_offsets, hq, hkq, hvq, hout, locals_=case.locals)
+        torch.cuda.synchronize()
+        case.pool.check()
+        bits = (lambda t: t.view(torch.int16)) if case.out.dtype == torch.bfloat16 else (lambda t: t.view(torch.int32))
+        assert torch.equal(bits(hout), bits(want_out.cpu()))
+        assert torch.equal(bits(case.cache_k), bits(want_k))
