@@ -134,9 +134,10 @@ def _span_args(span_offsets, spans, cache_offsets, locals_):
 class Pool:
     """A registered pool of precomputed chunk caches.
 
-    ``k``, ``v``: device tensors ``[entries, layers, kv_heads, entry_len, head_dim]``
-    (any strides with head_dim contiguous), keys rotated at entry-local
-    positions (or, with ``keys_unrotated``, before RoPE).  ``rope_interleaved``:
+    ``k``, ``v``: tensors ``[entries, layers, kv_heads, entry_len, head_dim]`` in
+    device memory or pinned host memory (any strides with head_dim contiguous),
+    keys rotated at entry-local positions (or, with ``keys_unrotated``, before
+    RoPE).  ``rope_interleaved``:
     RoPE pairs are (x_2i, x_2i+1) instead of (x_i, x_i+D/2), for the stored
     keys and every rotation the library makes.  The tensors must outlive the
     pool.
@@ -205,7 +206,9 @@ class Pool:
 
     def query_attention(self, cache_offsets, prefix_len, q_offsets, q, kq, vq, cache_k, cache_v,
                         out, softmax_scale: float = 0.0, stream=None):
-        """kvr_query_attention (appends the query K/V to the cache, writes out)."""
+        """kvr_query_attention (appends the query K/V to the cache, writes out).
+        ``q``, ``kq``, ``vq`` and ``out`` may be device or pinned host tensors;
+        with one token per request the call is a decode step (one kernel)."""
         co, pl, qo = _i64(cache_offsets), _i32(prefix_len), _i32(q_offsets)
         _raise(load().kvr_query_attention(self._h, len(qo) - 1, _np_ptr(co), _np_ptr(pl), _np_ptr(qo),
                                           _ptr(q), _ptr(kq), _ptr(vq), _ptr(cache_k), _ptr(cache_v),
