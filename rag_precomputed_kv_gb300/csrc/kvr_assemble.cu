@@ -161,7 +161,9 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
     T *cv = static_cast<T *>(a.cache_v);
 
     const int LH = a.n_layers * a.n_heads;
-    const int u0 = blockIdx.y * a.upc;
+    // last (layer, kv-head) groups first: what the kernel writes last stays in
+    // L2, and the attention kernel that follows starts on the first groups
+    const int u0 = (gridDim.y - 1 - blockIdx.y) * a.upc;
     const int nu = min(a.upc, LH - u0);
     const int total = nu * sp.len;
 
