@@ -9,9 +9,10 @@ kvr_query_attention (query RoPE + K/V append + tcgen05 prefill attention).
 The default workload is the full-chunk-reuse configuration (Qwen2-7B shape,
 five 512-token chunks after a 32-token system prompt, 64 query tokens,
 batch 1).  Prints ONE JSON line (rank 0).  Timing: CUDA events on the
-launching stream around every step, L2 flushed (256 MiB write) between steps
-outside the events, a barrier and synchronize on both sides of the timed
-region, max over ranks.  Each rank runs its own replica of the batch (the
+launching stream around every step, L2 flushed between steps outside the
+events (256 MiB written, then 256 MiB of another buffer read, so that no step
+pays for the flush's own dirty lines), a barrier and synchronize on both
+sides of the timed region, max over ranks.  Each rank runs its own replica of the batch (the
 path shards by request with no exchange), so scaling is weak.
 """
 from __future__ import annotations
@@ -206,6 +207,23 @@ def job_throughput(units_per_rank: float, seconds: float, world: int) -> float:
     return units_per_rank * world / max_over_ranks(seconds, world)
 
 
+class L2Flush:
+    """Empties the L2 of everything a step could reuse: writes a buffer twice
+    the L2's size, then reads another one, so that the write's dirty lines are
+    written back here and not during the next timed step."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.amax(self.r, dim=0, out=self.sink)
+
+
 def run_kvr(args):
     import torch
     world, rank, local = dist_setup()
@@ -213,12 +231,12 @@ def run_kvr(args):
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.config]
     wl = Workload(cfg, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     from rag_precomputed_kv_gb300 import kvr as K
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         wl.step()
     torch.cuda.synchronize()
     wl.pool.check()
@@ -235,7 +253,7 @@ def run_kvr(args):
     torch.cuda.synchronize()
     host = 0.0
     for k in range(args.steps):
-        flush.zero_()
+        flush()
         h0 = time.perf_counter()
         e0[k].record(stream)
         wl.step()
@@ -256,7 +274,7 @@ def run_kvr(args):
         e.record(stream)
     torch.cuda.synchronize()
     for k in range(n_kt):
-        flush.zero_()
+        flush()
         wl.pool.set_timing_events(ev[k])
         wl.step()
     torch.cuda.synchronize()
@@ -276,11 +294,11 @@ def run_kvr(args):
         g0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_g)]
         g1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_g)]
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             wl.step(skip_prefix_cache=True)
         torch.cuda.synchronize()
         for k in range(n_g):
-            flush.zero_()
+            flush()
             g0[k].record(stream)
             wl.step(skip_prefix_cache=True)
             g1[k].record(stream)
@@ -309,11 +327,11 @@ def run_kvr(args):
     d1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_d)]
     wl.step()
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         wl.pool.query_attention(wl.cache_offsets, n_dec, q1_off, q1, k1, v1, wl.cache_k, wl.cache_v, o1)
     torch.cuda.synchronize()
     for k in range(n_d):
-        flush.zero_()
+        flush()
         d0[k].record(stream)
         wl.pool.query_attention(wl.cache_offsets, n_dec, q1_off, q1, k1, v1, wl.cache_k, wl.cache_v, o1)
         d1[k].record(stream)
@@ -341,7 +359,7 @@ def run_kvr(args):
         h0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
         h1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
         for k in range(args.warmup + n_h):
-            flush.zero_()
+            flush()
             if k >= args.warmup:
                 h0[k - args.warmup].record(stream)
             hp.assemble(wl.span_offsets, wl.spans, wl.cache_offsets, wl.cache_k, wl.cache_v,
@@ -389,7 +407,7 @@ def run_kvr(args):
                                 wl.cache_v, out_h)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         e2e_step()
     torch.cuda.synchronize()
     f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -397,7 +415,7 @@ def run_kvr(args):
     barrier(world)
     torch.cuda.synchronize()
     for k in range(args.steps):
-        flush.zero_()
+        flush()
         f0[k].record(stream)
         e2e_step()
         f1[k].record(stream)
@@ -437,7 +455,8 @@ def run_kvr(args):
                    "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
                    "chunk_len": cfg.chunk_len, "pool_entries": cfg.pool_entries,
                    "stitched_tokens_per_step": tokens_per_step, "query_tokens_per_request": cfg.query_len,
-                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "l2": "flushed between steps outside the timed events: 256 MiB written, then 256 MiB "
+                         "of another buffer read (the L2 holds no line of the step's data, and none dirty)",
                    "parallelism": f"request replicas x{world}"},
         "roofline": dominant, "roofline_other": other,
         "assemble_gbs": round(asm_gbs, 1), "attention_tflops": round(att_tf, 2),
