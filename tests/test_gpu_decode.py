@@ -155,6 +155,19 @@ def test_decode_kernel_edges(variant):
     _run(dataclasses.replace(cfg, batch=len(reqs)), reqs, skip=skip, il=il)
 
 
+def test_decode_mixed_block_lengths():
+    """One step over blocks of very different lengths: a long request (ten
+    128-key tiles, its last one partial), a request of one partial tile, a
+    request that takes no token, and seven query heads per kv head (the
+    Qwen2-7B grouping, padded to sixteen MMA rows)."""
+    pid = EDGE.n_chunks
+    long_req = [[pid, 0, 5]] + [[c % 4, 0, 96] for c in range(12)]
+    lists = (long_req, [[1, 3, 40]], [[2, 0, 96], [3, 10, 90]])
+    reqs = [W.Request(np.asarray(r, np.int32).reshape(-1, 3), 0) for r in lists]
+    cfg = dataclasses.replace(EDGE, n_q_heads=14, n_kv_heads=2, query_len=3, batch=len(reqs))
+    _run(cfg, reqs, skip=(2,))
+
+
 def test_next_turn_after_decode_steps():
     """Prefill, three decode steps, then a five-token query on the same cache
     (the next turn): the decode steps leave the V rows past their token as
