@@ -50,6 +50,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "kvr_internal.cuh"
 
 namespace kvr {
@@ -1325,13 +1327,14 @@ bool attention_tc_supported(int dtype, int head_dim) { return dtype == KVR_DTYPE
 template <bool kG>
 static cudaError_t set_smem_attr()
 {
-    // the shared-memory opt-in is per device and per kernel
-    static bool attr_set[64] = {};
+    // the shared-memory opt-in is per device and per kernel (callers on
+    // several host threads may both set it: the same value)
+    static std::atomic<bool> attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev >= 64 || !attr_set[dev]) {
+    if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
         if constexpr (kG) {
             // the register split (setmaxnreg) must fit what the CTA is launched
             // with, or the softmax warpgroups' increase would wait forever
@@ -1345,7 +1348,7 @@ static cudaError_t set_smem_attr()
         if (e != cudaSuccess)
             return e;
         if (dev < 64)
-            attr_set[dev] = true;
+            attr_set[dev].store(true, std::memory_order_release);
     }
     return cudaSuccess;
 }
@@ -1353,11 +1356,11 @@ static cudaError_t set_smem_attr()
 template <bool kG>
 static bool pairs_fit(int n_sms)
 {
-    static int fit[64] = {};   // 0 unknown, 1 yes, 2 no
+    static std::atomic<int> fit[64] = {};   // 0 unknown, 1 yes, 2 no
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || (n_sms & 1))
         return false;
-    if (fit[dev] == 0) {
+    if (fit[dev].load(std::memory_order_acquire) == 0) {
         if (set_smem_attr<kG>() != cudaSuccess) {
             cudaGetLastError();
             return false;
@@ -1377,9 +1380,9 @@ static bool pairs_fit(int n_sms)
         const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_attention_tc<kG>, &cfg);
         if (e != cudaSuccess)
             cudaGetLastError();
-        fit[dev] = (e == cudaSuccess && 2 * n >= n_sms) ? 1 : 2;
+        fit[dev].store((e == cudaSuccess && 2 * n >= n_sms) ? 1 : 2, std::memory_order_release);
     }
-    return fit[dev] == 1;
+    return fit[dev].load(std::memory_order_acquire) == 1;
 }
 
 bool attention_tc_pairs_fit(int n_sms, bool gather) { return gather ? pairs_fit<true>(n_sms) : pairs_fit<false>(n_sms); }

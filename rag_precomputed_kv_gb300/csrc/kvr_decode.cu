@@ -30,6 +30,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "kvr_internal.cuh"
 
 namespace kvr {
@@ -510,17 +512,17 @@ cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const
         return cudaSuccess;
     if (ctas > 0x7fffffff)
         return cudaErrorInvalidValue;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};   // per device (host threads may race: same value)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev >= 64 || !attr_set[dev]) {
+    if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(k_decode_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
         if (e != cudaSuccess)
             return e;
         if (dev < 64)
-            attr_set[dev] = true;
+            attr_set[dev].store(true, std::memory_order_release);
     }
     k_decode_attention<<<(unsigned)ctas, kDecThreads, kDecSmem, s>>>(*static_cast<const CUtensorMap *>(tmap_k),
                                                                      *static_cast<const CUtensorMap *>(tmap_v), a, rt, io);

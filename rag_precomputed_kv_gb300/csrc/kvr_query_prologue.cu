@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "kvr_internal.cuh"
 
@@ -135,19 +136,19 @@ cudaError_t launch_query_prologue(const QueryPrologueArgs &a, const ReqTable &rt
     if (n_items == 0)
         return cudaSuccess;
     // one wave: the resident CTAs per SM (registers decide) times the SMs
-    static int per_sm[64] = {};
+    static std::atomic<int> per_sm[64] = {};   // per device (host threads may race: same value)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    int occ = dev < 64 ? per_sm[dev] : 0;
+    int occ = dev < 64 ? per_sm[dev].load(std::memory_order_relaxed) : 0;
     if (occ == 0) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_query_prologue, kQpThreads, 0);
         if (e != cudaSuccess)
             return e;
         occ = std::max(occ, 1);
         if (dev < 64)
-            per_sm[dev] = occ;
+            per_sm[dev].store(occ, std::memory_order_relaxed);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)std::min<int64_t>(n_items, (int64_t)n_sms * occ));
