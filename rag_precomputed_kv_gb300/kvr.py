@@ -30,7 +30,7 @@ STATUS = {0: "KVR_OK", 1: "KVR_ERR_INVALID_ARG", 2: "KVR_ERR_OUT_OF_RANGE", 3: "
 
 EXPORTED = ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
             "kvr_prefill", "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
-            "kvr_set_timing_events", "kvr_selftest_wait")
+            "kvr_set_timing_events", "kvr_selftest_wait", "kvr_assemble_noalloc")
 PATH_UNBOUND, PATH_CUDA_CORES, PATH_TCGEN05 = -1, 0, 1
 
 
@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
     lib.kvr_prefill.argtypes = [vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, ctypes.c_uint32,
                                 vp, vp, vp, vp, vp, ctypes.c_float, vp]
     lib.kvr_check.argtypes = [vp, vp]
+    lib.kvr_assemble_noalloc.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, vp, vp, i32, vp, vp, vp, vp, vp,
+                                         vp, ctypes.c_uint32, vp]
     lib.kvr_selftest_wait.argtypes = [vp, ctypes.c_uint64, vp]
     lib.kvr_status_string.restype = ctypes.c_char_p
     lib.kvr_status_string.argtypes = [ctypes.c_int]
@@ -85,8 +87,8 @@ def load(path: str = LIB_PATH):
     lib.kvr_set_timing_events.restype = ctypes.c_int
     lib.kvr_attention_path.argtypes = [vp]
     lib.kvr_attention_path.restype = ctypes.c_int32
-    for name in ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble",
-                 "kvr_query_attention", "kvr_prefill", "kvr_check"):
+    for name in ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
+                 "kvr_prefill", "kvr_check", "kvr_selftest_wait", "kvr_assemble_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -131,6 +133,40 @@ def _span_args(span_offsets, spans, cache_offsets, locals_):
     return so, sp, co, loc, len(so) - 1
 
 
+def _pool_desc(k, v, n_q_heads: int, rope_theta: float, keys_unrotated: bool, rope_interleaved: bool):
+    import torch
+    assert k.shape == v.shape and k.stride() == v.stride() and k.dtype == v.dtype
+    assert k.stride(-1) == 1
+    dt = {torch.bfloat16: KVR_DTYPE_BF16, torch.float32: KVR_DTYPE_FP32}[k.dtype]
+    E, L, H, T, D = k.shape
+    flags = ((KVR_POOL_KEYS_UNROTATED if keys_unrotated else 0)
+             | (KVR_POOL_ROPE_INTERLEAVED if rope_interleaved else 0))
+    return PoolDesc(L, n_q_heads, H, D, dt, flags, E, T, _ptr(k), _ptr(v),
+                    (ctypes.c_int64 * 4)(*k.stride()[:4]), float(rope_theta))
+
+
+def assemble_noalloc(k, v, n_q_heads: int, rope_theta: float, span_offsets: Sequence[int], spans,
+                     cache_offsets, cache_k, cache_v, locals_=(), pos_ids=None, src_map=None,
+                     composite: bool = False, keys_unrotated: bool = False,
+                     rope_interleaved: bool = False, stream=None) -> np.ndarray:
+    """kvr_assemble_noalloc: kvr_assemble for callers that cannot allocate.
+
+    No pool handle: the pool tensors ``k``, ``v`` are described as for
+    :class:`Pool` on every call.  Returns the per-request prefix lengths
+    (numpy int32).  The library's fixed scratch is shared by all such calls
+    (see the header for its limits and its one-call-at-a-time rule).
+    """
+    d = _pool_desc(k, v, n_q_heads, rope_theta, keys_unrotated, rope_interleaved)
+    so, sp, co, loc, batch = _span_args(span_offsets, spans, cache_offsets, locals_)
+    plen = np.zeros(max(batch, 1), np.int32)
+    _raise(load().kvr_assemble_noalloc(ctypes.byref(d), batch, _np_ptr(so), _np_ptr(sp) if sp.size else None,
+                                       ctypes.cast(loc, ctypes.c_void_p) if len(locals_) else None,
+                                       len(locals_), _np_ptr(co), _ptr(cache_k), _ptr(cache_v),
+                                       _ptr(pos_ids), _ptr(src_map), _np_ptr(plen),
+                                       KVR_POSITIONS_COMPOSITE if composite else 0, _stream_ptr(stream)))
+    return plen[:batch]
+
+
 class Pool:
     """A registered pool of precomputed chunk caches.
 
@@ -145,17 +181,9 @@ class Pool:
 
     def __init__(self, k, v, n_q_heads: int, rope_theta: float, keys_unrotated: bool = False,
                  rope_interleaved: bool = False):
-        import torch
         lib = load()
-        assert k.shape == v.shape and k.stride() == v.stride() and k.dtype == v.dtype
-        assert k.stride(-1) == 1
-        dt = {torch.bfloat16: KVR_DTYPE_BF16, torch.float32: KVR_DTYPE_FP32}[k.dtype]
-        E, L, H, T, D = k.shape
-        flags = ((KVR_POOL_KEYS_UNROTATED if keys_unrotated else 0)
-                 | (KVR_POOL_ROPE_INTERLEAVED if rope_interleaved else 0))
-        d = PoolDesc(L, n_q_heads, H, D, dt, flags, E, T,
-                     _ptr(k), _ptr(v),
-                     (ctypes.c_int64 * 4)(*k.stride()[:4]), float(rope_theta))
+        d = _pool_desc(k, v, n_q_heads, rope_theta, keys_unrotated, rope_interleaved)
+        _, L, H, _, D = k.shape
         h = ctypes.c_void_p()
         _raise(lib.kvr_pool_register(ctypes.byref(d), ctypes.byref(h)))
         self._h = h

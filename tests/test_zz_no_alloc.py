@@ -4,14 +4,14 @@ Some callers cannot call cudaMalloc where they stitch a prefix (an engine
 whose caching allocator already owns the free device memory, a request loop
 that forbids allocations, a plug-in restricted to its host's allocator).
 kvr_assemble_noalloc serves them with scratch in a fixed __device__ array.
-These tests call it through the C ABI and check that two calls in a row give
-exactly what kvr_assemble gives (stitched K and V, position ids, source map,
-prefix lengths), and that it refuses work beyond its fixed limits.
+These tests call it through the binding (argument marshalling over the C
+ABI) and check that two calls in a row give exactly what kvr_assemble gives
+(stitched K and V, position ids, source map, prefix lengths), and that it
+refuses work beyond its fixed limits.
 
 This file is collected last on purpose: it runs after every other test, and
 also passes alone in a fresh process.
 """
-import ctypes
 import dataclasses
 
 import numpy as np
@@ -25,33 +25,12 @@ from rag_precomputed_kv_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _entry():
-    lib = kvr.load()
-    fn = lib.kvr_assemble_noalloc
-    vp = ctypes.c_void_p
-    fn.argtypes = [vp, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp,
-                   ctypes.c_uint32, vp]
-    fn.restype = ctypes.c_int
-    return fn
-
-
-def _desc(case):
-    k, v = case.t.pool_k, case.t.pool_v
-    E, L, H, T, D = k.shape
-    dt = kvr.KVR_DTYPE_BF16 if k.dtype == torch.bfloat16 else kvr.KVR_DTYPE_FP32
-    return kvr.PoolDesc(L, case.cfg.n_q_heads, H, D, dt, 0, E, T, k.data_ptr(), v.data_ptr(),
-                        (ctypes.c_int64 * 4)(*k.stride()[:4]), float(case.cfg.rope_theta))
-
-
-def _call(fn, case, desc, spans, span_offsets, ck, cv, pos, src, plen):
-    loc = (kvr.LocalSrc * max(1, len(case.locals)))()
-    for i, (lk, lv) in enumerate(case.locals):
-        loc[i] = kvr.LocalSrc(lk.data_ptr(), lv.data_ptr(), lk.shape[2], (ctypes.c_int64 * 3)(*lk.stride()[:3]))
-    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
-    return fn(ctypes.byref(desc), len(span_offsets) - 1, p(span_offsets), p(spans),
-              ctypes.cast(loc, ctypes.c_void_p) if case.locals else None, len(case.locals),
-              p(case.cache_offsets), ck.data_ptr(), cv.data_ptr(), pos.data_ptr(), src.data_ptr(),
-              p(plen), 0, torch.cuda.current_stream().cuda_stream)
+def _call(case, spans, span_offsets, ck, cv, pos, src, cache_offsets=None):
+    """kvr_assemble_noalloc through the binding (the pool described on each call)."""
+    return kvr.assemble_noalloc(case.t.pool_k, case.t.pool_v, case.cfg.n_q_heads, case.cfg.rope_theta,
+                                span_offsets, spans,
+                                case.cache_offsets if cache_offsets is None else cache_offsets, ck, cv,
+                                locals_=case.locals, pos_ids=pos, src_map=src)
 
 
 def _bits(t):
@@ -62,20 +41,16 @@ def _bits(t):
                                  dataclasses.replace(W.CONFIGS[4], batch=1, n_layers=2, n_chunks=16)],
                          ids=["tiny-fp32", "nuggets-b4", "docs-inline-2-layers"])
 def test_noalloc_matches_assemble_on_two_calls(cfg):
-    fn = _entry()
     case = Case(cfg, prerotate=False)
     case.run(attention=False)                       # kvr_assemble, the existing entry point
     ref = [case.cache_k.clone(), case.cache_v.clone(), case.pos_ids.clone(), case.src_map.clone()]
     spans = np.ascontiguousarray(np.concatenate(case.spans), np.int32)
-    desc = _desc(case)
     for call in range(2):
         ck = torch.full_like(case.cache_k, float("nan"))
         cv = torch.full_like(case.cache_v, float("nan"))
         pos = torch.full_like(case.pos_ids, -1)
         src = torch.full_like(case.src_map, -1)
-        plen = np.zeros(len(case.reqs), np.int32)
-        st = _call(fn, case, desc, spans, case.span_offsets, ck, cv, pos, src, plen)
-        assert st == 0, f"call {call}: status {st}"
+        plen = _call(case, spans, case.span_offsets, ck, cv, pos, src)
         torch.cuda.synchronize()
         assert np.array_equal(plen, case.prefix), call
         assert torch.equal(_bits(ck), _bits(ref[0])), f"call {call}: K differs"
@@ -84,19 +59,14 @@ def test_noalloc_matches_assemble_on_two_calls(cfg):
 
 
 def test_noalloc_rejects_work_beyond_its_limits():
-    fn = _entry()
     case = Case(W.CONFIGS[1], prerotate=False)
-    desc = _desc(case)
     n = 4097                                        # one span more than the scratch holds
     spans = np.tile(np.array([[0, 0, 1]], np.int32), (n, 1))
     so = np.array([0, n], np.int32)
     co = np.array([0, n + 16], np.int64)
-    saved = case.cache_offsets
-    case.cache_offsets = co
     ck = torch.empty((int(co[-1]) * case.LH, case.cfg.head_dim), dtype=case.cache_k.dtype, device="cuda")
     pos = torch.empty(n, dtype=torch.int32, device="cuda")
     src = torch.empty((n, 2), dtype=torch.int32, device="cuda")
-    plen = np.zeros(1, np.int32)
-    st = _call(fn, case, desc, spans, so, ck, ck, pos, src, plen)
-    case.cache_offsets = saved
-    assert st == 1                                  # KVR_ERR_INVALID_ARG, before any GPU work
+    with pytest.raises(kvr.KvrError) as ei:
+        _call(case, spans, so, ck, ck, pos, src, cache_offsets=co)
+    assert ei.value.status == 1                     # KVR_ERR_INVALID_ARG, before any GPU work
