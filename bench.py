@@ -125,10 +125,17 @@ class ClockSampler:
 class Workload:
     """A batch of requests with its pool, cache and query tensors on one GPU."""
 
-    def __init__(self, cfg: W.Config, device):
+    def __init__(self, cfg: W.Config, device, variant: str = "default"):
+        """``variant``: the position / RoPE layout of the pool: "interleaved"
+        RoPE pairs, keys "unrotated" (kept before RoPE, rotated at their
+        stitched positions), or "composite" positions (the chunk-local ids
+        kept, delta 0).  The N(0,1) keys stand for any of them: a rotated
+        isotropic Gaussian pair is again one."""
         import torch
         from rag_precomputed_kv_gb300 import kvr
         self.cfg = cfg
+        self.variant = variant
+        self.composite = variant == "composite"
         self.reqs = W.draw_spans(cfg)
         self.t = W.make_tensors(cfg, self.reqs, device=device)
         self.locals = [(k, v) for k, v in zip(self.t.local_k, self.t.local_v) if k is not None]
@@ -154,7 +161,8 @@ class Workload:
         self.cache_k = torch.empty((rows, cfg.head_dim), dtype=self.t.pool_k.dtype, device=device)
         self.cache_v = torch.empty_like(self.cache_k)
         self.out = torch.empty_like(self.t.q)
-        self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta)
+        self.pool = kvr.Pool(self.t.pool_k, self.t.pool_v, cfg.n_q_heads, cfg.rope_theta,
+                             keys_unrotated=variant == "unrotated", rope_interleaved=variant == "interleaved")
         self.plen = self.prefix.astype(np.int32)
 
     def step(self, q=None, kq=None, vq=None, out=None, skip_prefix_cache=False):
@@ -163,7 +171,7 @@ class Workload:
                           self.cache_v, self.q_offsets, self.t.q if q is None else q,
                           self.t.kq if kq is None else kq, self.t.vq if vq is None else vq,
                           self.out if out is None else out, locals_=self.locals,
-                          skip_prefix_cache=skip_prefix_cache)
+                          composite=self.composite, skip_prefix_cache=skip_prefix_cache)
 
 
 def dist_setup():
@@ -230,7 +238,7 @@ def run_kvr(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.config]
-    wl = Workload(cfg, dev)
+    wl = Workload(cfg, dev, args.variant)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     from rag_precomputed_kv_gb300 import kvr as K
@@ -354,7 +362,8 @@ def run_kvr(args):
     except RuntimeError:
         hk = hv = None
     if hk is not None:
-        hp = K.Pool(hk, hv, cfg.n_q_heads, cfg.rope_theta)
+        hp = K.Pool(hk, hv, cfg.n_q_heads, cfg.rope_theta, keys_unrotated=wl.variant == "unrotated",
+                    rope_interleaved=wl.variant == "interleaved")
         n_h = min(args.steps, 200)
         h0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
         h1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
@@ -363,7 +372,7 @@ def run_kvr(args):
             if k >= args.warmup:
                 h0[k - args.warmup].record(stream)
             hp.assemble(wl.span_offsets, wl.spans, wl.cache_offsets, wl.cache_k, wl.cache_v,
-                        locals_=wl.locals)
+                        locals_=wl.locals, composite=wl.composite)
             if k >= args.warmup:
                 h1[k - args.warmup].record(stream)
         torch.cuda.synchronize()
@@ -401,7 +410,7 @@ def run_kvr(args):
             kq_d.copy_(kq_h, non_blocking=True)
             vq_d.copy_(vq_h, non_blocking=True)
         plen = wl.pool.assemble(wl.span_offsets, wl.spans, wl.cache_offsets, wl.cache_k, wl.cache_v,
-                                locals_=wl.locals)
+                                locals_=wl.locals, composite=wl.composite)
         stream.wait_stream(copy_s)
         wl.pool.query_attention(wl.cache_offsets, plen, wl.q_offsets, q_d, kq_d, vq_d, wl.cache_k,
                                 wl.cache_v, out_h)
@@ -457,7 +466,7 @@ def run_kvr(args):
                    "stitched_tokens_per_step": tokens_per_step, "query_tokens_per_request": cfg.query_len,
                    "l2": "flushed between steps outside the timed events: 256 MiB written, then 256 MiB "
                          "of another buffer read (the L2 holds no line of the step's data, and none dirty)",
-                   "parallelism": f"request replicas x{world}"},
+                   "parallelism": f"request replicas x{world}", "variant": args.variant},
         "roofline": dominant, "roofline_other": other,
         "assemble_gbs": round(asm_gbs, 1), "attention_tflops": round(att_tf, 2),
         "append_ms": round(app_mean, 5),
@@ -478,7 +487,7 @@ def run_kvr(args):
         "host_pool": host_pool,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.variant == "default":
         res["cpu_baseline"] = oracle_baseline(cfg, wl, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -643,6 +652,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="seconds of oracle work for the whole reference-arm run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", default="default", choices=["default", "interleaved", "unrotated", "composite"],
+                    help="pool RoPE layout / positions (the oracle baseline is timed for the default only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -31,13 +31,18 @@ __device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddep
 
 // (cos, sin) of pos * w_i for |pos| < 2^24 from the two table halves (angle
 // addition, one complex product in float); a negative pos is the conjugate.
+// Below 2^12 the high half's entry is row 0, exactly (1, 0): the product is
+// the low entry itself, bit for bit, and only that one is read.
 __device__ __forceinline__ float2 rope_cs(const float2 *__restrict__ tab, int half, int pos, int i)
 {
     const int a = pos < 0 ? -pos : pos;
-    const float2 h = __ldg(tab + (a >> 12) * half + i);
     const float2 l = __ldg(tab + (kRopeSplit + (a & (kRopeSplit - 1))) * half + i);
-    const float c = fmaf(h.x, l.x, -h.y * l.y);
-    const float s = fmaf(h.y, l.x, h.x * l.y);
+    float c = l.x, s = l.y;
+    if (a >= kRopeSplit) {
+        const float2 h = __ldg(tab + (a >> 12) * half + i);
+        c = fmaf(h.x, l.x, -h.y * l.y);
+        s = fmaf(h.y, l.x, h.x * l.y);
+    }
     return make_float2(c, pos < 0 ? -s : s);
 }
 
