@@ -36,6 +36,7 @@ from rag_precomputed_kv_gb300 import workloads as W  # noqa: E402
 METRIC = "stitched KV tokens/s & HBM GB/s; query-attn TFLOP/s; per-request latency"
 UNIT = "stitched tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+HOST_POOL_MAX_BYTES = 8 << 30   # the pinned-host-pool leg copies the pool (K and V) to the host
 
 
 def peaks():
@@ -357,10 +358,16 @@ def run_kvr(args):
     # ---- the stitch from a pool kept in pinned host memory (read over the
     # CPU-GPU link through its unified address) ----
     host_pool = None
-    try:
-        hk, hv = wl.t.pool_k.cpu().pin_memory(), wl.t.pool_v.cpu().pin_memory()
-    except RuntimeError:
-        hk = hv = None
+    hk = hv = None
+    pool_bytes = 2 * wl.t.pool_k.numel() * wl.t.pool_k.element_size()
+    if pool_bytes > HOST_POOL_MAX_BYTES:
+        host_pool = {"skipped": f"pool of {pool_bytes / 2**30:.1f} GiB: not copied to pinned host memory "
+                                f"(limit {HOST_POOL_MAX_BYTES / 2**30:.0f} GiB)"}
+    else:
+        try:
+            hk, hv = wl.t.pool_k.cpu().pin_memory(), wl.t.pool_v.cpu().pin_memory()
+        except RuntimeError:
+            hk = hv = None
     if hk is not None:
         hp = K.Pool(hk, hv, cfg.n_q_heads, cfg.rope_theta, keys_unrotated=wl.variant == "unrotated",
                     rope_interleaved=wl.variant == "interleaved")
