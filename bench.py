@@ -233,12 +233,24 @@ class L2Flush:
         torch.amax(self.r, dim=0, out=self.sink)
 
 
+def workload_config(args) -> W.Config:
+    """The configuration, with --layers / --batch (smaller cases of a workload
+    for profiling) applied; the bench line's config shows them."""
+    import dataclasses
+    cfg = W.CONFIGS[args.config]
+    if args.layers:
+        cfg = dataclasses.replace(cfg, n_layers=args.layers)
+    if args.batch:
+        cfg = dataclasses.replace(cfg, batch=args.batch)
+    return cfg
+
+
 def run_kvr(args):
     import torch
     world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cfg = W.CONFIGS[args.config]
+    cfg = workload_config(args)
     wl = Workload(cfg, dev, args.variant)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
@@ -625,7 +637,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    cfg = W.CONFIGS[args.config]
+    cfg = workload_config(args)
     smp = OracleSampler(cfg)
     per_step = max(0.02, args.ref_budget / (args.steps + args.warmup))
     lq_s = smp.choose_lq(per_step)
@@ -659,6 +671,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="seconds of oracle work for the whole reference-arm run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
     ap.add_argument("--variant", default="default", choices=["default", "interleaved", "unrotated", "composite"],
                     help="pool RoPE layout / positions (the oracle baseline is timed for the default only)")
     args = ap.parse_args()
