@@ -99,6 +99,24 @@ def _assemble(lib, h, spans, span_offsets, cache_offsets, locals_=None, n_locals
     return st, plen
 
 
+def test_empty_and_negative_batches(lib):
+    """A batch of no requests is a no-op (no table is read, no GPU work); a
+    negative batch is an invalid argument -- for each of the three calls."""
+    st, h = _register(lib, _desc())
+    assert st == 0
+    try:
+        f0 = ctypes.c_float(0)
+        for batch, want in ((0, 0), (-1, 1)):
+            assert lib.kvr_assemble(h, batch, None, None, None, 0, None, None, None, None, None, None, 0,
+                                    None) == want
+            assert lib.kvr_query_attention(h, batch, None, None, None, None, None, None, None, None, None,
+                                           f0, None) == want
+            assert lib.kvr_prefill(h, batch, None, None, None, 0, None, None, None, None, None, None, 0,
+                                   None, None, None, None, None, f0, None) == want
+    finally:
+        lib.kvr_pool_unregister(h)
+
+
 def test_assemble_validates_spans_before_any_gpu_work(lib):
     st, h = _register(lib, _desc())
     assert st == 0
