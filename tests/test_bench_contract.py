@@ -40,3 +40,15 @@ def test_too_few_warmup_steps_are_refused():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], cwd=ROOT,
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_workload_overrides_reach_the_line():
+    """--batch / --layers (smaller or larger cases of a workload, for
+    profiling) change the measured configuration, and the line says so."""
+    d = _run("--impl", "reference", "--config", "1", "--batch", "2", "--layers", "2", "--steps", "2",
+             "--warmup", "3", "--ref-budget", "2")
+    assert d["config"]["workload"] == "tiny-fp32"
+    assert d["config"]["batch"] == 2
+    one = _run("--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "3", "--ref-budget", "2")
+    assert one["config"]["batch"] == 1
+    assert d["config"]["stitched_tokens_per_step"] > one["config"]["stitched_tokens_per_step"]
