@@ -193,11 +193,32 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
                 if (sp.dstep) {  // un-rotated source: token t turns by delta + t
                     const int r = r0 + u * RPP;
                     const int row = r - (r / sp.len) * sp.len;
+                    const int pos = sp.delta + row;
+                    if (pos >= 0 && pos < kRopeSplit) {
+                        // the low table row alone (rope_cs below 2^12), its pairs
+                        // of this chunk read as 16-byte vectors straight into (c, s)
+                        const float4 *lo = reinterpret_cast<const float4 *>(a.rope + (kRopeSplit + pos) * H2);
+                        const int i0 = a.interleaved ? (E / 2) * j : E * j;
+                        const int i1 = a.interleaved ? D / 4 + (E / 2) * j : E * j + E / 2;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float2 cs = rope_cs(a.rope, H2, sp.delta + row, rope_pair(a.interleaved, D, E, j, e));
-                        c[e] = cs.x;
-                        s[e] = cs.y;
+                        for (int q = 0; q < E / 4; ++q) {
+                            const float4 v0 = __ldg(lo + i0 / 2 + q), v1 = __ldg(lo + i1 / 2 + q);
+                            c[2 * q] = v0.x;
+                            s[2 * q] = v0.y;
+                            c[2 * q + 1] = v0.z;
+                            s[2 * q + 1] = v0.w;
+                            c[E / 2 + 2 * q] = v1.x;
+                            s[E / 2 + 2 * q] = v1.y;
+                            c[E / 2 + 2 * q + 1] = v1.z;
+                            s[E / 2 + 2 * q + 1] = v1.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            const float2 cs = rope_cs(a.rope, H2, pos, rope_pair(a.interleaved, D, E, j, e));
+                            c[e] = cs.x;
+                            s[e] = cs.y;
+                        }
                     }
                 }
                 Vec<T>::rotate(klo[u], khi[u], c, s, a.interleaved);
