@@ -219,12 +219,19 @@ def test_config5_serving_pool_sampled():
     _ok(run_parity_case(5, sample_units=3, requests=[0, 31, 63]))
 
 
-@pytest.mark.parametrize("variant", ["fp32", "fp32_composite", "bf16_with_locals", "cfg2_prefill"])
+@pytest.mark.parametrize("variant", ["fp32", "fp32_composite", "bf16_with_locals", "cfg2_prefill",
+                                     "bf16_past_4096"])
 def test_pool_keys_kept_before_rope(variant):
     """A pool registered with KVR_POOL_KEYS_UNROTATED: stitching applies RoPE
     at each token's position (request-local sources stay rotated at their
-    local positions)."""
-    if variant.startswith("fp32"):
+    local positions).  `bf16_past_4096`: a prefix of 4,805 rows, whose
+    positions cross 2^12, where the RoPE table lookup changes form."""
+    if variant == "bf16_past_4096":
+        base = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=9)
+        long_req = [[4, 0, 5]] + [[c % 4, 0, 96] for c in range(50)]
+        cfg, reqs = _custom(base, [long_req, [[1, 7, 60]]])
+        composite = False
+    elif variant.startswith("fp32"):
         cfg, reqs, composite = W.CONFIGS[1], None, variant.endswith("composite")
     elif variant == "bf16_with_locals":
         base = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, prompt_len=0, query_len=11)
