@@ -25,8 +25,30 @@
  *     never frees them and keeps none past the call, except the pool pointers
  *     that a registered pool holds until kvr_pool_unregister.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
- *     Calls enqueue work on it and return without waiting for the GPU, except
- *     kvr_check, which synchronizes the stream.
+ *     Calls enqueue work on it and return without waiting for the GPU, with
+ *     these exceptions, which are the library's only allocations and waits:
+ *       1. kvr_check synchronizes the stream.
+ *       2. The first call that enqueues work on a pool (or kvr_pool_reserve)
+ *          binds it to the current device: it allocates the RoPE tables
+ *          (4 MiB for head_dim 128) and an error word and builds the tables,
+ *          synchronously.
+ *       3. Staging slots.  A call whose span, local-source or request tables
+ *          do not fit inside its kernels' parameters (more than 64 spans,
+ *          local sources or requests) copies them up from one of the pool's
+ *          8 pinned staging slots, taken in turn.  A slot is allocated on
+ *          first use, and freed and allocated larger when a call needs more
+ *          (cudaFreeHost / cudaFree synchronize the device).  If the slot's
+ *          previous call has not yet run on the GPU (8 such calls queued
+ *          ahead of it), the call waits on the host for it.
+ *       4. Query scratch (tensor-core attention: bf16, head_dim 128).  The
+ *          rotated query heads of a call need n_layers * T * n_q_heads *
+ *          head_dim * 2 bytes of device memory (T = query tokens of the
+ *          call).  A call with more than the scratch holds waits for the
+ *          previous call's attention, frees it and allocates it larger.
+ *     kvr_pool_reserve makes 3 and 4 happen up front: afterwards, calls
+ *     within the reserved sizes allocate nothing and wait only in the one
+ *     case of 3 (8 calls with uploaded tables still queued).  kvr_pool_unregister
+ *     synchronizes the handle's work before it frees.
  *   - Every failure is a returned kvr_status; nothing aborts or traps.  Host
  *     validation runs before any launch, so an error status from validation
  *     means nothing was enqueued.  kvr_last_error() gives a one-line reason.
@@ -140,8 +162,8 @@ typedef struct {
  * no CUDA call).  The first call that enqueues work on the pool binds it to
  * the then-current device and builds the RoPE cos/sin tables for
  * (rope_theta, head_dim) there, synchronously (so make that first call
- * outside any stream capture); these tables, an error word and small staging
- * buffers are the library's only allocations.
+ * outside any stream capture); the conventions above list every allocation
+ * the handle makes afterwards.
  * Errors: KVR_ERR_INVALID_ARG (null, negative or unaligned strides, head_dim
  * odd, n_q_heads % n_kv_heads), KVR_ERR_UNSUPPORTED (dtype, head_dim).
  * On error *out is left NULL.
@@ -151,6 +173,23 @@ KVR_API kvr_status kvr_pool_register(const kvr_pool_desc *desc, kvr_pool_t *out)
 /* Release a handle and the library's own buffers (synchronizes the device
  * work the handle enqueued).  NULL is a no-op. */
 KVR_API kvr_status kvr_pool_unregister(kvr_pool_t pool);
+
+/*
+ * kvr_pool_reserve -- bind the pool to the current device (if no call has
+ * yet) and allocate, now, every buffer that calls within these limits need:
+ * the 8 staging slots sized for the largest tables of a call with up to
+ * max_batch requests, max_spans spans and max_locals local sources, and the
+ * query scratch for up to max_query_tokens query tokens per call (tensor-core
+ * path only).  It synchronizes (allocation and the wait for slots in use).
+ * After it, kvr_assemble / kvr_query_attention / kvr_prefill calls within the
+ * limits never allocate and never wait on the host, except on a staging slot
+ * whose previous call is still queued (see the conventions above).  Calls
+ * beyond the limits still work: they grow the buffers as described there.
+ * Make it outside any stream capture.  Errors: KVR_ERR_INVALID_ARG (NULL pool,
+ * a negative limit, max_query_tokens > 2^31 - 1), KVR_ERR_CUDA.
+ */
+KVR_API kvr_status kvr_pool_reserve(kvr_pool_t pool, int32_t max_batch, int32_t max_spans,
+                                    int32_t max_locals, int64_t max_query_tokens);
 
 /*
  * kvr_assemble -- gather + re-rotate + stitch (CoinRAG blog section 2.3).
@@ -309,13 +348,17 @@ KVR_API kvr_status kvr_selftest_wait(kvr_pool_t pool, uint64_t limit_ns, void *s
  *
  * Limits: at most 4096 non-empty spans and 256 local sources per call, and
  * head_dim <= 128; beyond them the call returns KVR_ERR_INVALID_ARG before
- * any GPU work.  The first call on a device looks up the scratch address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the scratch and the host
- * table: calls from several host threads, or calls that overlap on the GPU
- * (on different streams), race; the RoPE tables are rebuilt in the scratch,
- * on the caller's stream, whenever (rope_theta, head_dim) differs from the
- * previous call on that device.  Nothing in the scratch has to start at zero.
+ * any GPU work, with the reason in kvr_last_error().  The first call on a
+ * device looks up the scratch address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  A call with at
+ * most 64 spans and 64 local sources passes its tables inside the kernel's
+ * parameters; a larger one copies them from the library's fixed host tables
+ * into the scratch on the caller's stream.  All calls share the scratch and
+ * the host tables: calls from several host threads, or calls that overlap on
+ * the GPU (on different streams), race; the RoPE tables are rebuilt in the
+ * scratch, on the caller's stream, whenever (rope_theta, head_dim) differs
+ * from the previous call on that device.  Nothing in the scratch has to start
+ * at zero.
  */
 KVR_API kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t batch,
                                         const int32_t *span_offsets, const kvr_span *spans,
@@ -325,8 +368,13 @@ KVR_API kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t batch
                                         uint32_t flags, void *stream);
 
 /* Synchronize `stream` and return (then clear) the first error a kernel of
- * this pool recorded: KVR_OK, KVR_ERR_TIMEOUT, KVR_ERR_DEVICE_CHECK or
- * KVR_ERR_CUDA. */
+ * this pool recorded: KVR_OK, KVR_ERR_TIMEOUT (a bounded wait ran out),
+ * KVR_ERR_DEVICE_CHECK or KVR_ERR_CUDA.  KVR_ERR_DEVICE_CHECK: the
+ * tensor-core prefill or decode attention found a query row whose softmax
+ * denominator was not a finite positive number -- a NaN or an infinity in
+ * its query heads or in a key it attends to (inputs the host cannot see
+ * without reading device memory); the row's output is written as computed
+ * (not finite) and the rest of the call is unaffected. */
 KVR_API kvr_status kvr_check(kvr_pool_t pool, void *stream);
 
 /* Static string naming a status. */

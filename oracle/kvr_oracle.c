@@ -30,7 +30,7 @@
  *                      Mask" (independent attention, Figure 4); SemPIC page
  *                      (inline tokens interleaved under a causal mask).
  *
- * Readings of points the pages leave open (all listed in the design notes):
+ * Readings of points the pages leave open:
  *   - spans are half-open [start, end), length end - start;
  *   - the rotation applied to a cached span is delta = target - start, since
  *     the cached key already carries its chunk-local position start + t;

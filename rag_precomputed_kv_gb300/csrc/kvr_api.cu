@@ -5,10 +5,13 @@
 // tables out (the stitched row of span i is the prefix sum of the lengths
 // before it -- CoinRAG blog section 2.3), copy them to the device with one
 // asynchronous H2D copy from a pinned staging slot, and launch the kernels on
-// the caller's stream.  No call waits for the GPU except kvr_check and
-// pool registration.
+// the caller's stream.  Allocations and host waits happen only where the
+// header lists them: binding the pool to a device, growing a staging slot or
+// the query scratch past its size (kvr_pool_reserve sizes both up front), and
+// reusing a staging slot that an earlier call's work still holds.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <climits>
@@ -25,16 +28,16 @@ using namespace kvr;
 
 namespace {
 
-thread_local std::string g_last_error;
+// One-line reason of the last failure on this thread (a fixed buffer: the
+// error paths allocate nothing, the allocation-free entry point included).
+thread_local char g_last_error[512];
 
 kvr_status fail(kvr_status st, const char *fmt, ...)
 {
-    char buf[512];
     va_list ap;
     va_start(ap, fmt);
-    vsnprintf(buf, sizeof buf, fmt, ap);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
     va_end(ap);
-    g_last_error = buf;
     return st;
 }
 
@@ -43,7 +46,27 @@ kvr_status cuda_fail(cudaError_t e, const char *what)
     return fail(KVR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-constexpr int kSlots = 4;
+}  // namespace
+
+kvr_status kvr::record_error(kvr_status st, const char *msg)
+{
+    snprintf(g_last_error, sizeof g_last_error, "%s", msg ? msg : "");
+    return st;
+}
+
+namespace {
+
+// Staging slots per pool: a call whose tables do not fit its kernels'
+// parameters takes the next slot in turn, and waits on the host only if that
+// slot's previous call has not yet run (kSlots such calls queued ahead).
+constexpr int kSlots = 8;
+
+// Scoped NVTX range (a profiler's timeline shows which library call and which
+// kernel each stretch of host time enqueued; nothing without a profiler).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 struct Slot {
     void *host = nullptr;   // pinned: tables built by the host
@@ -107,15 +130,31 @@ struct kvr_pool {
 
     // A staging slot with at least `host_bytes` of pinned and `dev_bytes` of
     // device memory; waits until the slot's last upload and the kernels that
-    // read it are done.
+    // read it are done (only when kSlots later calls have been enqueued since
+    // and that work has not run yet).  A slot smaller than asked is freed and
+    // allocated again (cudaFreeHost / cudaFree synchronize the device).
     kvr_status acquire(size_t host_bytes, size_t dev_bytes, Slot **out)
     {
         Slot &s = slots[next];
         next = (next + 1) % kSlots;
         cudaError_t e;
-        if (s.used && (e = cudaEventSynchronize(s.done)) != cudaSuccess)
-            return cuda_fail(e, "staging slot wait");
+        if (s.used && cudaEventQuery(s.done) != cudaSuccess) {
+            NvtxRange r("kvr.staging_slot_wait");
+            if ((e = cudaEventSynchronize(s.done)) != cudaSuccess)
+                return cuda_fail(e, "staging slot wait");
+        }
+        kvr_status st = grow(s, host_bytes, dev_bytes);
+        if (st == KVR_OK)
+            *out = &s;
+        return st;
+    }
+
+    // Slot `s` (idle) with at least the given capacities, and its event.
+    static kvr_status grow(Slot &s, size_t host_bytes, size_t dev_bytes)
+    {
+        cudaError_t e;
         if (s.host_cap < host_bytes) {
+            NvtxRange r("kvr.staging_alloc");
             const size_t cap = std::max<size_t>({host_bytes, 2 * s.host_cap, 65536});
             if (s.host)
                 cudaFreeHost(s.host);
@@ -126,6 +165,7 @@ struct kvr_pool {
             s.host_cap = cap;
         }
         if (s.dev_cap < dev_bytes) {
+            NvtxRange r("kvr.staging_alloc");
             const size_t cap = std::max<size_t>({dev_bytes, 2 * s.dev_cap, 65536});
             if (s.dev)
                 cudaFree(s.dev);
@@ -137,7 +177,29 @@ struct kvr_pool {
         }
         if (!s.done && (e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming)) != cudaSuccess)
             return cuda_fail(e, "staging event");
-        *out = &s;
+        return KVR_OK;
+    }
+
+    // The rotated-query scratch with at least `bytes`: a smaller one is freed
+    // (after the last call's attention is done with it) and allocated again.
+    kvr_status grow_query_scratch(size_t bytes)
+    {
+        cudaError_t e;
+        if (q_rot_cap < bytes) {
+            NvtxRange r("kvr.query_scratch_alloc");
+            if (q_rot_used && (e = cudaEventSynchronize(q_rot_done)) != cudaSuccess)
+                return cuda_fail(e, "query scratch wait");
+            if (q_rot)
+                cudaFree(q_rot);
+            q_rot = nullptr;
+            q_rot_cap = 0;
+            q_rot_used = false;
+            if ((e = cudaMalloc(&q_rot, bytes)) != cudaSuccess)
+                return cuda_fail(e, "query scratch");
+            q_rot_cap = bytes;
+        }
+        if (!q_rot_done && (e = cudaEventCreateWithFlags(&q_rot_done, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "query scratch event");
         return KVR_OK;
     }
 };
@@ -252,6 +314,43 @@ extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
 }
 
 // The tcgen05 kernel runs for bf16 pools with head_dim 128 on sm_103.
+static bool use_tensor_cores(const kvr_pool &p);
+
+extern "C" kvr_status kvr_pool_reserve(kvr_pool_t p, int32_t max_batch, int32_t max_spans, int32_t max_locals,
+                                       int64_t max_query_tokens)
+{
+    if (!p)
+        return fail(KVR_ERR_INVALID_ARG, "pool is NULL");
+    if (max_batch < 0 || max_spans < 0 || max_locals < 0 || max_query_tokens < 0 ||
+        max_query_tokens > INT32_MAX)
+        return fail(KVR_ERR_INVALID_ARG, "negative or too large reservation (batch %d, spans %d, locals %d, "
+                    "query tokens %lld)", max_batch, max_spans, max_locals, (long long)max_query_tokens);
+    NvtxRange call("kvr_pool_reserve");
+    kvr_status st;
+    if ((st = ensure_device(p)) != KVR_OK)
+        return st;
+    DeviceGuard g(p->device);
+    // the largest table a call within the limits uploads: an assemble's spans
+    // and local sources, or a query attention's request / append tables
+    const size_t asm_bytes = align16((size_t)max_spans * sizeof(DevSpan)) + (size_t)max_locals * sizeof(DevLocal);
+    const size_t qa_bytes = align16((size_t)max_batch * sizeof(DevReq)) +
+                            align16((size_t)max_batch * sizeof(DevSpan)) + (size_t)max_batch * sizeof(DevLocal);
+    const size_t bytes = std::max(asm_bytes, qa_bytes);
+    cudaError_t e;
+    for (Slot &s : p->slots) {
+        if (s.used && (e = cudaEventSynchronize(s.done)) != cudaSuccess)
+            return cuda_fail(e, "staging slot wait");
+        if ((st = kvr_pool::grow(s, bytes, bytes)) != KVR_OK)
+            return st;
+    }
+    if (use_tensor_cores(*p)) {
+        const size_t q_bytes = (size_t)p->d.n_layers * (size_t)max_query_tokens * p->d.n_q_heads * p->d.head_dim * 2;
+        if (q_bytes > 0 && (st = p->grow_query_scratch(q_bytes)) != KVR_OK)
+            return st;
+    }
+    return KVR_OK;
+}
+
 static bool use_tensor_cores(const kvr_pool &p)
 {
     return attention_tc_supported(p.d.dtype, p.d.head_dim) && p.cc == 103 && p.encode;
@@ -481,6 +580,7 @@ static kvr_status asm_stage(kvr_pool *p, AsmPlan &pl, cudaStream_t s)
 // launched programmatically after it).
 static kvr_status asm_launch(kvr_pool *p, AsmPlan &pl, cudaStream_t s, bool record_slot = true)
 {
+    NvtxRange r("kvr.k_assemble");
     p->mark(0, s);
     cudaError_t e = launch_assemble(pl.a, p->d.dtype, p->d.head_dim, (int)pl.ds.size(), s,
                                     pl.inl ? &pl.tab : nullptr);
@@ -504,6 +604,7 @@ extern "C" kvr_status kvr_assemble(kvr_pool_t p, int32_t batch, const int32_t *s
         return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
     if (batch == 0)
         return KVR_OK;
+    NvtxRange call("kvr_assemble");
     AsmPlan pl;
     kvr_status st;
     if ((st = asm_validate(*p, batch, span_offsets, spans, locals, n_locals, cache_offsets, flags,
@@ -691,21 +792,8 @@ static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
         const int64_t q_rows = (int64_t)L * T * Hq;
         if (rows > (int64_t)INT32_MAX - 256 || q_rows > (int64_t)INT32_MAX - 256)   // int32 TMA coordinates
             return fail(KVR_ERR_UNSUPPORTED, "cache or query rows exceed the int32 TMA coordinate range");
-        const size_t q_bytes = (size_t)q_rows * D * 2;
-        if (p->q_rot_cap < q_bytes) {
-            if (p->q_rot_used && (e = cudaEventSynchronize(p->q_rot_done)) != cudaSuccess)
-                return cuda_fail(e, "query scratch wait");
-            if (p->q_rot)
-                cudaFree(p->q_rot);
-            p->q_rot = nullptr;
-            p->q_rot_cap = 0;
-            p->q_rot_used = false;
-            if ((e = cudaMalloc(&p->q_rot, q_bytes)) != cudaSuccess)
-                return cuda_fail(e, "query scratch");
-            p->q_rot_cap = q_bytes;
-        }
-        if (!p->q_rot_done && (e = cudaEventCreateWithFlags(&p->q_rot_done, cudaEventDisableTiming)) != cudaSuccess)
-            return cuda_fail(e, "query scratch event");
+        if ((st = p->grow_query_scratch((size_t)q_rows * D * 2)) != KVR_OK)
+            return st;
         if ((st = encode_cache_map(*p, p->q_rot, q_rows, &pl.mq)) != KVR_OK ||
             (st = encode_cache_map(*p, pl.cache_k, rows, &pl.mk)) != KVR_OK ||
             (st = encode_cache_map(*p, pl.cache_v, rows, &pl.mv)) != KVR_OK)
@@ -813,17 +901,21 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         const bool decode = !gl && pl.max_lq == 1 &&
                             decode_supported(p->d.dtype, D, p->d.n_q_heads / p->d.n_kv_heads);
         p->mark(2, s);
-        if (!decode)
+        if (!decode) {
+            NvtxRange r("kvr.k_query_prologue");
             e = launch_query_prologue(qp, rt, p->n_sms, after_assemble && !p->timed, s);
-        else
+        } else {
             e = cudaSuccess;
+        }
         p->mark(3, s);
         if (e == cudaSuccess && decode) {
+            NvtxRange r("kvr.k_decode_attention");
             const DecodeIO io{pl.kq, pl.vq, pl.cache_k, pl.cache_v, pl.at.interleaved};
             p->mark(4, s);
             e = launch_decode_attention(pl.at, rt, &pl.mk, &pl.mv, io, s);
             p->mark(5, s);
         } else if (e == cudaSuccess) {
+            NvtxRange r(gl ? "kvr.k_attention_tc_gathering" : "kvr.k_attention_tc");
             if (gl) {
                 ta.gather = true;
                 ta.tmap_pk = &gl->mpk;
@@ -840,6 +932,7 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         cudaEventRecord(p->q_rot_done, s);
         p->q_rot_used = true;
     } else {
+        NvtxRange r("kvr.k_attention_simt");
         p->mark(2, s);
         e = launch_assemble(pl.a, p->d.dtype, D, (int)pl.ap.size(), s, pl.inl ? &pl.tab : nullptr);
         p->mark(3, s);
@@ -868,6 +961,7 @@ extern "C" kvr_status kvr_query_attention(kvr_pool_t p, int32_t batch, const int
         return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
     if (batch == 0)
         return KVR_OK;
+    NvtxRange call("kvr_query_attention");
     QaPlan pl;
     kvr_status st;
     if ((st = qa_validate(*p, batch, cache_offsets, prefix_len, q_offsets, q, kq, vq, cache_k, cache_v,
@@ -901,6 +995,7 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
         return fail(KVR_ERR_INVALID_ARG, "batch %d", batch);
     if (batch == 0)
         return KVR_OK;
+    NvtxRange call("kvr_prefill");
     // every check of both halves before anything is enqueued
     const bool gather = flags & KVR_PREFILL_SKIP_PREFIX_CACHE;
     if (gather) {
@@ -1008,6 +1103,9 @@ extern "C" kvr_status kvr_check(kvr_pool_t p, void *stream)
     cudaMemset(p->err, 0, sizeof(int));
     if (w == kDevTimeout)
         return fail(KVR_ERR_TIMEOUT, "a kernel's bounded wait ran out");
+    if (w == kDevBadInput)
+        return fail(KVR_ERR_DEVICE_CHECK, "an attention row's softmax denominator was not finite and positive "
+                                          "(NaN or infinity in the query heads or the keys it attends to)");
     return fail(KVR_ERR_DEVICE_CHECK, "a kernel flagged device-side input (code %d)", w);
 }
 
@@ -1025,7 +1123,7 @@ extern "C" const char *kvr_status_string(kvr_status s)
     return "KVR_ERR_UNKNOWN";
 }
 
-extern "C" const char *kvr_last_error(void) { return g_last_error.c_str(); }
+extern "C" const char *kvr_last_error(void) { return g_last_error; }
 
 extern "C" kvr_status kvr_set_timing_events(kvr_pool_t p, void *const *events)
 {

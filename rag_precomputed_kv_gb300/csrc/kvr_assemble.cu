@@ -125,6 +125,9 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
     constexpr int TPR = H2 / E;                   // threads per row
     constexpr int RPP = kAssembleThreads / TPR;   // rows per pass
     static_assert(H2 % E == 0 && kAssembleThreads % TPR == 0, "head_dim");
+    // the per-token (cos, sin) lookup below reads pairs i0 / 2 .. and i1 / 2 ..
+    // as 16-byte float4 vectors of two pairs: its pair indices must be even
+    static_assert(E % 4 == 0 && H2 % 2 == 0 && (D / 4) % 2 == 0, "16-byte (cos, sin) vector alignment");
 
     // the next kernel (the query prologue) touches none of this kernel's
     // rows: it may start alongside

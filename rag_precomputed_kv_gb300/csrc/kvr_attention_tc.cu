@@ -836,6 +836,10 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 l_fin = __fmaf_rn(x == 0 ? lp : l_run, w1, __fmul_rn(x == 0 ? l_run : lp, w0));
             }
             const float inv = row_ok ? 1.f / l_fin : 0.f;
+            // a NaN or infinity among the row's query or key elements leaves no
+            // finite positive denominator: report it (the row is written as computed)
+            if (row_ok && !(l_fin > 0.f && l_fin < INFINITY))
+                atomicCAS(a.err, kDevOk, kDevBadInput);
             const int64_t orow = row_ok ? (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD
                                         : -1;
             __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);

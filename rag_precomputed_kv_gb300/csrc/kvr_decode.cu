@@ -483,6 +483,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             L += ll[w * 16 + rr] * wgt[w];
         }
         const float inv = 1.f / L;
+        // a NaN or infinity among the row's query or key elements leaves no
+        // finite positive denominator: report it (the row is written as computed)
+        if (!(L > 0.f && L < INFINITY) && (threadIdx.x & 7) == 0 && a.err)
+            atomicCAS(a.err, kDevOk, kDevBadInput);
         const int c0 = 16 * (threadIdx.x & 7);
         uint32_t pk[8];
 #pragma unroll

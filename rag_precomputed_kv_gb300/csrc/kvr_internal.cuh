@@ -147,8 +147,14 @@ struct alignas(16) DevReq {
 };
 static_assert(sizeof(DevReq) == 48, "request table layout");
 
-// Device error word codes (first error wins).
+// Device error word codes (first error wins).  kDevBadInput: an attention
+// row's softmax denominator came out non-finite or zero (a NaN or infinity in
+// the query heads or the keys it saw); the row's output is written as computed.
 enum : int { kDevOk = 0, kDevTimeout = 1, kDevBadInput = 2 };
+
+// Records `msg` as this host thread's last error (kvr_last_error) and
+// returns `st`; allocates nothing.
+kvr_status record_error(kvr_status st, const char *msg);
 
 struct AssembleArgs {
     const DevSpan *spans;

@@ -42,8 +42,9 @@ NaDevice g_na_dev[kNaMaxDevices];
 DevSpan g_na_spans[kNaMaxSpans];     // host-side tables, built per call
 DevLocal g_na_locals[kNaMaxLocals];
 
-// The status is the whole error report (the message says why, for readers).
-kvr_status na_fail(kvr_status st, const char *) { return st; }
+// The status, with its reason recorded for kvr_last_error (a fixed
+// thread-local buffer: no allocation).
+kvr_status na_fail(kvr_status st, const char *why) { return record_error(st, why); }
 
 bool na_aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -201,11 +202,22 @@ extern "C" kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t ba
     for (int i = 0; i < n_locals; ++i)
         g_na_locals[i] = DevLocal{locals[i].k, locals[i].v, locals[i].stride[0], locals[i].stride[1],
                                   locals[i].stride[2], locals[i].len};
-    if ((e = cudaMemcpyAsync(dspans, g_na_spans, sizeof(DevSpan) * n, cudaMemcpyHostToDevice, s)) !=
-            cudaSuccess ||
-        (n_locals > 0 && (e = cudaMemcpyAsync(dlocals, g_na_locals, sizeof(DevLocal) * n_locals,
-                                              cudaMemcpyHostToDevice, s)) != cudaSuccess))
+    // a small call's tables travel inside the kernel parameters (a stack copy,
+    // like kvr_assemble's); a larger call's go up into the scratch from the
+    // host tables above
+    const bool inl = n <= kInlineEntries && n_locals <= kInlineEntries;
+    AssembleTables tab;
+    if (inl) {
+        for (int i = 0; i < n; ++i)
+            tab.spans[i] = g_na_spans[i];
+        for (int i = 0; i < n_locals; ++i)
+            tab.locals[i] = g_na_locals[i];
+    } else if ((e = cudaMemcpyAsync(dspans, g_na_spans, sizeof(DevSpan) * n, cudaMemcpyHostToDevice, s)) !=
+                   cudaSuccess ||
+               (n_locals > 0 && (e = cudaMemcpyAsync(dlocals, g_na_locals, sizeof(DevLocal) * n_locals,
+                                                     cudaMemcpyHostToDevice, s)) != cudaSuccess)) {
         return na_fail(KVR_ERR_CUDA, cudaGetErrorString(e));
+    }
 
     AssembleArgs a{};
     a.spans = dspans;
@@ -226,7 +238,7 @@ extern "C" kvr_status kvr_assemble_noalloc(const kvr_pool_desc *desc, int32_t ba
     const int64_t avg = flat / n > 0 ? flat / n : 1;
     a.upc = (int)(256 / avg > LH ? LH : (256 / avg < 1 ? 1 : 256 / avg));
     a.interleaved = (d.flags & KVR_POOL_ROPE_INTERLEAVED) ? 1 : 0;
-    if ((e = launch_assemble(a, d.dtype, d.head_dim, n, s)) != cudaSuccess)
+    if ((e = launch_assemble(a, d.dtype, d.head_dim, n, s, inl ? &tab : nullptr)) != cudaSuccess)
         return na_fail(KVR_ERR_CUDA, cudaGetErrorString(e));
     return KVR_OK;
 }

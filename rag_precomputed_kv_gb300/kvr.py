@@ -30,7 +30,7 @@ STATUS = {0: "KVR_OK", 1: "KVR_ERR_INVALID_ARG", 2: "KVR_ERR_OUT_OF_RANGE", 3: "
 
 EXPORTED = ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
             "kvr_prefill", "kvr_check", "kvr_status_string", "kvr_last_error", "kvr_attention_path",
-            "kvr_set_timing_events", "kvr_selftest_wait", "kvr_assemble_noalloc")
+            "kvr_set_timing_events", "kvr_selftest_wait", "kvr_assemble_noalloc", "kvr_pool_reserve")
 PATH_UNBOUND, PATH_CUDA_CORES, PATH_TCGEN05 = -1, 0, 1
 
 
@@ -80,6 +80,7 @@ def load(path: str = LIB_PATH):
     lib.kvr_assemble_noalloc.argtypes = [ctypes.POINTER(PoolDesc), i32, vp, vp, vp, i32, vp, vp, vp, vp, vp,
                                          vp, ctypes.c_uint32, vp]
     lib.kvr_selftest_wait.argtypes = [vp, ctypes.c_uint64, vp]
+    lib.kvr_pool_reserve.argtypes = [vp, i32, i32, i32, i64]
     lib.kvr_status_string.restype = ctypes.c_char_p
     lib.kvr_status_string.argtypes = [ctypes.c_int]
     lib.kvr_last_error.restype = ctypes.c_char_p
@@ -88,7 +89,7 @@ def load(path: str = LIB_PATH):
     lib.kvr_attention_path.argtypes = [vp]
     lib.kvr_attention_path.restype = ctypes.c_int32
     for name in ("kvr_pool_register", "kvr_pool_unregister", "kvr_assemble", "kvr_query_attention",
-                 "kvr_prefill", "kvr_check", "kvr_selftest_wait", "kvr_assemble_noalloc"):
+                 "kvr_prefill", "kvr_check", "kvr_selftest_wait", "kvr_assemble_noalloc", "kvr_pool_reserve"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -190,6 +191,13 @@ class Pool:
         self._keep = (k, v)
         self.n_layers, self.n_kv_heads, self.n_q_heads, self.head_dim = L, H, n_q_heads, D
         self.dtype = k.dtype
+
+    def reserve(self, max_batch: int = 0, max_spans: int = 0, max_locals: int = 0, max_query_tokens: int = 0):
+        """kvr_pool_reserve: bind the pool to the current device and allocate
+        now every staging and scratch buffer that calls within these limits
+        need; later calls within them never allocate."""
+        _raise(load().kvr_pool_reserve(self._h, int(max_batch), int(max_spans), int(max_locals),
+                                       int(max_query_tokens)))
 
     def close(self):
         if getattr(self, "_h", None):

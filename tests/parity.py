@@ -171,11 +171,13 @@ class Case:
 
 def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requests=None,
                     attention=True, composite=False, seed_units=0, case=None, prefill=False,
-                    skip_prefix=False):
+                    skip_prefix=False, force_units=()):
     """Run one configuration and compare with the oracle; returns a summary
     dict with ``ok`` and the worst errors.  skip_prefix: kvr_prefill with
     KVR_PREFILL_SKIP_PREFIX_CACHE, whose cache prefix rows must stay as they
-    were (NaN), everything else compared as usual."""
+    were (NaN), everything else compared as usual.  ``sample_units`` seeded
+    (layer, kv-head) units are checked per request, plus ``force_units``
+    (e.g. the last layer's)."""
     import torch
     cfg = cfg or W.CONFIGS[cid]
     case = case or Case(cfg, device=device, composite=composite)
@@ -191,7 +193,8 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
     flat0 = np.concatenate([[0], np.cumsum(case.prefix)])
     for b in req_ids:
         units = list(range(case.LH)) if sample_units is None else sorted(
-            rng.choice(case.LH, size=min(sample_units, case.LH), replace=False).tolist())
+            set(rng.choice(case.LH, size=min(sample_units, case.LH), replace=False).tolist())
+            | {int(u) % case.LH for u in force_units})
         spans = case.spans[b]
         srcs = {int(s): case.source(int(s), units) for s in np.unique(spans[:, 0])}
         if srcs:

@@ -74,6 +74,18 @@ def test_register_rejects_bad_descriptors(lib, bad, status):
     assert lib.kvr_last_error().decode()
 
 
+def test_reserve_rejects_bad_limits_before_any_cuda_call(lib):
+    st, h = _register(lib, _desc())
+    assert st == 0 and h.value
+    try:
+        assert lib.kvr_pool_reserve(None, 1, 1, 0, 1) == 1
+        for bad in ((-1, 0, 0, 0), (0, -1, 0, 0), (0, 0, -1, 0), (0, 0, 0, -1), (0, 0, 0, 1 << 31)):
+            assert lib.kvr_pool_reserve(h, *bad) == 1, bad
+            assert "reservation" in lib.kvr_last_error().decode()
+    finally:
+        lib.kvr_pool_unregister(h)
+
+
 def test_null_arguments(lib):
     h = ctypes.c_void_p()
     assert lib.kvr_pool_register(None, ctypes.byref(h)) == 1

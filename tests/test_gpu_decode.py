@@ -19,25 +19,32 @@ pytestmark = pytest.mark.gpu
 STEPS = 3
 
 
-def _run(cfg, reqs, sample_units=None, skip=(), il=False, turn=0):
+def _run(cfg, reqs, sample_units=None, skip=(), il=False, turn=0, check=None, steps=STEPS, force_units=()):
     """`skip`: requests that take no token in the decode steps (q_len 0);
     `il`: a pool with interleaved RoPE pairs; `turn`: after the decode steps,
     a further query of that many tokens per request on the same cache (the
-    next turn of a conversation)."""
+    next turn of a conversation); `check`: the requests compared with the
+    oracle (default all; every request decodes either way)."""
     import torch
-    case = Case(cfg, reqs=reqs, spare_rows=STEPS + 2 + turn, rope_interleaved=il)
+    case = Case(cfg, reqs=reqs, spare_rows=steps + 2 + turn, rope_interleaved=il)
     case.run(prefill=True)
     L, H, Hq, D = cfg.n_layers, cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim
     G, lq, B = Hq // H, cfg.query_len, len(case.reqs)
     dev = case.cache_k.device
     rng = np.random.default_rng(7)
     units = list(range(case.LH)) if sample_units is None else sorted(
-        rng.choice(case.LH, size=sample_units, replace=False).tolist())
+        set(rng.choice(case.LH, size=sample_units, replace=False).tolist()) | set(force_units))
+    checked = set(range(B) if check is None else check)
     li = [u // H for u in units]
     hi = [u % H for u in units]
     # the oracle's cache of every sampled unit: stitched prefix + query rows
     kc, vc = [], []
     for b in range(B):
+        if b not in checked:   # never compared: a placeholder of the right length
+            n_b = int(case.prefix[b]) + lq
+            kc.append(np.zeros((0, n_b, D)))
+            vc.append(np.zeros((0, n_b, D)))
+            continue
         spans = case.spans[b]
         srcs = {int(s): case.source(int(s), units) for s in np.unique(spans[:, 0])}
         if srcs:
@@ -61,7 +68,7 @@ def _run(cfg, reqs, sample_units=None, skip=(), il=False, turn=0):
     tok = {b: i for i, b in enumerate(act)}
     qoffs = np.concatenate([[0], np.cumsum([0 if b in skip else 1 for b in range(B)])]).astype(np.int32)
     worst = (0.0, 0.0)
-    for step in range(STEPS):
+    for step in range(steps):
         n = np.array([kc[b].shape[1] for b in range(B)], np.int32)   # rows before this step
         T = len(act)
         q1 = torch.randn((L, T, Hq, D), generator=g, device=dev).to(dt)
@@ -74,6 +81,10 @@ def _run(cfg, reqs, sample_units=None, skip=(), il=False, turn=0):
         q1n, k1n, v1n, o1n = (to_np64(x) for x in (q1, k1, v1, o1))
         for b in act:
             t = tok[b]
+            if b not in checked:
+                kc[b] = np.zeros((0, kc[b].shape[1] + 1, D))
+                vc[b] = np.zeros((0, vc[b].shape[1] + 1, D))
+                continue
             qu = np.stack([q1n[l, t, h * G:(h + 1) * G][None] for l, h in zip(li, hi)])   # [U, 1, G, D]
             ku = np.stack([k1n[l, t, h][None] for l, h in zip(li, hi)])                    # [U, 1, D]
             vu = np.stack([v1n[l, t, h][None] for l, h in zip(li, hi)])
@@ -102,7 +113,7 @@ def _run(cfg, reqs, sample_units=None, skip=(), il=False, turn=0):
         torch.cuda.synchronize()
         case.pool.check()
         q2n, k2n, v2n, o2n = (to_np64(x) for x in (q2, k2, v2, o2))
-        for b in range(B):
+        for b in sorted(checked):
             sl = slice(b * turn, (b + 1) * turn)
             qu = np.stack([q2n[l, sl, h * G:(h + 1) * G] for l, h in zip(li, hi)])
             ku = np.stack([k2n[l, sl, h] for l, h in zip(li, hi)])
@@ -131,6 +142,16 @@ def test_decode_steps_fp32_cuda_cores():
 
 def test_decode_steps_default_workload_sampled():
     _run(W.CONFIGS[2], None, sample_units=6)
+
+
+def test_decode_step_serving_pool():
+    """One decode step on the serving-scale workload (Qwen3-8B shape, 77 GB
+    pool, 64 requests) after its prefill: every request decodes; requests
+    0, 31 and 63 are compared, on 16 seeded units plus the last layer's
+    first and last kv head."""
+    c = W.CONFIGS[5]
+    last = ((c.n_layers - 1) * c.n_kv_heads, c.n_layers * c.n_kv_heads - 1)
+    _run(c, None, sample_units=16, check=[0, 31, 63], steps=1, force_units=last)
 
 
 @pytest.mark.parametrize("variant", ["g1", "g16", "short_blocks_and_idle_requests", "interleaved_rope"])

@@ -42,8 +42,18 @@ def test_fp32_and_head_dim_64_use_cuda_cores():
     assert case.pool.attention_path == kvr.PATH_CUDA_CORES
 
 
+def _last_layer(cid):
+    """The first and last kv head of the last layer (units of the last
+    (layer, kv-head) rows of every cache block)."""
+    c = W.CONFIGS[cid]
+    return ((c.n_layers - 1) * c.n_kv_heads, c.n_layers * c.n_kv_heads - 1)
+
+
 def test_config3_nuggets_sampled_units():
-    _ok(run_parity_case(3, sample_units=6))
+    """Every request of the batch, 16 seeded (layer, kv-head) units each plus
+    the last layer's first and last kv head."""
+    res = _ok(run_parity_case(3, sample_units=16, force_units=_last_layer(3)))
+    assert res["units"] >= 16 * 16
 
 
 def _custom(cfg, span_lists, local_lens=None):
@@ -212,11 +222,19 @@ def test_prefill_matches_oracle_and_the_two_calls(name):
 
 
 def test_config4_inline_docs_sampled():
-    _ok(run_parity_case(4, sample_units=2, requests=[0, 7]))
+    """All eight requests (33,248-row prefixes), 8 seeded units each plus
+    the last layer's first and last kv head."""
+    res = _ok(run_parity_case(4, sample_units=8, force_units=_last_layer(4)))
+    assert res["units"] >= 8 * 8
 
 
 def test_config5_serving_pool_sampled():
-    _ok(run_parity_case(5, sample_units=3, requests=[0, 31, 63]))
+    """Eight requests spread over the batch of 64, the last one included
+    (the shortest requests run in the attention's last, split round), 16
+    seeded units each plus the last layer's first and last kv head."""
+    reqs = [0, 9, 18, 27, 36, 45, 54, 63]
+    res = _ok(run_parity_case(5, sample_units=16, requests=reqs, force_units=_last_layer(5)))
+    assert res["units"] >= 8 * 16
 
 
 @pytest.mark.parametrize("variant", ["fp32", "fp32_composite", "bf16_with_locals", "cfg2_prefill",
