@@ -645,6 +645,25 @@ kvr_status encode_cache_map(const kvr_pool &p, void *base, int64_t rows, CUtenso
     return KVR_OK;
 }
 
+// The output [L * T][H_q][D] as a 3-D tensor with a box of one 64-column half
+// of G heads x 32 / G tokens (a warp's 32 packed rows), 128-byte swizzle.
+kvr_status encode_out_map(const kvr_pool &p, void *base, int64_t tokens, CUtensorMap *m)
+{
+    if (!p.encode)
+        return fail(KVR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled not available");
+    const int G = p.d.n_q_heads / p.d.n_kv_heads;
+    const cuuint64_t dims[3] = {(cuuint64_t)p.d.head_dim, (cuuint64_t)p.d.n_q_heads, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.d.head_dim * 2, (cuuint64_t)p.d.n_q_heads * p.d.head_dim * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(32 / G)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = p.encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(KVR_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+    return KVR_OK;
+}
+
 // The pool as a 2-D [entries * L * H_kv * entry_len, D] tensor with a box of
 // one row (64 columns): the attention kernel's gather4 source.
 kvr_status encode_gather_map(const kvr_pool &p, const void *base, CUtensorMap *m, uint32_t box_rows = 1)
@@ -686,7 +705,7 @@ struct QaPlan {
     std::vector<DevSpan> ap;     // the query keys / values as append spans (CUDA-core path)
     std::vector<DevLocal> al;
     bool tc = false, inl = false;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     ReqTable rt_inl;
     AssembleTables tab;
     AssembleArgs a{};
@@ -798,6 +817,20 @@ static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
             (st = encode_cache_map(*p, pl.cache_k, rows, &pl.mk)) != KVR_OK ||
             (st = encode_cache_map(*p, pl.cache_v, rows, &pl.mv)) != KVR_OK)
             return st;
+        // G a power of two and `out` in device memory: the attention's epilogue
+        // writes each warp's 32 rows (32 / G whole tokens) with one TMA store
+        const int G = Hq / Hkv;
+        pl.at.out_tma = 0;
+        if ((G & (G - 1)) == 0 && G <= 32) {
+            cudaPointerAttributes pa{};
+            if (cudaPointerGetAttributes(&pa, pl.out) == cudaSuccess && pa.type == cudaMemoryTypeDevice) {
+                if ((st = encode_out_map(*p, pl.out, (int64_t)L * T, &pl.mo)) != KVR_OK)
+                    return st;
+                pl.at.out_tma = 1;
+            } else {
+                cudaGetLastError();
+            }
+        }
         // the previous call's attention must be done with the query scratch
         if (p->q_rot_used && (e = cudaStreamWaitEvent(s, p->q_rot_done, 0)) != cudaSuccess)
             return cuda_fail(e, "query scratch ordering");
@@ -886,6 +919,7 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
     cudaError_t e;
     if (pl.tc) {
         TcAttnArgs ta{pl.at, &rt, &pl.mq, &pl.mk, &pl.mv, pl.m_blocks, p->n_sms};
+        ta.tmap_out = &pl.mo;
         // the last wave's units split in two halves of their keys when two
         // halves of each fit one wave and the grid can run as two-CTA clusters
         const int64_t units = (int64_t)pl.m_blocks * p->d.n_layers * p->d.n_kv_heads;

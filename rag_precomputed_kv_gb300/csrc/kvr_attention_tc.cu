@@ -104,11 +104,17 @@ constexpr int kBarReady = kBarDrain + 1;          // [kSlots] gathered tile rota
 // take this CTA's half of the partner's tile
 constexpr int kBarPeerData = kBarReady + kSlots;
 constexpr int kBarPeerFree = kBarPeerData + 1;
-constexpr int kNumBars = kBarPeerFree + 1;
+// the geometry of the CTA's next items, written by the producer warp (two
+// slots): full (1 arrival), read by every consumer warp (one arrival each)
+constexpr int kBarGeoFull = kBarPeerFree + 1;     // [2]
+constexpr int kBarGeoEmpty = kBarGeoFull + 2;     // [2]
+constexpr int kNumBars = kBarGeoEmpty + 2;
 constexpr int kOffMeta = kOffBar + 8 * kNumBars;  // [2][128] int: rotation of each row of the K slots
 constexpr int kOffTmemAddr = kOffMeta + 2 * kTileN * 4;
 constexpr int kOffAbort = kOffTmemAddr + 4;
-constexpr int kSmemBytes = kOffAbort + 4 + 1024;   // + alignment slack
+constexpr int kOffGeo = (kOffAbort + 4 + 15) & ~15;   // [2] Item
+constexpr int kGeoBytes = 128;
+constexpr int kSmemBytes = kOffGeo + 2 * kGeoBytes + 1024;   // + alignment slack
 // where a split unit's partner CTA leaves its half of this CTA's tile: O as
 // fp16 with a power-of-two scale per row ([16-byte piece of 8][row]) over the
 // K/V ring; the running max, sum and scale (fp32 [3][128]) over the Q tiles
@@ -229,6 +235,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
 }
+
+// Shared memory -> global through a 3-D tensor map (bulk async-group of the
+// issuing thread); commit, and wait until the group no longer reads shared
+// memory / has completed.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -518,20 +538,12 @@ struct Unit {
 // same time on neighbouring SMs and read the same K/V tiles (the second read
 // hits L2).  With the longest requests first, every round of units is of
 // even length and the last, partial round holds the shortest.
-__device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, int n_blocks, int u)
+// The geometry of unit u of request `rq` (table index b).
+__device__ __forceinline__ Unit unit_geometry(const AttnArgs &a, const DevReq &rq, int b, int u)
 {
     Unit w;
-    (void)n_blocks;
-    int lo = 0, hi = a.n_reqs - 1;
-    while (lo < hi) {   // the last request whose first unit is <= u
-        const int mid = (lo + hi + 1) >> 1;
-        if (reqs[mid].unit0 <= u)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    w.rq = reqs[lo];
-    w.b = lo;
+    w.rq = rq;
+    w.b = b;
     const int G = a.n_q_heads / a.n_kv_heads;
     const int nb = (G * w.rq.q_len + 2 * kTileM - 1) / (2 * kTileM);   // 256-row blocks of the request
     const int local = u - w.rq.unit0;
@@ -559,6 +571,61 @@ __device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, i
     return w;
 }
 
+__device__ __forceinline__ Unit unit_at(const AttnArgs &a, const DevReq *reqs, int n_blocks, int u)
+{
+    (void)n_blocks;
+    int lo = 0, hi = a.n_reqs - 1;
+    while (lo < hi) {   // the last request whose first unit is <= u
+        const int mid = (lo + hi + 1) >> 1;
+        if (reqs[mid].unit0 <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return unit_geometry(a, reqs[lo], lo, u);
+}
+
+// The request table of a batch of up to 64 requests held in a warp's
+// registers (lane i: requests i and 32 + i), so that the producer warp finds a
+// unit's request with a ballot and shuffles instead of a chain of dependent
+// loads (kernel parameters or global memory, whose lines the K/V stream keeps
+// evicting: about 2 us per item otherwise).
+struct ReqRegs {
+    DevReq r[2];
+    bool ok;            // the batch has at most 64 requests (else: table lookups)
+
+    __device__ __forceinline__ void load(const AttnArgs &a, const DevReq *reqs, int lane)
+    {
+        ok = a.n_reqs <= 64;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = lane + 32 * k;
+            r[k] = {};
+            if (ok && i < a.n_reqs)
+                r[k] = reqs[i];
+        }
+    }
+};
+
+__device__ __forceinline__ Unit unit_at_warp(const AttnArgs &a, const ReqRegs &rr, int u, int lane)
+{
+    const unsigned lo = __ballot_sync(0xffffffffu, lane < a.n_reqs && rr.r[0].unit0 <= u);
+    const unsigned hi = __ballot_sync(0xffffffffu, lane + 32 < a.n_reqs && rr.r[1].unit0 <= u);
+    const int b = hi ? 32 + 31 - __clz(hi) : 31 - __clz(lo);   // the last request whose first unit is <= u
+    const int k = b >> 5, src = b & 31;
+    DevReq rq;
+    rq.cache_row0 = __shfl_sync(0xffffffffu, k ? rr.r[1].cache_row0 : rr.r[0].cache_row0, src);
+    rq.cap = __shfl_sync(0xffffffffu, k ? rr.r[1].cap : rr.r[0].cap, src);
+    rq.prefix = __shfl_sync(0xffffffffu, k ? rr.r[1].prefix : rr.r[0].prefix, src);
+    rq.q_off = __shfl_sync(0xffffffffu, k ? rr.r[1].q_off : rr.r[0].q_off, src);
+    rq.q_len = __shfl_sync(0xffffffffu, k ? rr.r[1].q_len : rr.r[0].q_len, src);
+    rq.unit0 = __shfl_sync(0xffffffffu, k ? rr.r[1].unit0 : rr.r[0].unit0, src);
+    rq.span0 = __shfl_sync(0xffffffffu, k ? rr.r[1].span0 : rr.r[0].span0, src);
+    rq.span_end = __shfl_sync(0xffffffffu, k ? rr.r[1].span_end : rr.r[0].span_end, src);
+    rq.pad_[0] = rq.pad_[1] = rq.pad_[2] = 0;
+    return unit_geometry(a, rq, b, u);
+}
+
 // Work item `it` of the persistent loop: units 0..n_full-1 whole, then two
 // halves of each remaining unit (key tiles [0, h) and [h, n), h = ceil(n/2)).
 struct Item {
@@ -567,12 +634,53 @@ struct Item {
     int jb, je;         // key tiles of the item
 };
 
-__device__ __forceinline__ Item item_at(const AttnArgs &a, const DevReq *reqs, int n_blocks, int it)
+// The producer warp computes each item's geometry once and publishes it in
+// shared memory; the other roles read it there.  (Computed by every role, its
+// request-table and argument reads -- kernel parameters or global memory,
+// whose lines the K/V stream evicts from the caches -- held each role 2-4 us
+// at every item boundary, all waiting on the same lines.)
+// What the consumer roles read of an item.
+struct Geo {
+    int jb, je, half, n_tiles;
+    int n_t[2], row0[2];
+    int m_rows, q_len, prefix, q_off;
+    int l, h, n_valid, pad_;
+    int64_t kv_row0;
+};
+static_assert(sizeof(Geo) <= kGeoBytes, "geometry slot");
+
+__device__ __forceinline__ void geo_of(const Item &t, Geo &o)
+{
+    o.jb = t.jb;
+    o.je = t.je;
+    o.half = t.half;
+    o.n_tiles = t.w.n_tiles;
+    o.n_t[0] = t.w.n_t[0];
+    o.n_t[1] = t.w.n_t[1];
+    o.row0[0] = t.w.row0[0];
+    o.row0[1] = t.w.row0[1];
+    o.m_rows = t.w.m_rows;
+    o.q_len = t.w.rq.q_len;
+    o.prefix = t.w.rq.prefix;
+    o.q_off = t.w.rq.q_off;
+    o.l = t.w.l;
+    o.h = t.w.h;
+    o.n_valid = t.w.n_valid;
+    o.pad_ = 0;
+    o.kv_row0 = t.w.kv_row0;
+}
+template <bool kG>
+constexpr uint32_t geo_consumer_warps() { return kG ? 13u : 9u; }   // softmax 8, MMA 1, rotators 4
+
+// `rr`: the producer warp's register copy of the request table (all 32
+// lanes call with the same `it`), or NULL.
+__device__ __forceinline__ Item item_at(const AttnArgs &a, const DevReq *reqs, int n_blocks, int it,
+                                        const ReqRegs *rr = nullptr, int lane = 0)
 {
     Item t;
     const int u = it < a.n_full ? it : a.n_full + ((it - a.n_full) >> 1);
     t.half = it < a.n_full ? -1 : ((it - a.n_full) & 1);
-    t.w = unit_at(a, reqs, n_blocks, u);
+    t.w = (rr && rr->ok) ? unit_at_warp(a, *rr, u, lane) : unit_at(a, reqs, n_blocks, u);
     const int hs = (t.w.n_tiles + 1) >> 1;
     t.jb = t.half == 1 ? hs : 0;
     t.je = t.half == 0 ? hs : t.w.n_tiles;
@@ -588,7 +696,8 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                    const __grid_constant__ ReqTable rt, const int n_blocks,
                    const __grid_constant__ CUtensorMap tmpk, const __grid_constant__ CUtensorMap tmpv,
                    const __grid_constant__ CUtensorMap tmbk, const __grid_constant__ CUtensorMap tmbv,
-                   const __grid_constant__ GatherArgs g, const __grid_constant__ SpanTable st)
+                   const __grid_constant__ GatherArgs g, const __grid_constant__ SpanTable st,
+                   const __grid_constant__ CUtensorMap tmo)
 {
     const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
     extern __shared__ uint8_t smem_raw[];
@@ -604,12 +713,36 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     const int n_units = n_blocks * a.n_layers * a.n_kv_heads;
     const int n_items = 2 * n_units - a.n_full;
 
+    // geometry of this CTA's k-th item: slot k & 1 of the shared-memory ring
+    auto geo_slot = [&](int k) { return reinterpret_cast<Geo *>(smem + kOffGeo + (k & 1) * kGeoBytes); };
+    // consumer warps: wait for item k's geometry (then read its fields and
+    // release the slot with geo_done)
+    auto geo_wait = [&](int k) -> const Geo * {
+        if (!mbar_wait(bar(kBarGeoFull + (k & 1)), (uint32_t)(k >> 1) & 1u, abort_flag))
+            return nullptr;
+        return geo_slot(k);
+    };
+    auto geo_done = [&](int k) {
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar(kBarGeoEmpty + (k & 1)));
+    };
+    // producer (one thread): publish item k's geometry once its slot is free
+    auto geo_put = [&](int k, const Item &gm) -> bool {
+        if (k >= 2 && !mbar_wait(bar(kBarGeoEmpty + (k & 1)), (uint32_t)((k >> 1) - 1) & 1u, abort_flag))
+            return false;
+        geo_of(gm, *geo_slot(k));
+        mbar_arrive(bar(kBarGeoFull + (k & 1)));   // release: the record is visible to the waiters
+        return true;
+    };
+
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool wg = (i >= kBarPFull && i < kBarPFull + 2) || (i >= kBarOEmpty && i < kBarOEmpty + 2) ||
                             i == kBarPeerData;
             const bool rot = i >= kBarReady && i < kBarReady + kSlots;
-            mbar_init(bar(i), wg ? 128u : rot ? (uint32_t)kRotThreads : 1u);
+            const bool geo_empty = i >= kBarGeoEmpty && i < kBarGeoEmpty + 2;
+            mbar_init(bar(i), wg ? 128u : rot ? (uint32_t)kRotThreads : geo_empty ? geo_consumer_warps<kG>() : 1u);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -620,6 +753,8 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         prefetch_tmap(&tmq);
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
+        if (a.out_tma)
+            prefetch_tmap(&tmo);
         if constexpr (kG) {
             prefetch_tmap(&tmpk);
             prefetch_tmap(&tmpv);
@@ -655,20 +790,27 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float sc = a.scale_log2;
         const int G = a.n_q_heads / a.n_kv_heads;
-        int s_cnt = 0, o_cnt = 0;
+        int s_cnt = 0, o_cnt = 0, gk = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-            const Item itm = item_at(a, reqs, n_blocks, it);
-            const Unit &w = itm.w;
-            const int jb = itm.jb;
-            const int nx = min(itm.je, w.n_t[x]);   // this tile's key tiles in the item: [jb, nx)
-            if (jb >= nx)
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
+            const Geo *gp = geo_wait(gk);
+            if (!gp) {
+                ok = false;
+                break;
+            }
+            // the fields the key-tile loop needs; the epilogue reads the rest
+            // from the slot afterwards (held until then: fewer live registers)
+            const int jb = gp->jb;
+            const int nx = min(gp->je, gp->n_t[x]);   // this tile's key tiles in the item: [jb, nx)
+            if (jb >= nx) {
+                geo_done(gk);
                 continue;
-            const int rr = w.row0[x] + r;          // packed row in the request
-            const bool row_ok = rr < w.m_rows;
-            const int t = row_ok ? rr / G : w.rq.q_len - 1;
+            }
+            const int rr = gp->row0[x] + r;        // packed row in the request
+            const bool row_ok = rr < gp->m_rows;
+            const int t = row_ok ? rr / G : gp->q_len - 1;
             const int g = row_ok ? rr - (rr / G) * G : 0;
-            const int pos = w.rq.prefix + t;
+            const int pos = gp->prefix + t;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = jb; j < nx; ++j) {
                 if (!mbar_wait(bar(kBarSFull + x), s_cnt & 1, abort_flag)) {
@@ -752,6 +894,9 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             }
             if (!ok)
                 break;
+            const int half = gp->half, n_tiles = gp->n_tiles, ntx = gp->n_t[x], row0x = gp->row0[x];
+            const int m_rows = gp->m_rows, q_off = gp->q_off, wl = gp->l, wh = gp->h;
+            geo_done(gk);
             // epilogue: O / l -> bf16 -> out[l][q_off + t][h*G + g][:], read from
             // TMEM 64 columns at a time (a whole row of O in registers spills)
             if (!mbar_wait(bar(kBarOFull + x), o_cnt & 1, abort_flag)) {
@@ -768,8 +913,8 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             // half of tile x through distributed shared memory, O as fp16 with a
             // power-of-two scale per row (exact to ~2^-12, below the output's bf16
             // rounding, at half the bytes of fp32).  Nothing of it touches L2.
-            const bool split2 = itm.half >= 0 && (w.n_tiles + 1) / 2 < w.n_t[x];
-            const bool merger = split2 && itm.half == x;
+            const bool split2 = half >= 0 && (n_tiles + 1) / 2 < ntx;
+            const bool merger = split2 && half == x;
             const uint32_t peer_o = sbase + kOffPeerO, peer_ml = sbase + kOffPeerML;
             if (split2 && !merger) {
                 // the partner's ring and Q tiles are free once its MMAs are done
@@ -840,8 +985,15 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             // finite positive denominator: report it (the row is written as computed)
             if (row_ok && !(l_fin > 0.f && l_fin < INFINITY))
                 atomicCAS(a.err, kDevOk, kDevBadInput);
-            const int64_t orow = row_ok ? (((int64_t)w.l * a.total_q + w.rq.q_off + t) * a.n_q_heads + w.h * G + g) * kD
-                                        : -1;
+            // this warp's 32 rows are whole tokens of the request: one TMA store
+            // per 64-column half, and the warp does not wait for global memory
+            const int wrow0 = row0x + (warp & 3) * 32;
+            const bool tma_out = a.out_tma && wrow0 + 31 < m_rows;
+            // TMA stores: the box's (head, token) coordinates; otherwise this
+            // row's output element offset (-1: no row)
+            const int64_t orow = tma_out ? (((int64_t)(wh * G) << 32) | (uint32_t)(wl * a.total_q + q_off + wrow0 / G))
+                                 : row_ok ? (((int64_t)wl * a.total_q + q_off + t) * a.n_q_heads + wh * G + g) * kD
+                                          : -1;
             __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
             const uint32_t stg = sbase + kOffStage + (uint32_t)warp * 32 * 128;
             const int wr = r & 31;
@@ -854,6 +1006,11 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 if (hh == 1) {
                     tc_fence_before();
                     mbar_arrive(bar(kBarOEmpty + x));   // O_x may now take the next unit's PV
+                }
+                if (a.out_tma) {   // the staging is free once the last TMA store has read it
+                    if (lane == 0)
+                        bulk_wait_read();
+                    __syncwarp();
                 }
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -882,51 +1039,79 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                                  pack_bf16(v[2] * inv, v[3] * inv), pack_bf16(v[4] * inv, v[5] * inv),
                                  pack_bf16(v[6] * inv, v[7] * inv));
                 }
-                __syncwarp();
+                if (tma_out) {
+                    // the staging is the box's 128B-swizzled layout: rows t * G + g
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tmo, stg, 64 * hh, (int)(orow >> 32), (int)(uint32_t)orow);
+                        bulk_commit();
+                    }
+                } else {
+                    __syncwarp();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int row = 4 * i + (lane >> 3), c = lane & 7;
-                    const int64_t base = __shfl_sync(0xffffffffu, orow, row);
-                    const uint4 v = ld_shared_v4(stg + row * 128 + ((c ^ (row & 7)) << 4));
-                    if (base >= 0)
-                        *reinterpret_cast<uint4 *>(out + base + 64 * hh + 8 * c) = v;
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = 4 * i + (lane >> 3), c = lane & 7;
+                        const int64_t base = __shfl_sync(0xffffffffu, orow, row);
+                        const uint4 v = ld_shared_v4(stg + row * 128 + ((c ^ (row & 7)) << 4));
+                        if (base >= 0)
+                            *reinterpret_cast<uint4 *>(out + base + 64 * hh + 8 * c) = v;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
+        if (a.out_tma && lane == 0)
+            bulk_wait_all();   // every output store has landed before the CTA ends
         if (!ok)
             flag_timeout(a.err, abort_flag);
     } else if (warp == 8) {
         regs_other();
         if constexpr (!kG) {
-            if (lane == 0) {
-                int tt = 0, nq = 0;
-                bool ok = true;
-                for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-                    const Item itm = item_at(a, reqs, n_blocks, it);
-                    const Unit &w = itm.w;
-                    if (itm.je <= itm.jb)
-                        continue;
-                    if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const int nqt = w.n_t[1] > 0 ? 2 : 1;
-                    mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
-                    for (int x = 0; x < nqt; ++x) {
-                        const uint32_t dst = sbase + kOffQ + x * kTileBytes;
-                        tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
-                        tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
-                    }
-                    ++nq;
-                    if (it + (int)gridDim.x < n_items) {
-                        const Unit wn = item_at(a, reqs, n_blocks, it + gridDim.x).w;
-                        for (int x = 0; x < (wn.n_t[1] > 0 ? 2 : 1); ++x) {
-                            tma_prefetch_2d(&tmq, 0, wn.q_row0 + x * kTileM);
-                            tma_prefetch_2d(&tmq, 64, wn.q_row0 + x * kTileM);
+            // ====== stitched producer: the whole warp computes each item's
+            // geometry (request table in registers), lane 0 waits and issues ======
+            int tt = 0, nq = 0, gk = 0;
+            bool ok = true;
+            ReqRegs rr;
+            rr.load(a, reqs, lane);
+            Item nxt;
+            if ((int)blockIdx.x < n_items) {
+                nxt = item_at(a, reqs, n_blocks, blockIdx.x, &rr, lane);
+                if (lane == 0)
+                    ok = geo_put(0, nxt);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
+                const Item itm = nxt;
+                const Unit &w = itm.w;
+                // the next item's geometry now, while this item's first loads wait
+                // for ring slots -- except on the first item, whose loads go
+                // first (nothing else can start before them)
+                const bool more = it + (int)gridDim.x < n_items;
+                if (more && gk > 0)
+                    nxt = item_at(a, reqs, n_blocks, it + gridDim.x, &rr, lane);
+                if (itm.je > itm.jb && lane == 0) {
+                    // K_0 and V_0 first (their ring slots free up a tile before the
+                    // previous item ends), then Q (its buffer frees only once the
+                    // previous item's last S MMAs are done), then the other tiles
+                    const int n_loads = 2 * (itm.je - itm.jb);
+                    for (int i = 0; i <= n_loads && ok; ++i) {
+                        if (i == 2) {
+                            if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            const int nqt = w.n_t[1] > 0 ? 2 : 1;
+                            mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
+                            for (int x = 0; x < nqt; ++x) {
+                                const uint32_t dst = sbase + kOffQ + x * kTileBytes;
+                                tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
+                                tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
+                            }
+                            ++nq;
                         }
-                    }
-                    for (int i = 0; i < 2 * (itm.je - itm.jb); ++i, ++tt) {
+                        if (i == n_loads)
+                            break;
                         const int slot = tt % kSlots;
                         if (tt >= kSlots && !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag)) {
                             ok = false;
@@ -938,8 +1123,31 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                         mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
                         tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
                         tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
+                        ++tt;
                     }
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                tt = __shfl_sync(0xffffffffu, tt, 0);
+                nq = __shfl_sync(0xffffffffu, nq, 0);
+                // the next item's geometry, published for the other roles; its Q
+                // brought into L2 ahead of its load (the K/V tiles are not: their
+                // loads are issued a tile ahead anyway, and a prefetch costs the
+                // SM's TMA unit as much time as the load that follows it)
+                if (ok && more) {
+                    if (gk == 0)
+                        nxt = item_at(a, reqs, n_blocks, it + gridDim.x, &rr, lane);
+                    if (lane == 0) {
+                        ok = geo_put(gk + 1, nxt);
+                        if (ok && nxt.je > nxt.jb)
+                            for (int x = 0; x < (nxt.w.n_t[1] > 0 ? 2 : 1); ++x) {
+                                tma_prefetch_2d(&tmq, 0, nxt.w.q_row0 + x * kTileM);
+                                tma_prefetch_2d(&tmq, 64, nxt.w.q_row0 + x * kTileM);
+                            }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                }
+            }
+            if (lane == 0) {
                 if (!ok)
                     flag_timeout(a.err, abort_flag);
                 // drain: every issued copy lands before the CTA leaves
@@ -956,16 +1164,44 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             // ====== gathering producer: Q as above (lane 0); each K/V tile is 128
             // stitched rows resolved through the span table, lane i loading rows
             // 4i..4i+3 with one gather4 per 64-column panel ======
-            int tt = 0, nq = 0;
+            int tt = 0, nq = 0, gk = 0;
             bool ok = true;
             const DevSpan *spans = g.spans ? g.spans : st.spans;
             int *meta = reinterpret_cast<int *>(smem + kOffMeta);
             const int64_t e_rows = (int64_t)a.n_layers * a.n_kv_heads * g.entry_len;   // pool rows per entry
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-                const Item itm = item_at(a, reqs, n_blocks, it);
+            ReqRegs rr;
+            rr.load(a, reqs, lane);
+            Item nxt;
+            if ((int)blockIdx.x < n_items) {
+                nxt = item_at(a, reqs, n_blocks, blockIdx.x, &rr, lane);
+                if (lane == 0)
+                    ok = geo_put(0, nxt);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
+                const Item itm = nxt;
                 const Unit &w = itm.w;
-                if (itm.je <= itm.jb)
+                // the next item's geometry once this item's loads are issued
+                // (published for the other roles, its Q brought into L2)
+                auto publish_next = [&]() -> bool {
+                    if (it + (int)gridDim.x >= n_items)
+                        return true;
+                    nxt = item_at(a, reqs, n_blocks, it + gridDim.x, &rr, lane);
+                    bool okp = true;
+                    if (lane == 0) {
+                        okp = geo_put(gk + 1, nxt);
+                        if (okp && nxt.je > nxt.jb)
+                            for (int x = 0; x < (nxt.w.n_t[1] > 0 ? 2 : 1); ++x) {
+                                tma_prefetch_2d(&tmq, 0, nxt.w.q_row0 + x * kTileM);
+                                tma_prefetch_2d(&tmq, 64, nxt.w.q_row0 + x * kTileM);
+                            }
+                    }
+                    return __shfl_sync(0xffffffffu, okp, 0);
+                };
+                if (itm.je <= itm.jb) {
+                    ok = publish_next();
                     continue;
+                }
                 if (lane == 0) {
                     if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
                         ok = false;
@@ -976,13 +1212,6 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                             const uint32_t dst = sbase + kOffQ + x * kTileBytes;
                             tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
                             tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
-                        }
-                        if (it + (int)gridDim.x < n_items) {
-                            const Unit wn = item_at(a, reqs, n_blocks, it + gridDim.x).w;
-                            for (int x = 0; x < (wn.n_t[1] > 0 ? 2 : 1); ++x) {
-                                tma_prefetch_2d(&tmq, 0, wn.q_row0 + x * kTileM);
-                                tma_prefetch_2d(&tmq, 64, wn.q_row0 + x * kTileM);
-                            }
                         }
                     }
                 }
@@ -1059,6 +1288,8 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                         tma_gather4(dst + kPanelBytes, map, 64, rows, bar(kBarFull + slot));
                     }
                 }
+                if (ok)
+                    ok = publish_next();
             }
             if (!ok)
                 flag_timeout(a.err, abort_flag);
@@ -1110,14 +1341,20 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 tc_fence_after();
                 return true;
             };
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-                const Item itm = item_at(a, reqs, n_blocks, it);
-                const Unit &w = itm.w;
-                const int jb = itm.jb, je = itm.je;
+            int gk = 0;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
+                const Geo *gp = geo_wait(gk);
+                if (!gp) {
+                    ok = false;
+                    break;
+                }
+                const int jb = gp->jb, je = gp->je, half = gp->half, n_tiles = gp->n_tiles;
+                const int nt0 = gp->n_t[0], nt1 = gp->n_t[1];
+                geo_done(gk);
                 if (je <= jb)
                     continue;
-                const int jx[2] = {min(je, w.n_t[0]), min(je, w.n_t[1])};   // tile x's key tiles: [jb, jx[x])
-                peer_wait = itm.half >= 0 && (w.n_tiles + 1) / 2 < w.n_t[itm.half] ? itm.half : -1;
+                const int jx[2] = {min(je, nt0), min(je, nt1)};   // tile x's key tiles: [jb, jx[x])
+                peer_wait = half >= 0 && (n_tiles + 1) / 2 < (half ? nt1 : nt0) ? half : -1;
                 if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag) || !wait_kv(tt)) {
                     ok = false;
                     break;
@@ -1214,18 +1451,24 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         // so the tables are read again only where the delta changes
         int d_cur = kNoRotation;
         float c[8], sn[8];
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        int gk = 0;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
             // the few fields the loop needs, as scalars (the item struct would
             // otherwise be read from the stack frame on every row)
             int jb, je, prefix, n_valid;
             int64_t kv_row0;
             {
-                const Item itm = item_at(a, reqs, n_blocks, it);
-                jb = itm.jb;
-                je = itm.je;
-                prefix = itm.w.rq.prefix;
-                n_valid = itm.w.n_valid;
-                kv_row0 = itm.w.kv_row0;
+                const Geo *gp = geo_wait(gk);
+                if (!gp) {
+                    ok = false;
+                    break;
+                }
+                jb = gp->jb;
+                je = gp->je;
+                prefix = gp->prefix;
+                n_valid = gp->n_valid;
+                kv_row0 = gp->kv_row0;
+                geo_done(gk);
             }
             for (int j = jb; j < je; ++j, tt += 2) {
                 const int sk = tt % kSlots, sv = (tt + 1) % kSlots;
@@ -1428,7 +1671,8 @@ static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool
                               kG ? *static_cast<const CUtensorMap *>(ta.tmap_pv) : no_map,
                               kG ? *static_cast<const CUtensorMap *>(ta.tmap_bk) : no_map,
                               kG ? *static_cast<const CUtensorMap *>(ta.tmap_bv) : no_map, kG ? ta.g : no_gather,
-                              kG && ta.st ? *ta.st : no_spans);
+                              kG && ta.st ? *ta.st : no_spans,
+                              ta.base.out_tma ? *static_cast<const CUtensorMap *>(ta.tmap_out) : no_map);
 }
 
 cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)

@@ -204,6 +204,11 @@ struct AttnArgs {
     // two-CTA clusters
     int32_t n_full;
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
+    // tensor-core kernel: the output goes out through TMA tensor stores (the
+    // tmap_out parameter), a warp's 32 rows = 32 / G whole tokens of the G
+    // query heads of one kv head; set when G is a power of two and `out` is
+    // device memory
+    int32_t out_tma;
 };
 
 struct QueryPrologueArgs {
@@ -263,6 +268,7 @@ struct TcAttnArgs {
     const void *tmap_bv;
     GatherArgs g;
     const SpanTable *st;
+    const void *tmap_out;       // out as [L*T][H_q][D] with a (64, G, 32 / G) box (base.out_tma)
 };
 // `pdl`: the kernel before it on the stream is the assemble kernel of the
 // same prefill (which it may overlap: it reads only the caller's inputs and
