@@ -252,6 +252,68 @@ def workload_config(args) -> W.Config:
     return cfg
 
 
+def decode_timing(wl, cfg, dev, steps, warmup, flush):
+    """A decode step after the prefill: a query token per request at row (and
+    position) P_b + Lq, attending to rows 0..P_b + Lq; one kvr_query_attention
+    call.  Timed two ways: `us_per_step` over consecutive steps (a decode
+    loop: the host enqueues ahead, each step reads every cache block, and the
+    step's K/V bytes exceed the L2 on every workload here), and `us_isolated`
+    for one call after an L2 flush, launch latency included."""
+    import torch
+    stream = torch.cuda.current_stream()
+    B = len(wl.reqs)
+    gdec = torch.Generator(device=dev)
+    gdec.manual_seed(cfg.seed + 7)
+    L, Hq, Hkv, Dh = cfg.n_layers, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    q1 = torch.randn((L, B, Hq, Dh), generator=gdec, device=dev).to(wl.t.q.dtype)
+    k1 = torch.randn((L, B, Hkv, Dh), generator=gdec, device=dev).to(wl.t.q.dtype)
+    v1 = torch.randn((L, B, Hkv, Dh), generator=gdec, device=dev).to(wl.t.q.dtype)
+    o1 = torch.empty_like(q1)
+    n_dec = (wl.prefix + cfg.query_len).astype(np.int32)
+    q1_off = np.arange(B + 1, dtype=np.int32)
+
+    def step():
+        wl.pool.query_attention(wl.cache_offsets, n_dec, q1_off, q1, k1, v1, wl.cache_k, wl.cache_v, o1)
+
+    wl.step()
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    n_d = max(20, min(steps, 500))
+    # consecutive steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush()
+    e0.record(stream)
+    for _ in range(n_d):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    loop_ms = e0.elapsed_time(e1) / n_d
+    # isolated calls
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_d)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_d)]
+    for k in range(n_d):
+        flush()
+        d0[k].record(stream)
+        step()
+        d1[k].record(stream)
+    torch.cuda.synchronize()
+    wl.pool.check()
+    iso_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(d0, d1))
+    elt = 2 if cfg.dtype == "bf16" else 4
+    dec_bytes = int((n_dec.astype(np.int64) + 1).sum()) * L * Hkv * Dh * elt * 2
+    hbm = peaks()["hbm_gbs"]
+    return {"workload": cfg.name, "us_per_step": round(loop_ms * 1e3, 2), "steps": n_d, "kv_bytes": dec_bytes,
+            "gbs": round(dec_bytes / (loop_ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(dec_bytes / (loop_ms * 1e-3) / 1e9 / hbm, 4),
+            "us_isolated": round(iso_ms * 1e3, 2),
+            "frac_hbm_isolated": round(dec_bytes / (iso_ms * 1e-3) / 1e9 / hbm, 4),
+            "what": "kvr_query_attention with one token per request (append at P_b + Lq, attend to all rows); "
+                    "bytes = K and V rows read once; us_per_step: consecutive steps (no flush: the step reads more "
+                    "than the L2 holds), us_isolated: one call after an L2 flush"}
+
+
 LATENCY_CONFIG = 2
 LATENCY_REPS = 200
 
@@ -307,6 +369,7 @@ def latency_case(reps: int, warmup: int, dev, flush, variant: str = "default"):
                         "traffic": ncu_traffic("k_assemble", cfg.name)},
            "what": "one kvr_prefill call (stitch + query attention) for one request, device time per call, "
                    "L2 flushed before each; kernel durations from the timing hook (serialized)"}
+    res["decode"] = decode_timing(wl, cfg, dev, reps, warmup, flush)
     wl.pool.close()
     return res
 
@@ -397,41 +460,8 @@ def run_kvr(args):
                   "what": "kvr_prefill with KVR_PREFILL_SKIP_PREFIX_CACHE: the attention gathers and "
                           "re-rotates the prefix from the pool, no stitched cache written"}
 
-    # ---- one decode step after the prefill: a query token per request at
-    # row (and position) P_b + Lq, attending to rows 0..P_b + Lq ----
-    B = len(wl.reqs)
-    gdec = torch.Generator(device=dev)
-    gdec.manual_seed(cfg.seed + 7)
-    L, Hq, Hkv, Dh = cfg.n_layers, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
-    q1 = torch.randn((L, B, Hq, Dh), generator=gdec, device=dev).to(wl.t.q.dtype)
-    k1 = torch.randn((L, B, Hkv, Dh), generator=gdec, device=dev).to(wl.t.q.dtype)
-    v1 = torch.randn((L, B, Hkv, Dh), generator=gdec, device=dev).to(wl.t.q.dtype)
-    o1 = torch.empty_like(q1)
-    n_dec = (wl.prefix + cfg.query_len).astype(np.int32)
-    q1_off = np.arange(B + 1, dtype=np.int32)
-    n_d = min(args.steps, 500)
-    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_d)]
-    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_d)]
-    wl.step()
-    for _ in range(args.warmup):
-        flush()
-        wl.pool.query_attention(wl.cache_offsets, n_dec, q1_off, q1, k1, v1, wl.cache_k, wl.cache_v, o1)
-    torch.cuda.synchronize()
-    for k in range(n_d):
-        flush()
-        d0[k].record(stream)
-        wl.pool.query_attention(wl.cache_offsets, n_dec, q1_off, q1, k1, v1, wl.cache_k, wl.cache_v, o1)
-        d1[k].record(stream)
-    torch.cuda.synchronize()
-    wl.pool.check()
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(d0, d1))
-    elt = 2 if cfg.dtype == "bf16" else 4
-    dec_bytes = int((n_dec.astype(np.int64) + 1).sum()) * L * Hkv * Dh * elt * 2
-    decode = {"us_per_step": round(dec_ms * 1e3, 2), "steps": n_d, "kv_bytes": dec_bytes,
-              "gbs": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
-              "frac_hbm": round(dec_bytes / (dec_ms * 1e-3) / 1e9 / peaks()["hbm_gbs"], 4),
-              "what": "kvr_query_attention with one token per request (append at P_b + Lq, attend to "
-                      "all rows); bytes = K and V rows read once"}
+    # ---- one decode step after the prefill ----
+    decode = decode_timing(wl, cfg, dev, args.steps, args.warmup, flush)
 
     # ---- the stitch from a pool kept in pinned host memory (read over the
     # CPU-GPU link through its unified address) ----
