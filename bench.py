@@ -314,6 +314,61 @@ def decode_timing(wl, cfg, dev, steps, warmup, flush):
                     "than the L2 holds), us_isolated: one call after an L2 flush"}
 
 
+def host_pool_timing(wl, cfg, steps, warmup, flush):
+    """The same batch from a copy of the pool in pinned host memory (the GPU
+    reads it over the CPU-GPU link through its unified address): the stitch
+    alone (kvr_assemble), the query attention alone (kvr_query_attention, on
+    the stitched cache), and kvr_prefill, which stitches by layer groups on a
+    second stream so that each group's attention overlaps the next group's
+    stitch.  Skipped for pools above HOST_POOL_MAX_BYTES."""
+    import torch
+    from rag_precomputed_kv_gb300 import kvr as K
+    pool_bytes = 2 * wl.t.pool_k.numel() * wl.t.pool_k.element_size()
+    if pool_bytes > HOST_POOL_MAX_BYTES:
+        return {"skipped": f"pool of {pool_bytes / 2**30:.1f} GiB: not copied to pinned host memory "
+                           f"(limit {HOST_POOL_MAX_BYTES / 2**30:.0f} GiB)"}
+    try:
+        hk, hv = wl.t.pool_k.cpu().pin_memory(), wl.t.pool_v.cpu().pin_memory()
+    except RuntimeError as e:
+        return {"skipped": f"pinned host copy failed: {e}"}
+    stream = torch.cuda.current_stream()
+    hp = K.Pool(hk, hv, cfg.n_q_heads, cfg.rope_theta, keys_unrotated=wl.variant == "unrotated",
+                rope_interleaved=wl.variant == "interleaved")
+    n_h = max(5, min(steps, 100))
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
+        for k in range(n_h):
+            flush()
+            e0[k].record(stream)
+            fn()
+            e1[k].record(stream)
+        torch.cuda.synchronize()
+        hp.check()
+        return statistics.mean(a.elapsed_time(b) for a, b in zip(e0, e1))
+
+    asm = lambda: hp.assemble(wl.span_offsets, wl.spans, wl.cache_offsets, wl.cache_k, wl.cache_v,
+                              locals_=wl.locals, composite=wl.composite)
+    att = lambda: hp.query_attention(wl.cache_offsets, wl.plen, wl.q_offsets, wl.t.q, wl.t.kq, wl.t.vq,
+                                     wl.cache_k, wl.cache_v, wl.out)
+    pre = lambda: hp.prefill(wl.span_offsets, wl.spans, wl.cache_offsets, wl.cache_k, wl.cache_v, wl.q_offsets,
+                             wl.t.q, wl.t.kq, wl.t.vq, wl.out, locals_=wl.locals, composite=wl.composite)
+    a_ms, q_ms, p_ms = timed(asm), timed(att), timed(pre)
+    host_read = W.assemble_bytes(cfg, wl.reqs) // 2
+    hp.close()
+    return {"workload": cfg.name, "assemble_us": round(a_ms * 1e3, 2), "query_attention_us": round(q_ms * 1e3, 2),
+            "serial_sum_us": round((a_ms + q_ms) * 1e3, 2), "prefill_us": round(p_ms * 1e3, 2), "steps": n_h,
+            "host_read_gbs": round(host_read / (a_ms * 1e-3) / 1e9, 1),
+            "what": "pool in pinned host memory, K/V rows read over the CPU-GPU link: kvr_assemble alone, "
+                    "kvr_query_attention alone, and kvr_prefill (layer-group stitch on a second stream, each "
+                    "group's attention beside the next group's stitch)"}
+
+
 LATENCY_CONFIG = 2
 LATENCY_REPS = 200
 
@@ -370,6 +425,7 @@ def latency_case(reps: int, warmup: int, dev, flush, variant: str = "default"):
            "what": "one kvr_prefill call (stitch + query attention) for one request, device time per call, "
                    "L2 flushed before each; kernel durations from the timing hook (serialized)"}
     res["decode"] = decode_timing(wl, cfg, dev, reps, warmup, flush)
+    res["host_pool"] = host_pool_timing(wl, cfg, reps, warmup, flush)
     wl.pool.close()
     return res
 
@@ -463,43 +519,8 @@ def run_kvr(args):
     # ---- one decode step after the prefill ----
     decode = decode_timing(wl, cfg, dev, args.steps, args.warmup, flush)
 
-    # ---- the stitch from a pool kept in pinned host memory (read over the
-    # CPU-GPU link through its unified address) ----
-    host_pool = None
-    hk = hv = None
-    pool_bytes = 2 * wl.t.pool_k.numel() * wl.t.pool_k.element_size()
-    if pool_bytes > HOST_POOL_MAX_BYTES:
-        host_pool = {"skipped": f"pool of {pool_bytes / 2**30:.1f} GiB: not copied to pinned host memory "
-                                f"(limit {HOST_POOL_MAX_BYTES / 2**30:.0f} GiB)"}
-    else:
-        try:
-            hk, hv = wl.t.pool_k.cpu().pin_memory(), wl.t.pool_v.cpu().pin_memory()
-        except RuntimeError:
-            hk = hv = None
-    if hk is not None:
-        hp = K.Pool(hk, hv, cfg.n_q_heads, cfg.rope_theta, keys_unrotated=wl.variant == "unrotated",
-                    rope_interleaved=wl.variant == "interleaved")
-        n_h = min(args.steps, 200)
-        h0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
-        h1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_h)]
-        for k in range(args.warmup + n_h):
-            flush()
-            if k >= args.warmup:
-                h0[k - args.warmup].record(stream)
-            hp.assemble(wl.span_offsets, wl.spans, wl.cache_offsets, wl.cache_k, wl.cache_v,
-                        locals_=wl.locals, composite=wl.composite)
-            if k >= args.warmup:
-                h1[k - args.warmup].record(stream)
-        torch.cuda.synchronize()
-        hp.check()
-        h_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(h0, h1))
-        host_read = asm_bytes_of(cfg, wl) // 2
-        host_pool = {"assemble_us": round(h_ms * 1e3, 2), "steps": n_h,
-                     "host_read_gbs": round(host_read / (h_ms * 1e-3) / 1e9, 1),
-                     "what": "kvr_assemble from a pool in pinned host memory: K/V rows read over the "
-                             "CPU-GPU link, stitched cache written to HBM"}
-        hp.close()
-        del hk, hv
+    # ---- the prefill from a pool kept in pinned host memory ----
+    host_pool = host_pool_timing(wl, cfg, args.steps, args.warmup, flush)
 
     # ---- end to end through the public API with host buffers ----
     # The batch is stitched with one kvr_assemble; its requests' query-side

@@ -61,6 +61,11 @@ namespace {
 // slot's previous call has not yet run (kSlots such calls queued ahead).
 constexpr int kSlots = 8;
 
+// Host-pool prefill pipeline: layer groups, and the CTAs its stitch keeps
+// (the attention runs on the other SMs meanwhile).
+constexpr int kMaxLayerParts = 8;
+constexpr int kHostStitchCtas = 64;
+
 // Scoped NVTX range (a profiler's timeline shows which library call and which
 // kernel each stretch of host time enqueued; nothing without a profiler).
 struct NvtxRange {
@@ -124,6 +129,13 @@ struct kvr_pool {
     size_t dec_cnt_cap = 0;      // blocks
     cudaEvent_t dec_done = nullptr;
     bool dec_used = false;
+    // a pool in pinned host memory: kvr_prefill stitches it by layer groups on
+    // a second stream, each group's attention overlapping the next group's
+    // stitch (which reads over the CPU-GPU link)
+    bool host_pool = false;
+    cudaStream_t side = nullptr;
+    cudaEvent_t side_start = nullptr;
+    cudaEvent_t part_ev[kMaxLayerParts] = {};
     cudaEvent_t timing[6] = {};  // optional kernel timing events (caller-owned)
     bool timed = false;
 
@@ -311,6 +323,11 @@ static kvr_status ensure_device(kvr_pool *p)
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
         p->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, p->d.k) == cudaSuccess)
+        p->host_pool = pa.type == cudaMemoryTypeHost;
+    else
+        cudaGetLastError();
     p->ready = true;
     return KVR_OK;
 }
@@ -348,6 +365,15 @@ extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
         cudaEventSynchronize(p->dec_done);
         cudaEventDestroy(p->dec_done);
     }
+    if (p->side) {
+        cudaStreamSynchronize(p->side);
+        cudaStreamDestroy(p->side);
+    }
+    if (p->side_start)
+        cudaEventDestroy(p->side_start);
+    for (cudaEvent_t e : p->part_ev)
+        if (e)
+            cudaEventDestroy(e);
     if (p->dec_ws)
         cudaFree(p->dec_ws);
     if (p->dec_cnt)
@@ -756,6 +782,7 @@ struct QaPlan {
     std::vector<DevLocal> al;
     bool tc = false, inl = false;
     bool dec_stream = false;     // decode step over all SMs (k_decode_stream)
+    int32_t parts = 1;           // layer groups of a host-pool prefill (attention per group)
     int64_t dec_tiles = 0;
     CUtensorMap mq, mk, mv, mo;
     ReqTable rt_inl;
@@ -900,7 +927,7 @@ static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
         int64_t u0 = 0;
         for (DevReq &r : pl.rq) {
             r.unit0 = (int32_t)u0;
-            u0 += ((int64_t)(Hq / Hkv) * r.q_len + 255) / 256 * LH;
+            u0 += ((int64_t)(Hq / Hkv) * r.q_len + 255) / 256 * (LH / pl.parts);
         }
         // a decode step over fewer blocks than two per SM spreads its 128-key
         // tiles over every SM (k_decode_stream); the request table holds each
@@ -992,14 +1019,21 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
     const int D = p->d.head_dim;
     cudaError_t e;
     if (pl.tc) {
-        TcAttnArgs ta{pl.at, &rt, &pl.mq, &pl.mk, &pl.mv, pl.m_blocks, p->n_sms};
+        // a host-pool prefill in layer groups, stitched last group first: the
+        // attention of group g runs on the SMs the stitch leaves, beside the
+        // stitch of group g - 1, once the stitch of group g is done
+        const int n_sms = pl.parts > 1 ? p->n_sms - kHostStitchCtas : p->n_sms;
+        const int lh_part = p->d.n_layers * p->d.n_kv_heads / pl.parts;
+        TcAttnArgs ta{pl.at, &rt, &pl.mq, &pl.mk, &pl.mv, pl.m_blocks, n_sms};
         ta.tmap_out = &pl.mo;
+        if (pl.parts > 1)
+            ta.base.lh_count = lh_part;
         // the last wave's units split in two halves of their keys when two
         // halves of each fit one wave and the grid can run as two-CTA clusters
-        const int64_t units = (int64_t)pl.m_blocks * p->d.n_layers * p->d.n_kv_heads;
-        const int64_t tail = units % p->n_sms;
+        const int64_t units = (int64_t)pl.m_blocks * lh_part;
+        const int64_t tail = units % n_sms;
         ta.base.n_full = (int32_t)units;
-        if (tail > 0 && 2 * tail <= p->n_sms && attention_tc_pairs_fit(p->n_sms, gl != nullptr))
+        if (tail > 0 && 2 * tail <= n_sms && attention_tc_pairs_fit(n_sms, gl != nullptr))
             ta.base.n_full = (int32_t)(units - tail);
         QueryPrologueArgs qp{pl.at.reqs, p->rope, pl.q, pl.kq, pl.vq, pl.cache_k, pl.cache_v, p->q_rot,
                              p->d.n_layers, p->d.n_q_heads, p->d.n_kv_heads, pl.T, pl.max_lq, pl.batch,
@@ -1034,18 +1068,29 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
             p->mark(5, s);
         } else if (e == cudaSuccess) {
             NvtxRange r(gl ? "kvr.k_attention_tc_gathering" : "kvr.k_attention_tc");
-            if (gl) {
-                ta.gather = true;
-                ta.tmap_pk = &gl->mpk;
-                ta.tmap_pv = &gl->mpv;
-                ta.tmap_bk = &gl->mbk;
-                ta.tmap_bv = &gl->mbv;
-                ta.g = gl->g;
-                ta.st = gl->inl ? &gl->st : nullptr;
+            if (pl.parts > 1) {
+                p->mark(4, s);
+                for (int g = pl.parts - 1; g >= 0 && e == cudaSuccess; --g) {
+                    if ((e = cudaStreamWaitEvent(s, p->part_ev[g], 0)) != cudaSuccess)
+                        break;
+                    ta.base.lh_base = g * lh_part;
+                    e = launch_attention_tc(ta, false, s);
+                }
+                p->mark(5, s);
+            } else {
+                if (gl) {
+                    ta.gather = true;
+                    ta.tmap_pk = &gl->mpk;
+                    ta.tmap_pv = &gl->mpv;
+                    ta.tmap_bk = &gl->mbk;
+                    ta.tmap_bv = &gl->mbv;
+                    ta.g = gl->g;
+                    ta.st = gl->inl ? &gl->st : nullptr;
+                }
+                p->mark(4, s);
+                e = launch_attention_tc(ta, !p->timed, s);
+                p->mark(5, s);
             }
-            p->mark(4, s);
-            e = launch_attention_tc(ta, !p->timed, s);
-            p->mark(5, s);
         }
         cudaEventRecord(p->q_rot_done, s);
         p->q_rot_used = true;
@@ -1182,11 +1227,67 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
             cudaEventRecord(ap.slot->done, s);
         return st;
     }
+    // a pool in pinned host memory: layer groups, whose stitch (bound by the
+    // CPU-GPU link, on a bounded grid and a second stream) overlaps the
+    // previous group's attention
+    const int L = p->d.n_layers;
+    if (p->host_pool && stitch && qp.max_lq > 1 && use_tensor_cores(*p))
+        for (int n = kMaxLayerParts; n > 1; --n)
+            if (L % n == 0) {
+                qp.parts = n;
+                break;
+            }
     // uploads and stream waits first, so that the kernels follow one another
     // on the stream with nothing in between
     if ((stitch && (st = asm_stage(p, ap, s)) != KVR_OK) ||
         (qp.T > 0 && (st = qa_stage(p, qp, s)) != KVR_OK))
         return st;
+    if (qp.parts > 1) {
+        cudaError_t e = cudaSuccess;
+        if (!p->side && (e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "host-pool stitch stream");
+        if (!p->side_start && (e = cudaEventCreateWithFlags(&p->side_start, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "host-pool stitch event");
+        for (int g = 0; g < qp.parts; ++g)
+            if (!p->part_ev[g] && (e = cudaEventCreateWithFlags(&p->part_ev[g], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "host-pool stitch event");
+        // the stitch stream starts after everything the caller's stream holds
+        if ((e = cudaEventRecord(p->side_start, s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(p->side, p->side_start, 0)) != cudaSuccess)
+            return cuda_fail(e, "host-pool stitch ordering");
+        // The last 128-key tile of a request's last block reaches into the
+        // first rows of the next request's first block, which the last stitch
+        // group (the first layers) writes: until then those prefix rows' values
+        // must be finite, since a masked key has weight 0 but 0 x NaN is NaN.
+        const int LHn = L * p->d.n_kv_heads;
+        const size_t row_bytes = (size_t)p->d.head_dim * p->elt();
+        for (int b = 1; b < batch && e == cudaSuccess; ++b) {
+            const int64_t rows = std::min<int64_t>(ap.plen[b], 128);
+            if (rows > 0)
+                e = cudaMemsetAsync(static_cast<char *>(cache_v) + (size_t)cache_offsets[b] * LHn * row_bytes, 0,
+                                    (size_t)rows * row_bytes, p->side);
+        }
+        const int lh_part = LHn / qp.parts;
+        for (int g = qp.parts - 1; g >= 0 && e == cudaSuccess; --g) {
+            NvtxRange r("kvr.k_assemble_loop");
+            AssembleArgs a = ap.a;
+            a.lh_begin = g * lh_part;
+            a.lh_count = lh_part;
+            a.max_ctas = kHostStitchCtas;
+            if ((e = launch_assemble(a, p->d.dtype, p->d.head_dim, (int)ap.ds.size(), p->side,
+                                     ap.inl ? &ap.tab : nullptr)) == cudaSuccess)
+                e = cudaEventRecord(p->part_ev[g], p->side);
+        }
+        if (e != cudaSuccess) {
+            if (ap.slot)
+                cudaEventRecord(ap.slot->done, s);
+            return cuda_fail(e, "host-pool stitch launch");
+        }
+        st = qa_launch(p, qp, s, false);
+        if (ap.slot)   // after the last group's attention, which waited for every stitch group
+            cudaEventRecord(ap.slot->done, s);
+        return st;
+    }
     if (stitch && (st = asm_launch(p, ap, s, false)) != KVR_OK) {
         if (ap.slot)
             cudaEventRecord(ap.slot->done, s);

@@ -15,6 +15,8 @@
 // issues 16-byte loads/stores over whole 128-byte lines.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kvr_internal.cuh"
 
 namespace kvr {
@@ -118,7 +120,7 @@ constexpr int kAssembleThreads = 256;
 // [j*E, j*E+E) and their RoPE partners [D/2 + j*E, D/2 + j*E + E).
 template <typename T, int D>
 __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSpan *spans,
-                                              const DevLocal *locals)
+                                              const DevLocal *locals, int span_i, int grp, int n_grp)
 {
     constexpr int H2 = D / 2;
     constexpr int E = Vec<T>::E;
@@ -132,7 +134,7 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
     // the next kernel (the query prologue) touches none of this kernel's
     // rows: it may start alongside
     pdl_launch_dependents();
-    const DevSpan sp = spans[blockIdx.x];
+    const DevSpan sp = spans[span_i];
     const int j = threadIdx.x % TPR;
 
     // this thread's E (cos, sin) pairs for the span's rotation
@@ -163,11 +165,11 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
     T *ck = static_cast<T *>(a.cache_k);
     T *cv = static_cast<T *>(a.cache_v);
 
-    const int LH = a.n_layers * a.n_heads;
+    const int lh_end = a.lh_count > 0 ? a.lh_begin + a.lh_count : a.n_layers * a.n_heads;
     // last (layer, kv-head) groups first: what the kernel writes last stays in
     // L2, and the attention kernel that follows starts on the first groups
-    const int u0 = (gridDim.y - 1 - blockIdx.y) * a.upc;
-    const int nu = min(a.upc, LH - u0);
+    const int u0 = a.lh_begin + (n_grp - 1 - grp) * a.upc;
+    const int nu = min(a.upc, lh_end - u0);
     const int total = nu * sp.len;
 
     for (int r0 = threadIdx.x / TPR; r0 < total; r0 += 2 * RPP) {
@@ -234,7 +236,7 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
     }
 
     // position ids and source map, written once per span
-    if (blockIdx.y == 0) {
+    if (grp == 0 && a.lh_begin == 0) {
         for (int t = threadIdx.x; t < sp.len; t += kAssembleThreads) {
             if (a.pos_ids)
                 a.pos_ids[sp.flat0 + t] = sp.pos0 + t;
@@ -247,10 +249,11 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
 }
 
 // Tables in global memory (uploaded by the host).
+// One CTA per (span, unit group): blockIdx.x, blockIdx.y.
 template <typename T, int D>
 __global__ void __launch_bounds__(kAssembleThreads) k_assemble(const __grid_constant__ AssembleArgs a)
 {
-    assemble_body<T, D>(a, a.spans, a.locals);
+    assemble_body<T, D>(a, a.spans, a.locals, blockIdx.x, blockIdx.y, gridDim.y);
 }
 
 // Tables inside the kernel parameters: nothing to upload for small calls.
@@ -258,27 +261,48 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kAssembleThreads)
     k_assemble_inl(const __grid_constant__ AssembleArgs a, const __grid_constant__ AssembleTables tab)
 {
-    assemble_body<T, D>(a, tab.spans, tab.locals);
+    assemble_body<T, D>(a, tab.spans, tab.locals, blockIdx.x, blockIdx.y, gridDim.y);
+}
+
+// A bounded grid (a.max_ctas) whose CTAs take the (span, unit group) pieces
+// in turn, leaving the other SMs to a kernel that runs alongside.
+template <typename T, int D>
+__global__ void __launch_bounds__(kAssembleThreads)
+    k_assemble_loop(const __grid_constant__ AssembleArgs a, const __grid_constant__ AssembleTables tab, bool inl)
+{
+    const DevSpan *spans = inl ? tab.spans : a.spans;
+    const DevLocal *locals = inl ? tab.locals : a.locals;
+    const int lh_n = a.lh_count > 0 ? a.lh_count : a.n_layers * a.n_heads;
+    const int n_grp = (lh_n + a.upc - 1) / a.upc;
+    for (int v = blockIdx.x; v < a.n_spans * n_grp; v += gridDim.x)
+        assemble_body<T, D>(a, spans, locals, v % a.n_spans, v / a.n_spans, n_grp);
 }
 
 template <typename T, int D>
 static void launch_one(const AssembleArgs &a, dim3 grid, cudaStream_t s, const AssembleTables *inl)
 {
-    if (inl)
+    static const AssembleTables no_tables{};
+    if (a.max_ctas > 0)
+        k_assemble_loop<T, D><<<grid, kAssembleThreads, 0, s>>>(a, inl ? *inl : no_tables, inl != nullptr);
+    else if (inl)
         k_assemble_inl<T, D><<<grid, kAssembleThreads, 0, s>>>(a, *inl);
     else
         k_assemble<T, D><<<grid, kAssembleThreads, 0, s>>>(a);
 }
 
-cudaError_t launch_assemble(const AssembleArgs &a, int dtype, int head_dim, int n_spans,
+cudaError_t launch_assemble(const AssembleArgs &args, int dtype, int head_dim, int n_spans,
                             cudaStream_t s, const AssembleTables *inl)
 {
     if (n_spans == 0)
         return cudaSuccess;
     if (inl && n_spans > kInlineEntries)
         return cudaErrorInvalidValue;
-    const int LH = a.n_layers * a.n_heads;
-    dim3 grid(n_spans, (LH + a.upc - 1) / a.upc);
+    AssembleArgs a = args;
+    a.n_spans = n_spans;
+    const int lh_n = a.lh_count > 0 ? a.lh_count : a.n_layers * a.n_heads;
+    dim3 grid(n_spans, (lh_n + a.upc - 1) / a.upc);
+    if (a.max_ctas > 0)
+        grid = dim3((unsigned)std::min<int64_t>((int64_t)grid.x * grid.y, a.max_ctas), 1);
     if (dtype == KVR_DTYPE_BF16 && head_dim == 128)
         launch_one<__nv_bfloat16, 128>(a, grid, s, inl);
     else if (dtype == KVR_DTYPE_BF16 && head_dim == 64)

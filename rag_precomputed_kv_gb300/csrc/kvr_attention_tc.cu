@@ -547,8 +547,9 @@ __device__ __forceinline__ Unit unit_geometry(const AttnArgs &a, const DevReq &r
     const int G = a.n_q_heads / a.n_kv_heads;
     const int nb = (G * w.rq.q_len + 2 * kTileM - 1) / (2 * kTileM);   // 256-row blocks of the request
     const int local = u - w.rq.unit0;
-    w.lh = local / nb;
-    const int mb = local - w.lh * nb;
+    const int lh_i = local / nb;           // within the kernel's (layer, kv-head) slice
+    const int mb = local - lh_i * nb;
+    w.lh = a.lh_base + lh_i;
     w.l = w.lh / a.n_kv_heads;
     w.h = w.lh - w.l * a.n_kv_heads;
     w.m_rows = G * w.rq.q_len;
@@ -711,7 +712,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n_units = n_blocks * a.n_layers * a.n_kv_heads;
+    const int n_units = n_blocks * (a.lh_count > 0 ? a.lh_count : a.n_layers * a.n_kv_heads);
     const int n_items = 2 * n_units - a.n_full;
 
     // geometry of this CTA's k-th item: slot k & 1 of the shared-memory ring
@@ -1680,7 +1681,8 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
 {
     if (ta.n_m_blocks == 0)
         return cudaSuccess;
-    const int64_t units = (int64_t)ta.n_m_blocks * ta.base.n_layers * ta.base.n_kv_heads;
+    const int64_t units = (int64_t)ta.n_m_blocks *
+                          (ta.base.lh_count > 0 ? ta.base.lh_count : ta.base.n_layers * ta.base.n_kv_heads);
     if (units > 0x7fffffff)
         return cudaErrorInvalidValue;
     const int64_t items = 2 * units - ta.base.n_full;

@@ -171,6 +171,14 @@ struct AssembleArgs {
     int32_t n_layers, n_heads;  // kv heads
     int32_t upc;                // (layer, head) units per CTA
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
+    // a slice of the (layer, kv-head) units, [lh_begin, lh_begin + lh_count)
+    // (lh_count 0: all of them); the position ids and source map are written
+    // with the slice that starts at unit 0
+    int32_t lh_begin, lh_count;
+    // > 0: at most this many CTAs, each looping over (span, unit group)
+    // pieces (the stitch then leaves the other SMs to a concurrent kernel)
+    int32_t max_ctas;
+    int32_t n_spans;            // set by launch_assemble
 };
 
 // Span / local-source tables passed inside the kernel parameters (no upload)
@@ -205,6 +213,10 @@ struct AttnArgs {
     // two-CTA clusters
     int32_t n_full;
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
+    // tensor-core kernel: a slice of each request's (layer, kv-head) units,
+    // [lh_base, lh_base + lh_count) (lh_count 0: all); the request table's
+    // unit0 counts lh_count units per 256-row block
+    int32_t lh_base, lh_count;
     // tensor-core kernel: the output goes out through TMA tensor stores (the
     // tmap_out parameter), a warp's 32 rows = 32 / G whole tokens of the G
     // query heads of one kv head; set when G is a power of two and `out` is

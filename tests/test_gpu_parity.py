@@ -301,14 +301,24 @@ def test_pool_with_interleaved_rope_pairs(variant):
         assert torch.equal(got.view(torch.int16), case.out.view(torch.int16))
 
 
-def test_pool_in_pinned_host_memory():
+@pytest.mark.parametrize("name", ["edge_2_layers", "cfg2_28_layers"])
+def test_pool_in_pinned_host_memory(name):
     """A pool kept in pinned host memory (read by the stitch kernel through
-    its unified address): same results, bit for bit, as the device pool."""
+    its unified address).  kvr_prefill then stitches it in layer groups on a
+    second stream, each group's attention running beside the next group's
+    stitch: the stitched cache is the device pool's bit for bit, the output
+    matches the oracle (its rounding may differ from the device pool's run,
+    whose attention splits its last round of units differently)."""
     import torch
+    from parity import attn_within_tolerance, to_np64
     from rag_precomputed_kv_gb300 import kvr
-    cfg = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=13)
-    pid = cfg.n_chunks
-    cfg, reqs = _custom(cfg, [[[pid, 0, 5], [0, 3, 90], [2, 0, 96]], [[1, 7, 60], [3, 0, 96]]])
+    if name == "edge_2_layers":
+        cfg = dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=13)
+        pid = cfg.n_chunks
+        cfg, reqs = _custom(cfg, [[[pid, 0, 5], [0, 3, 90], [2, 0, 96]], [[1, 7, 60], [3, 0, 96]]])
+        sample = None
+    else:
+        cfg, reqs, sample = W.CONFIGS[2], None, 8
     case = Case(cfg, reqs=reqs)
     case.run(prefill=True)
     want = [x.clone() for x in (case.out, case.cache_k, case.cache_v)]
@@ -316,9 +326,11 @@ def test_pool_in_pinned_host_memory():
     case.pool = kvr.Pool(hk, hv, cfg.n_q_heads, cfg.rope_theta)
     for x in (case.out, case.cache_k, case.cache_v):
         x.fill_(float("nan"))
-    _ok(run_parity_case(cfg=cfg, case=case, prefill=True))
-    for g_, w_ in zip((case.out, case.cache_k, case.cache_v), want):
+    _ok(run_parity_case(cfg=cfg, case=case, prefill=True, sample_units=sample))
+    for g_, w_ in zip((case.cache_k, case.cache_v), want[1:]):
         assert torch.equal(g_.view(torch.int16), w_.view(torch.int16))
+    ok, mx, rel = attn_within_tolerance(to_np64(case.out), to_np64(want[0]), cfg.dtype)
+    assert ok, (mx, rel)
     with pytest.raises(kvr.KvrError) as e:      # the gathering attention wants device memory
         case.run(prefill=True, skip_prefix=True)
     assert e.value.status == 3
