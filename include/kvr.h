@@ -45,7 +45,13 @@
  *          head_dim * 2 bytes of device memory (T = query tokens of the
  *          call).  A call with more than the scratch holds waits for the
  *          previous call's attention, frees it and allocates it larger.
- *     kvr_pool_reserve makes 3 and 4 happen up front: afterwards, calls
+ *       5. Decode workspace (a decode step over fewer cache blocks than two
+ *          per SM, see kvr_query_attention): two partial-state slots per SM
+ *          (16.6 KB each) and one 4-byte arrival count per block of the
+ *          call; larger counts are allocated like 4.
+ *       6. A pool in pinned host memory: the first kvr_prefill on it creates
+ *          an internal stream and its events (kept until unregister).
+ *     kvr_pool_reserve makes 3, 4 and 5 happen up front: afterwards, calls
  *     within the reserved sizes allocate nothing and wait only in the one
  *     case of 3 (8 calls with uploaded tables still queued).  kvr_pool_unregister
  *     synchronizes the handle's work before it frees.
@@ -253,7 +259,10 @@ KVR_API kvr_status kvr_assemble(kvr_pool_t pool, int32_t batch, const int32_t *s
  * blog section 2.3: decoding continues normally on top of the stitched
  * cache) -- on a bf16 pool with head_dim 128 and at most 16 query heads per
  * kv head runs as a single kernel that rotates, appends and attends, each
- * (request, layer, kv-head) block streamed once.  Other calls on the
+ * (request, layer, kv-head) block streamed once: one CTA per block, or, with
+ * fewer blocks than two per SM, one CTA per SM over equal shares of all the
+ * blocks' key tiles (blocks split between CTAs are merged in a fixed order,
+ * in the decode workspace).  Other calls on the
  * tensor-core path (bf16, head_dim 128) also write zeros into the V rows
  * between a block's last query row and the end of its last 128-row key tile
  * (rows of the block, never past R_b); a decode step leaves those rows as
@@ -275,7 +284,8 @@ KVR_API kvr_status kvr_query_attention(kvr_pool_t pool, int32_t batch, const int
  * then KV_M(q; C_ctx) computed online).  Arguments mean what they mean in
  * those two calls (cache_k / cache_v and cache_offsets are shared; the
  * blocks must hold P_b + Lq_b rows); prefix_len is an optional host output.
- * Results are identical, bit for bit, to the two calls in a row.
+ * Results are identical, bit for bit, to the two calls in a row (a pool in
+ * pinned host memory: see below).
  *
  * The difference is scheduling: every check of both halves runs before
  * anything is enqueued, the table uploads go first, and the kernels follow
@@ -283,6 +293,19 @@ KVR_API kvr_status kvr_query_attention(kvr_pool_t pool, int32_t batch, const int
  * query-side kernel (rotation and append of the query tokens, which touches
  * no prefix row) runs alongside the stitch, and the attention kernel's setup
  * overlaps it.  The timing hook (kvr_set_timing_events) serializes them.
+ *
+ * A pool in pinned host memory (on the tensor-core path, more than one query
+ * token in some request, n_layers divisible by 2..8): the stitch, bound by
+ * the CPU-GPU link, runs by groups of layers, last group first, on 64 CTAs of
+ * an internal stream that starts after the work already on `stream`; the
+ * attention of each group runs on `stream`, on the other SMs, beside the
+ * stitch of the next group.  Before that stitch, zeros are written into the
+ * first min(P_b, 128) V rows of the first block of requests 1..batch-1 (rows
+ * the stitch then overwrites), so that the attention of the previous request's
+ * last block, whose last key tile reaches into them with weight 0, reads
+ * finite values.  When the call returns, all of its work is ordered before
+ * later work on `stream`.  The output is that of the two calls up to rounding
+ * order (the attention's last round of units splits differently on fewer SMs).
  *
  * flags: KVR_POSITIONS_COMPOSITE as in kvr_assemble; KVR_PREFILL_SKIP_PREFIX_CACHE
  * (above) needs a bf16 pool in device memory with head_dim 128, laid out contiguously
