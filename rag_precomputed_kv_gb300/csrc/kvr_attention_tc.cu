@@ -28,7 +28,7 @@
 // rescaled lazily: O_X is rescaled in TMEM only when a row's max grows by more
 // than 8 (log2 units).
 //
-// Warp roles (320 threads, one CTA per SM): warps 0-3 and 4-7 are the
+// Warp roles (384 threads, one CTA per SM): warps 0-3 and 4-7 are the
 // warpgroups of tiles A and B (softmax, epilogue); warp 8 issues the TMA loads
 // of Q (already rotated and packed by the query-prologue kernel; the next
 // unit's Q is prefetched into L2) and of the K/V tiles into a 4-slot ring;
@@ -36,7 +36,10 @@
 // one lane (elected once) issuing the tcgen05 instructions: with the
 // schedule's descriptor arithmetic warp-uniform, one MMA issues about as fast
 // as the tensor core retires it (issued from a single-lane branch it was the
-// bottleneck).  Barrier phases run on across units.
+// bottleneck); warps 10-11 only complete the third warpgroup, so that the
+// registers can be split by warpgroup (setmaxnreg): the softmax warpgroups
+// hold a whole row of S and run without spills.  Barrier phases run on
+// across units.
 //
 // Epilogue: each softmax thread holds one output row; its warp stages 32 rows
 // x 64 columns at a time in shared memory and writes them back as whole
@@ -58,7 +61,14 @@ namespace kvr {
 
 namespace {
 
-constexpr int kThreads = 320;           // stitched-cache variant
+// stitched-cache variant: 10 working warps and 2 idle ones completing the
+// third warpgroup; launched at 168 registers a thread (the most for 384), the
+// softmax warpgroups take 200 and the third gives up to 104 (setmaxnreg):
+// 2 x 128 x 200 + 128 x 104 = 384 x 168.  At 320 threads and a flat 168 the
+// softmax loop spilled, and G = 7 workloads ran 6-15 % slower.
+constexpr int kThreads = 384;
+constexpr int kRegsLaunchS = 168, kRegsSoftmaxS = 200, kRegsOtherS = 104;
+static_assert(2 * 128 * kRegsSoftmaxS + 128 * kRegsOtherS <= kThreads * kRegsLaunchS, "register split");
 // gathering variant: + 4 rotator warps (10-13, one per SM sub-partition) and
 // 2 idle warps completing the fourth warpgroup; launched at 128 registers a
 // thread, the softmax warpgroups take 152 and the other two give up to 104
@@ -769,16 +779,20 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
     tc_fence_after();
     cluster_sync();   // the partner CTA's barriers are initialised before any remote arrive
     const uint32_t tmem = *tmem_slot;
-    // gathering variant: each role's branch starts by setting its warp's
-    // register count, for whole warpgroups (0-1: softmax; 2: producer, MMA,
-    // rotators; 3: rotators and the two idle warps)
+    // each role's branch starts by setting its warp's register count, for
+    // whole warpgroups (0-1: softmax; 2: producer, MMA and rotators or idle
+    // warps; 3, gathering variant: rotators and two idle warps)
     auto regs_softmax = [] {
         if constexpr (kG)
             asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmaxG));
+        else
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmaxS));
     };
     auto regs_other = [] {
         if constexpr (kG)
             asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOtherG));
+        else
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOtherS));
     };
     // setup above overlaps the previous kernel's tail; its outputs (the
     // stitched cache, the rotated queries) are read only from here on
@@ -1559,7 +1573,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         if (!ok)
             flag_timeout(a.err, abort_flag);
     } else {
-        regs_other();   // warps 14-15 of the gathering variant: no role
+        regs_other();   // warps 10-11 (stitched) or 14-15 (gathering): no role
     }
 
     tc_fence_before();
@@ -1584,13 +1598,13 @@ static cudaError_t set_smem_attr()
     if (e != cudaSuccess)
         return e;
     if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-        if constexpr (kG) {
+        {
             // the register split (setmaxnreg) must fit what the CTA is launched
             // with, or the softmax warpgroups' increase would wait forever
             cudaFuncAttributes fa{};
             if ((e = cudaFuncGetAttributes(&fa, k_attention_tc<kG>)) != cudaSuccess)
                 return e;
-            if (fa.numRegs != kRegsLaunchG)
+            if (fa.numRegs != (kG ? kRegsLaunchG : kRegsLaunchS))
                 return cudaErrorInvalidConfiguration;
         }
         e = cudaFuncSetAttribute(k_attention_tc<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
