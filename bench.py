@@ -511,10 +511,27 @@ def run_kvr(args):
         torch.cuda.synchronize()
         wl.pool.check()
         g_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(g0, g1))
+        # its kernels through the timing hook (serialized), as for the stitched step
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_g)]
+        for e in [x for row in gev for x in row]:
+            e.record(stream)
+        torch.cuda.synchronize()
+        for k in range(n_g):
+            flush()
+            wl.pool.set_timing_events(gev[k])
+            wl.step(skip_prefix_cache=True)
+        torch.cuda.synchronize()
+        wl.pool.set_timing_events(None)
+        wl.pool.check()
         gather = {"ms_per_step": round(g_ms, 5), "steps": n_g,
                   "value": round(int(wl.prefix.sum()) / (g_ms * 1e-3), 1), "unit": UNIT,
-                  "what": "kvr_prefill with KVR_PREFILL_SKIP_PREFIX_CACHE: the attention gathers and "
-                          "re-rotates the prefix from the pool, no stitched cache written"}
+                  "kernel_ms": {
+                      "stitch_keys": round(statistics.mean(e[0].elapsed_time(e[1]) for e in gev), 5),
+                      "query_prologue": round(statistics.mean(e[2].elapsed_time(e[3]) for e in gev), 5),
+                      "attention_values_gathered": round(statistics.mean(e[4].elapsed_time(e[5]) for e in gev), 5)},
+                  "what": "kvr_prefill with KVR_PREFILL_SKIP_PREFIX_CACHE: a keys-only stitch, then the "
+                          "attention reads the keys from the cache and gathers the prefix values from the "
+                          "pool; the cache's prefix value rows are not written"}
 
     # ---- one decode step after the prefill ----
     decode = decode_timing(wl, cfg, dev, args.steps, args.warmup, flush)

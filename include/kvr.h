@@ -112,11 +112,12 @@ enum { KVR_DTYPE_BF16 = 0, KVR_DTYPE_FP32 = 1 };
  * this pool: stored keys, query keys and query heads. */
 #define KVR_POOL_ROPE_INTERLEAVED 2u
 
-/* kvr_prefill flag: no decode follows, so the stitched prefix is not kept.
- * The prefix rows [0, P_b) of the cache blocks are left as they are; the
- * attention gathers the prefix keys and values straight from the pool and
- * re-rotates the keys on chip (the query rows P_b.. are still appended, and
- * pos_ids / src_map are still written).  The output is the same. */
+/* kvr_prefill flag: no decode follows, so the stitched prefix values are not
+ * kept.  The prefix keys are stitched (re-rotated) into the cache's K blocks
+ * as usual, but the value rows [0, P_b) of the cache's V blocks are left as
+ * they are: the attention reads the prefix values straight from the pool
+ * (the query rows P_b.. are still appended, and pos_ids / src_map are still
+ * written).  Half the stitch's traffic; the output is the same, bit for bit. */
 #define KVR_PREFILL_SKIP_PREFIX_CACHE 2u
 
 typedef struct kvr_pool *kvr_pool_t;

@@ -765,6 +765,7 @@ struct GatherLaunch {
     GatherArgs g{};
     SpanTable st;
     bool inl = false;
+    bool values_only = false;   // keys from the cache (stitched, keys only), values from the pool
 };
 
 }  // namespace
@@ -1033,7 +1034,7 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         const int64_t units = (int64_t)pl.m_blocks * lh_part;
         const int64_t tail = units % n_sms;
         ta.base.n_full = (int32_t)units;
-        if (tail > 0 && 2 * tail <= n_sms && attention_tc_pairs_fit(n_sms, gl != nullptr))
+        if (tail > 0 && 2 * tail <= n_sms && attention_tc_pairs_fit(n_sms, gl && !gl->values_only))
             ta.base.n_full = (int32_t)(units - tail);
         QueryPrologueArgs qp{pl.at.reqs, p->rope, pl.q, pl.kq, pl.vq, pl.cache_k, pl.cache_v, p->q_rot,
                              p->d.n_layers, p->d.n_q_heads, p->d.n_kv_heads, pl.T, pl.max_lq, pl.batch,
@@ -1067,7 +1068,8 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
             }
             p->mark(5, s);
         } else if (e == cudaSuccess) {
-            NvtxRange r(gl ? "kvr.k_attention_tc_gathering" : "kvr.k_attention_tc");
+            NvtxRange r(!gl ? "kvr.k_attention_tc" : gl->values_only ? "kvr.k_attention_tc_values_gathered"
+                                                                    : "kvr.k_attention_tc_gathering");
             if (pl.parts > 1) {
                 p->mark(4, s);
                 for (int g = pl.parts - 1; g >= 0 && e == cudaSuccess; --g) {
@@ -1079,7 +1081,8 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
                 p->mark(5, s);
             } else {
                 if (gl) {
-                    ta.gather = true;
+                    ta.gather = !gl->values_only;
+                    ta.gather_v = gl->values_only;
                     ta.tmap_pk = &gl->mpk;
                     ta.tmap_pv = &gl->mpv;
                     ta.tmap_bk = &gl->mbk;
@@ -1192,7 +1195,9 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
     DeviceGuard g(p->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (gather) {
-        // the attention gathers the prefix from the pool; nothing stitched
+        // the stitch writes the prefix keys (re-rotated) and the maps only; the
+        // attention reads the keys from the cache and gathers the prefix values
+        // from the pool
         if (!use_tensor_cores(*p))
             return fail(KVR_ERR_UNSUPPORTED, "KVR_PREFILL_SKIP_PREFIX_CACHE needs the tensor-core attention");
         cudaPointerAttributes pa{};
@@ -1203,9 +1208,8 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
         if (qp.T == 0)
             return KVR_OK;
         GatherLaunch gl;
-        if ((st = encode_gather_map(*p, p->d.k, &gl.mpk)) != KVR_OK ||
-            (st = encode_gather_map(*p, p->d.v, &gl.mpv)) != KVR_OK ||
-            (st = encode_gather_map(*p, p->d.k, &gl.mbk, 32)) != KVR_OK ||
+        gl.values_only = true;
+        if ((st = encode_gather_map(*p, p->d.v, &gl.mpv)) != KVR_OK ||
             (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK)
             return st;
         for (int b = 0; b < batch; ++b) {
@@ -1220,9 +1224,15 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
         gl.g.spans = gl.inl ? nullptr : ap.a.spans;
         gl.g.n_spans = (int32_t)ap.ds.size();
         gl.g.entry_len = (int32_t)p->d.entry_len;
-        gl.g.pos_ids = pos_ids;
-        gl.g.src_map = src_map;
-        st = qa_launch(p, qp, s, false, &gl);
+        if (stitch) {
+            ap.a.keys_only = 1;
+            if ((st = asm_launch(p, ap, s, false)) != KVR_OK) {
+                if (ap.slot)
+                    cudaEventRecord(ap.slot->done, s);
+                return st;
+            }
+        }
+        st = qa_launch(p, qp, s, stitch, &gl);
         if (ap.slot)
             cudaEventRecord(ap.slot->done, s);
         return st;

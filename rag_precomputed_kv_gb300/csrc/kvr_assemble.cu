@@ -187,8 +187,10 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
                 const int64_t so = l * sl + h * sh + (int64_t)(sp.start + row) * st + j * E;
                 klo[u] = ld_stream(kb + so);
                 khi[u] = ld_stream(kb + so + H2);
-                vlo[u] = ld_stream(vb + so);
-                vhi[u] = ld_stream(vb + so + H2);
+                if (!a.keys_only) {
+                    vlo[u] = ld_stream(vb + so);
+                    vhi[u] = ld_stream(vb + so + H2);
+                }
                 dst[u] = (sp.dst_row0 + (int64_t)unit * sp.cap + sp.row + row) * D + j * E;
             }
         }
@@ -229,8 +231,10 @@ __device__ __forceinline__ void assemble_body(const AssembleArgs &a, const DevSp
                 Vec<T>::rotate(klo[u], khi[u], c, s, a.interleaved);
                 st_vec(ck + dst[u], klo[u]);
                 st_vec(ck + dst[u] + H2, khi[u]);
-                st_vec(cv + dst[u], vlo[u]);
-                st_vec(cv + dst[u] + H2, vhi[u]);
+                if (!a.keys_only) {
+                    st_vec(cv + dst[u], vlo[u]);
+                    st_vec(cv + dst[u] + H2, vhi[u]);
+                }
             }
         }
     }

@@ -118,7 +118,15 @@ constexpr int kBarPeerFree = kBarPeerData + 1;
 // slots): full (1 arrival), read by every consumer warp (one arrival each)
 constexpr int kBarGeoFull = kBarPeerFree + 1;     // [2]
 constexpr int kBarGeoEmpty = kBarGeoFull + 2;     // [2]
-constexpr int kNumBars = kBarGeoEmpty + 2;
+// values-gathering variant: a V tile patched on chip is complete (1 arrival);
+// one per V ring slot (odd slots), so that none runs more than a phase ahead
+// of its waiter (a slot is refilled only after the MMAs consumed it)
+constexpr int kBarPatched = kBarGeoEmpty + 2;     // [2]
+// ... and the producer has issued that tile's copies (1 arrival): the patch
+// warp waits for this before it waits for the copies, so that its parity
+// wait on the slot's full barrier never runs ahead of the slot's previous load
+constexpr int kBarPatchJob = kBarPatched + 2;     // [2]
+constexpr int kNumBars = kBarPatchJob + 2;
 constexpr int kOffMeta = kOffBar + 8 * kNumBars;  // [2][128] int: rotation of each row of the K slots
 constexpr int kOffTmemAddr = kOffMeta + 2 * kTileN * 4;
 constexpr int kOffAbort = kOffTmemAddr + 4;
@@ -257,6 +265,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// 16 bytes global -> shared, asynchronous (this thread's copies complete at
+// cp_async_wait_all); no register holds the data
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -656,7 +674,7 @@ struct Geo {
     int jb, je, half, n_tiles;
     int n_t[2], row0[2];
     int m_rows, q_len, prefix, q_off;
-    int l, h, n_valid, pad_;
+    int l, h, n_valid, cap;
     int64_t kv_row0;
 };
 static_assert(sizeof(Geo) <= kGeoBytes, "geometry slot");
@@ -678,11 +696,23 @@ __device__ __forceinline__ void geo_of(const Item &t, Geo &o)
     o.l = t.w.l;
     o.h = t.w.h;
     o.n_valid = t.w.n_valid;
-    o.pad_ = 0;
+    o.cap = t.w.rq.cap;
     o.kv_row0 = t.w.kv_row0;
 }
-template <bool kG>
-constexpr uint32_t geo_consumer_warps() { return kG ? 13u : 9u; }   // softmax 8, MMA 1, rotators 4
+// the kernel's variants: K and V from the stitched cache; both gathered from
+// the pool (keys re-rotated on chip); values gathered, keys from the cache
+constexpr int kModeStitched = 0, kModeGather = 1, kModeGatherV = 2;
+// softmax 8, MMA 1, and the rotators (4) or the patch warp (1)
+template <int kM>
+constexpr uint32_t geo_consumer_warps() { return kM == kModeGather ? 13u : kM == kModeGatherV ? 10u : 9u; }
+
+// The value tile j of a values-gathering item that is patched on chip: it
+// holds the first query rows after prefix rows from the pool, or it reaches
+// past the cache block (into rows this variant does not write).
+__device__ __forceinline__ bool v_patched(int j, int prefix, int cap)
+{
+    return (j * kTileN < prefix && prefix < (j + 1) * kTileN) || (j + 1) * kTileN > cap;
+}
 
 // `rr`: the producer warp's register copy of the request table (all 32
 // lanes call with the same `it`), or NULL.
@@ -701,8 +731,8 @@ __device__ __forceinline__ Item item_at(const AttnArgs &a, const DevReq *reqs, i
 
 }  // namespace
 
-template <bool kG>
-__global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
+template <int kM>
+__global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
     k_attention_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnArgs a,
                    const __grid_constant__ ReqTable rt, const int n_blocks,
@@ -711,6 +741,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                    const __grid_constant__ GatherArgs g, const __grid_constant__ SpanTable st,
                    const __grid_constant__ CUtensorMap tmo)
 {
+    constexpr bool kG = kM == kModeGather, kV = kM == kModeGatherV;
     const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -754,7 +785,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                             i == kBarPeerData;
             const bool rot = i >= kBarReady && i < kBarReady + kSlots;
             const bool geo_empty = i >= kBarGeoEmpty && i < kBarGeoEmpty + 2;
-            mbar_init(bar(i), wg ? 128u : rot ? (uint32_t)kRotThreads : geo_empty ? geo_consumer_warps<kG>() : 1u);
+            mbar_init(bar(i), wg ? 128u : rot ? (uint32_t)kRotThreads : geo_empty ? geo_consumer_warps<kM>() : 1u);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -771,6 +802,9 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             prefetch_tmap(&tmpk);
             prefetch_tmap(&tmpv);
             prefetch_tmap(&tmbk);
+            prefetch_tmap(&tmbv);
+        } else if constexpr (kV) {
+            prefetch_tmap(&tmpv);
             prefetch_tmap(&tmbv);
         }
     }
@@ -1083,7 +1117,159 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
             flag_timeout(a.err, abort_flag);
     } else if (warp == 8) {
         regs_other();
-        if constexpr (!kG) {
+        if constexpr (kV) {
+            // ====== values-gathering producer: Q and the K tiles as in the
+            // stitched variant; a V tile with prefix rows comes from the pool
+            // (lane i: rows 4i..4i+3, resolved through the span table; a group
+            // of 8 lanes whose 32 rows are consecutive pool rows takes one
+            // 32-row box load per panel, other lanes a gather4 each), later V
+            // tiles from the cache block ======
+            int tt = 0, nq = 0, gk = 0;
+            bool ok = true;
+            const DevSpan *spans = g.spans ? g.spans : st.spans;
+            const int64_t e_rows = (int64_t)a.n_layers * a.n_kv_heads * g.entry_len;   // pool rows per entry
+            ReqRegs rr;
+            rr.load(a, reqs, lane);
+            Item nxt;
+            if ((int)blockIdx.x < n_items) {
+                nxt = item_at(a, reqs, n_blocks, blockIdx.x, &rr, lane);
+                if (lane == 0)
+                    ok = geo_put(0, nxt);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
+                const Item itm = nxt;
+                const Unit &w = itm.w;
+                const bool more = it + (int)gridDim.x < n_items;
+                if (more && gk > 0)
+                    nxt = item_at(a, reqs, n_blocks, it + gridDim.x, &rr, lane);
+                if (itm.je > itm.jb) {
+                    const int prefix = w.rq.prefix, s_end = w.rq.span_end;
+                    const int64_t lh_row = (int64_t)w.lh * g.entry_len;   // (layer, kv-head) block inside an entry
+                    // the span holding the item's first row (a request's spans are in
+                    // stitched-row order); each lane's cursor then only moves forward
+                    int cur = w.rq.span0;
+                    if (itm.jb * kTileN < prefix) {
+                        int lo = w.rq.span0, hi = s_end - 1;
+                        while (lo < hi) {
+                            const int mid = (lo + hi + 1) >> 1;
+                            if (spans[mid].row <= itm.jb * kTileN)
+                                lo = mid;
+                            else
+                                hi = mid - 1;
+                        }
+                        cur = lo;
+                    }
+                    const int n_loads = 2 * (itm.je - itm.jb);
+                    int rows[4] = {0, 0, 0, 0};
+                    bool run32 = false;   // this lane's 32-row group is 32 consecutive pool rows
+                    for (int i = 0; i <= n_loads; ++i) {
+                        if (i == 2 && lane == 0) {   // Q after K_0 and V_0, as in the stitched variant
+                            if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
+                                ok = false;
+                            } else {
+                                const int nqt = w.n_t[1] > 0 ? 2 : 1;
+                                mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
+                                for (int x = 0; x < nqt; ++x) {
+                                    const uint32_t dst = sbase + kOffQ + x * kTileBytes;
+                                    tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
+                                    tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
+                                }
+                            }
+                        }
+                        if (i == 2)
+                            ++nq;
+                        if (i == n_loads)
+                            break;
+                        const int slot = tt % kSlots;
+                        if (lane == 0 && ok && tt >= kSlots &&
+                            !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag))
+                            ok = false;
+                        if (!(ok = __shfl_sync(0xffffffffu, ok, 0)))
+                            break;
+                        const int j = itm.jb + (i >> 1);
+                        const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
+                        if ((i & 1) == 0 || j * kTileN >= prefix) {
+                            // a K tile, or a V tile past the prefix: the cache block's rows
+                            if (lane == 0) {
+                                const CUtensorMap *map = (i & 1) ? &tmv : &tmk;
+                                const int row = (int)(w.kv_row0 + (int64_t)j * kTileN);
+                                mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
+                                tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
+                                tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
+                            }
+                            // V tile j's pool rows, resolved while its slot drains (rows
+                            // past the prefix: any pool row, which the patch warp replaces)
+                            if ((i & 1) == 0 && j * kTileN < prefix) {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const int r = j * kTileN + 4 * lane + k;
+                                    rows[k] = 0;
+                                    if (r < prefix) {
+                                        while (cur + 1 < s_end && spans[cur].row + spans[cur].len <= r)
+                                            ++cur;
+                                        const DevSpan &sp = spans[cur];
+                                        rows[k] = (int)((int64_t)sp.src * e_rows + lh_row + sp.start + (r - sp.row));
+                                    }
+                                }
+                                const int last = __shfl_up_sync(0xffffffffu, rows[3], 1);
+                                const bool mine = (j * kTileN + 4 * lane + 3 < prefix) && rows[1] == rows[0] + 1 &&
+                                                  rows[2] == rows[0] + 2 && rows[3] == rows[0] + 3 &&
+                                                  ((lane & 7) == 0 || rows[0] == last + 1);
+                                const unsigned ball = __ballot_sync(0xffffffffu, mine);
+                                run32 = ((ball >> (lane & ~7)) & 0xffu) == 0xffu;
+                            }
+                        } else {
+                            if (lane == 0)
+                                mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
+                            __syncwarp();
+                            const uint32_t d4 = dst + (uint32_t)(4 * lane) * 128u;
+                            if (run32) {
+                                if ((lane & 7) == 0) {
+                                    tma_load_2d(d4, &tmbv, 0, rows[0], bar(kBarFull + slot));
+                                    tma_load_2d(d4 + kPanelBytes, &tmbv, 64, rows[0], bar(kBarFull + slot));
+                                }
+                            } else {
+                                tma_gather4(d4, &tmpv, 0, rows, bar(kBarFull + slot));
+                                tma_gather4(d4 + kPanelBytes, &tmpv, 64, rows, bar(kBarFull + slot));
+                            }
+                        }
+                        if ((i & 1) == 1 && lane == 0 && v_patched(j, prefix, w.rq.cap))
+                            mbar_arrive(bar(kBarPatchJob + (slot >> 1)));
+                        ++tt;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                // the next item's geometry, published for the other roles; its Q
+                // brought into L2 ahead of its load
+                if (ok && more) {
+                    if (gk == 0)
+                        nxt = item_at(a, reqs, n_blocks, it + gridDim.x, &rr, lane);
+                    if (lane == 0) {
+                        ok = geo_put(gk + 1, nxt);
+                        if (ok && nxt.je > nxt.jb)
+                            for (int x = 0; x < (nxt.w.n_t[1] > 0 ? 2 : 1); ++x) {
+                                tma_prefetch_2d(&tmq, 0, nxt.w.q_row0 + x * kTileM);
+                                tma_prefetch_2d(&tmq, 64, nxt.w.q_row0 + x * kTileM);
+                            }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                }
+            }
+            if (lane == 0) {
+                if (!ok)
+                    flag_timeout(a.err, abort_flag);
+                // drain: every issued copy lands before the CTA leaves
+                const uint64_t t0 = globaltimer();
+                for (int k = (tt > kSlots ? tt - kSlots : 0); k < tt; ++k)
+                    while (!mbar_try_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1) &&
+                           globaltimer() - t0 < kWaitNs) {
+                    }
+                if (nq > 0)
+                    while (!mbar_try_wait(bar(kBarQFull), (nq - 1) & 1) && globaltimer() - t0 < kWaitNs) {
+                    }
+            }
+        } else if constexpr (!kG) {
             // ====== stitched producer: the whole warp computes each item's
             // geometry (request table in registers), lane 0 waits and issues ======
             int tt = 0, nq = 0, gk = 0;
@@ -1357,6 +1543,22 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 tc_fence_after();
                 return true;
             };
+            // values-gathering variant: a patched V tile is complete once the
+            // patch warp has written it (it waited for the tile's copies)
+            int np[2] = {0, 0}, prefix_v = 0, cap_v = 0;
+            auto wait_v = [&](int k, int j) -> bool {
+                if constexpr (kV) {
+                    if (v_patched(j, prefix_v, cap_v)) {
+                        const int b = (k % kSlots) >> 1;   // V tiles sit in slots 1 and 3
+                        if (!mbar_wait(bar(kBarPatched + b), np[b] & 1, abort_flag))
+                            return false;
+                        ++np[b];
+                        tc_fence_after();
+                        return true;
+                    }
+                }
+                return wait_kv(k);
+            };
             int gk = 0;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
                 const Geo *gp = geo_wait(gk);
@@ -1366,6 +1568,10 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                 }
                 const int jb = gp->jb, je = gp->je, half = gp->half, n_tiles = gp->n_tiles;
                 const int nt0 = gp->n_t[0], nt1 = gp->n_t[1];
+                if constexpr (kV) {
+                    prefix_v = gp->prefix;
+                    cap_v = gp->cap;
+                }
                 geo_done(gk);
                 if (je <= jb)
                     continue;
@@ -1395,7 +1601,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
                             break;
                         }
                         ++p_cnt[x];
-                        if (!v_ready && !(v_ready = wait_kv(tv))) {
+                        if (!v_ready && !(v_ready = wait_v(tv, j))) {
                             ok = false;
                             break;
                         }
@@ -1572,6 +1778,71 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
         }
         if (!ok)
             flag_timeout(a.err, abort_flag);
+    } else if (kV && warp == 10) {
+        regs_other();
+        // ========== patch (values-gathering variant, warp 10) ==========
+        // A V tile that holds prefix rows came from the pool, with pool row 0
+        // in place of its query rows: copy those from the cache block (the
+        // query prologue appended them there).  Rows past the request's keys
+        // are zeroed (a masked key has weight 0, but 0 x NaN is NaN, and a
+        // tile that reaches past the cache block reads rows this variant does
+        // not write).  Lane l owns 16-byte chunk l % 8 of rows l / 8 + 4k.
+        const int c8 = lane & 7;
+        const __nv_bfloat16 *cv = static_cast<const __nv_bfloat16 *>(a.cache_v);
+        int tt = 0, gk = 0, nj[2] = {0, 0};
+        bool ok = true;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
+            int jb, je, prefix, n_valid, cap;
+            int64_t kv_row0;
+            {
+                const Geo *gp = geo_wait(gk);
+                if (!gp) {
+                    ok = false;
+                    break;
+                }
+                jb = gp->jb;
+                je = gp->je;
+                prefix = gp->prefix;
+                n_valid = gp->n_valid;
+                cap = gp->cap;
+                kv_row0 = gp->kv_row0;
+                geo_done(gk);
+            }
+            for (int j = jb; j < je; ++j, tt += 2) {
+                if (!v_patched(j, prefix, cap))
+                    continue;
+                const int sv = (tt + 1) % kSlots, b = sv >> 1;
+                if (!mbar_wait(bar(kBarPatchJob + b), nj[b] & 1, abort_flag) ||
+                    !mbar_wait(bar(kBarFull + sv), ((tt + 1) / kSlots) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++nj[b];
+                const uint32_t vb = sbase + kOffKV + sv * kTileBytes;
+                // from the pool: rows from the prefix on; from the cache: rows past the keys
+                const int first = max(j * kTileN < prefix ? prefix : n_valid, j * kTileN) - j * kTileN;
+                // every copy of the warp in flight at once, then one wait
+                for (int r = first + (lane >> 3); r < kTileN; r += 4) {
+                    const int rr = j * kTileN + r;
+                    const uint32_t lo_a = vb + r * 128 + ((c8 ^ (r & 7)) << 4);
+                    if (rr < n_valid) {
+                        const __nv_bfloat16 *src = cv + (kv_row0 + rr) * kD + 8 * c8;
+                        cp_async16(lo_a, src);
+                        cp_async16(lo_a + kPanelBytes, src + kD / 2);
+                    } else {
+                        st_shared_v4(lo_a, 0u, 0u, 0u, 0u);
+                        st_shared_v4(lo_a + kPanelBytes, 0u, 0u, 0u, 0u);
+                    }
+                }
+                cp_async_wait_all();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(kBarPatched + b));
+            }
+        }
+        if (!ok)
+            flag_timeout(a.err, abort_flag);
     } else {
         regs_other();   // warps 10-11 (stitched) or 14-15 (gathering): no role
     }
@@ -1587,7 +1858,7 @@ __global__ void __launch_bounds__(kG ? kThreadsG : kThreads, 1)
 
 bool attention_tc_supported(int dtype, int head_dim) { return dtype == KVR_DTYPE_BF16 && head_dim == kD; }
 
-template <bool kG>
+template <int kM>
 static cudaError_t set_smem_attr()
 {
     // the shared-memory opt-in is per device and per kernel (callers on
@@ -1602,12 +1873,12 @@ static cudaError_t set_smem_attr()
             // the register split (setmaxnreg) must fit what the CTA is launched
             // with, or the softmax warpgroups' increase would wait forever
             cudaFuncAttributes fa{};
-            if ((e = cudaFuncGetAttributes(&fa, k_attention_tc<kG>)) != cudaSuccess)
+            if ((e = cudaFuncGetAttributes(&fa, k_attention_tc<kM>)) != cudaSuccess)
                 return e;
-            if (fa.numRegs != (kG ? kRegsLaunchG : kRegsLaunchS))
+            if (fa.numRegs != (kM == kModeGather ? kRegsLaunchG : kRegsLaunchS))
                 return cudaErrorInvalidConfiguration;
         }
-        e = cudaFuncSetAttribute(k_attention_tc<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(k_attention_tc<kM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess)
             return e;
         if (dev < 64)
@@ -1616,7 +1887,7 @@ static cudaError_t set_smem_attr()
     return cudaSuccess;
 }
 
-template <bool kG>
+template <int kM>
 static bool pairs_fit(int n_sms)
 {
     static std::atomic<int> fit[64] = {};   // 0 unknown, 1 yes, 2 no
@@ -1624,13 +1895,13 @@ static bool pairs_fit(int n_sms)
     if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || (n_sms & 1))
         return false;
     if (fit[dev].load(std::memory_order_acquire) == 0) {
-        if (set_smem_attr<kG>() != cudaSuccess) {
+        if (set_smem_attr<kM>() != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(n_sms);
-        cfg.blockDim = dim3(kG ? kThreadsG : kThreads);
+        cfg.blockDim = dim3(kM == kModeGather ? kThreadsG : kThreads);
         cfg.dynamicSmemBytes = kSmemBytes;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -1640,7 +1911,7 @@ static bool pairs_fit(int n_sms)
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n = 0;
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_attention_tc<kG>, &cfg);
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_attention_tc<kM>, &cfg);
         if (e != cudaSuccess)
             cudaGetLastError();
         fit[dev].store((e == cudaSuccess && 2 * n >= n_sms) ? 1 : 2, std::memory_order_release);
@@ -1648,12 +1919,17 @@ static bool pairs_fit(int n_sms)
     return fit[dev].load(std::memory_order_acquire) == 1;
 }
 
-bool attention_tc_pairs_fit(int n_sms, bool gather) { return gather ? pairs_fit<true>(n_sms) : pairs_fit<false>(n_sms); }
+bool attention_tc_pairs_fit(int n_sms, bool gather)
+{
+    // the values-gathering variant has the stitched variant's block and shared memory
+    return gather ? pairs_fit<kModeGather>(n_sms) : pairs_fit<kModeStitched>(n_sms);
+}
 
-template <bool kG>
+template <int kM>
 static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool pairs, cudaStream_t s)
 {
-    cudaError_t e = set_smem_attr<kG>();
+    constexpr bool kG = kM == kModeGather, kV = kM == kModeGatherV;
+    cudaError_t e = set_smem_attr<kM>();
     if (e != cudaSuccess)
         return e;
     static const CUtensorMap no_map{};
@@ -1680,14 +1956,14 @@ static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool
     }
     cfg.attrs = attr;
     cfg.numAttrs = n_attr;
-    return cudaLaunchKernelEx(&cfg, k_attention_tc<kG>, *static_cast<const CUtensorMap *>(ta.tmap_q),
+    return cudaLaunchKernelEx(&cfg, k_attention_tc<kM>, *static_cast<const CUtensorMap *>(ta.tmap_q),
                               *static_cast<const CUtensorMap *>(ta.tmap_k),
                               *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base, *ta.rt, ta.n_m_blocks,
                               kG ? *static_cast<const CUtensorMap *>(ta.tmap_pk) : no_map,
-                              kG ? *static_cast<const CUtensorMap *>(ta.tmap_pv) : no_map,
+                              kG || kV ? *static_cast<const CUtensorMap *>(ta.tmap_pv) : no_map,
                               kG ? *static_cast<const CUtensorMap *>(ta.tmap_bk) : no_map,
-                              kG ? *static_cast<const CUtensorMap *>(ta.tmap_bv) : no_map, kG ? ta.g : no_gather,
-                              kG && ta.st ? *ta.st : no_spans,
+                              kG || kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv) : no_map,
+                              kG || kV ? ta.g : no_gather, (kG || kV) && ta.st ? *ta.st : no_spans,
                               ta.base.out_tma ? *static_cast<const CUtensorMap *>(ta.tmap_out) : no_map);
 }
 
@@ -1706,7 +1982,9 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
     // CTAs 2i and 2i + 1 of the last round when n_full is a multiple of the grid
     if (pairs && ((grid & 1) || ta.base.n_full % grid != 0))
         return cudaErrorInvalidValue;
-    return ta.gather ? launch_variant<true>(ta, grid, pdl, pairs, s) : launch_variant<false>(ta, grid, pdl, pairs, s);
+    return ta.gather     ? launch_variant<kModeGather>(ta, grid, pdl, pairs, s)
+           : ta.gather_v ? launch_variant<kModeGatherV>(ta, grid, pdl, pairs, s)
+                         : launch_variant<kModeStitched>(ta, grid, pdl, pairs, s);
 }
 
 }  // namespace kvr

@@ -179,6 +179,7 @@ struct AssembleArgs {
     // pieces (the stitch then leaves the other SMs to a concurrent kernel)
     int32_t max_ctas;
     int32_t n_spans;            // set by launch_assemble
+    int32_t keys_only;          // stitch K (and the maps) only; V is gathered by the attention
 };
 
 // Span / local-source tables passed inside the kernel parameters (no upload)
@@ -275,6 +276,7 @@ struct TcAttnArgs {
     int32_t n_m_blocks;         // total 256-row query blocks over all requests
     int32_t n_sms;              // persistent grid size bound
     bool gather;                // K/V from the pool (tmap_pk / tmap_pv, g, st) instead of the cache
+    bool gather_v;              // V tiles of prefix rows from the pool (tmap_pv, tmap_bv, g, st), K from the cache
     const void *tmap_pk;        // pool K and V as [rows, D] with a one-row box (gather4)
     const void *tmap_pv;
     const void *tmap_bk;        // the same with a 32-row box (runs of consecutive pool rows)

@@ -174,8 +174,8 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
                     skip_prefix=False, force_units=()):
     """Run one configuration and compare with the oracle; returns a summary
     dict with ``ok`` and the worst errors.  skip_prefix: kvr_prefill with
-    KVR_PREFILL_SKIP_PREFIX_CACHE, whose cache prefix rows must stay as they
-    were (NaN), everything else compared as usual.  ``sample_units`` seeded
+    KVR_PREFILL_SKIP_PREFIX_CACHE, whose cache prefix value rows must stay as
+    they were (NaN), everything else compared as usual.  ``sample_units`` seeded
     (layer, kv-head) units are checked per request, plus ``force_units``
     (e.g. the last layer's)."""
     import torch
@@ -215,16 +215,17 @@ def run_parity_case(cid=None, cfg=None, device="cuda:0", sample_units=None, requ
         ck = to_np64(case.cache_block("k", b)[units])
         cv = to_np64(case.cache_block("v", b)[units])
         if skip_prefix:
-            if not (np.isnan(ck[:, :P]).all() and np.isnan(cv[:, :P]).all()):
+            # the attention gathers the prefix values from the pool: the cache's
+            # prefix value rows stay as they were
+            if not np.isnan(cv[:, :P]).all():
                 res["ok"] = False
-                res["prefix"] = f"request {b}: prefix rows were written"
-        else:
-            if not np.array_equal(cv[:, :P], V_ref[0]):
-                res["ok"] = False
-                res["v"] = f"request {b}: gathered V differs"
-            okk, ratio = k_within_tolerance(ck[:, :P], K_ref[0], cfg.dtype, case.il)
-            res["k_ratio"] = max(res["k_ratio"], ratio)
-            res["ok"] &= okk
+                res["prefix"] = f"request {b}: prefix value rows were written"
+        elif not np.array_equal(cv[:, :P], V_ref[0]):
+            res["ok"] = False
+            res["v"] = f"request {b}: gathered V differs"
+        okk, ratio = k_within_tolerance(ck[:, :P], K_ref[0], cfg.dtype, case.il)
+        res["k_ratio"] = max(res["k_ratio"], ratio)
+        res["ok"] &= okk
         if attention:
             qo = int(case.q_offsets[b])
             li = [u // H for u in units]

@@ -1,11 +1,12 @@
-"""GPU parity of kvr_prefill with KVR_PREFILL_SKIP_PREFIX_CACHE: the attention
-gathers the prefix keys and values straight from the pool (re-rotating the
-keys on chip) and leaves the cache's prefix rows alone.
+"""GPU parity of kvr_prefill with KVR_PREFILL_SKIP_PREFIX_CACHE: a keys-only
+stitch, then the attention reads the keys from the cache and gathers the
+prefix values straight from the pool; the cache's prefix value rows are left
+alone (NaN here), so a key tile that reaches past its cache block meets them.
 
-Checked against the oracle (attention output, appended query rows, position
-ids and source map) and, bit for bit, against the stitched path: the key
-rotation is the same arithmetic and the MMAs run in the same order, so the
-outputs must be identical.
+Checked against the oracle (attention output, stitched keys, appended query
+rows, position ids and source map) and, bit for bit, against the stitched
+path: the keys come from the same stitch kernel, the values are the pool's
+bytes, and the MMAs run in the same order, so the outputs must be identical.
 """
 import dataclasses
 
@@ -108,9 +109,8 @@ def test_gathering_prefill_refuses_what_it_cannot_gather():
 
 
 def test_gathering_prefill_with_pool_keys_kept_before_rope():
-    """The gathering attention turns each pool row by its position when the
-    pool keeps its keys before RoPE; output still bit-identical to the
-    stitched path."""
+    """With the pool's keys kept before RoPE the keys-only stitch turns each
+    row by its position; output still bit-identical to the stitched path."""
     import torch
     cfg = W.CONFIGS[2]
     case = Case(cfg, keys_unrotated=True)
