@@ -759,13 +759,14 @@ kvr_status encode_gather_map(const kvr_pool &p, const void *base, CUtensorMap *m
     return KVR_OK;
 }
 
-// What the gathering attention needs beyond a query-attention launch.
+// What the values-gathering attention needs beyond a query-attention launch:
+// the pool's values as gather4 (one-row box) and 32-row box sources, and the
+// span table.
 struct GatherLaunch {
-    CUtensorMap mpk, mpv, mbk, mbv;
+    CUtensorMap mpv, mbv;
     GatherArgs g{};
     SpanTable st;
     bool inl = false;
-    bool values_only = false;   // keys from the cache (stitched, keys only), values from the pool
 };
 
 }  // namespace
@@ -1034,7 +1035,7 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         const int64_t units = (int64_t)pl.m_blocks * lh_part;
         const int64_t tail = units % n_sms;
         ta.base.n_full = (int32_t)units;
-        if (tail > 0 && 2 * tail <= n_sms && attention_tc_pairs_fit(n_sms, gl && !gl->values_only))
+        if (tail > 0 && 2 * tail <= n_sms && attention_tc_pairs_fit(n_sms))
             ta.base.n_full = (int32_t)(units - tail);
         QueryPrologueArgs qp{pl.at.reqs, p->rope, pl.q, pl.kq, pl.vq, pl.cache_k, pl.cache_v, p->q_rot,
                              p->d.n_layers, p->d.n_q_heads, p->d.n_kv_heads, pl.T, pl.max_lq, pl.batch,
@@ -1068,8 +1069,7 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
             }
             p->mark(5, s);
         } else if (e == cudaSuccess) {
-            NvtxRange r(!gl ? "kvr.k_attention_tc" : gl->values_only ? "kvr.k_attention_tc_values_gathered"
-                                                                    : "kvr.k_attention_tc_gathering");
+            NvtxRange r(gl ? "kvr.k_attention_tc_values_gathered" : "kvr.k_attention_tc");
             if (pl.parts > 1) {
                 p->mark(4, s);
                 for (int g = pl.parts - 1; g >= 0 && e == cudaSuccess; --g) {
@@ -1081,11 +1081,8 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
                 p->mark(5, s);
             } else {
                 if (gl) {
-                    ta.gather = !gl->values_only;
-                    ta.gather_v = gl->values_only;
-                    ta.tmap_pk = &gl->mpk;
+                    ta.gather_v = true;
                     ta.tmap_pv = &gl->mpv;
-                    ta.tmap_bk = &gl->mbk;
                     ta.tmap_bv = &gl->mbv;
                     ta.g = gl->g;
                     ta.st = gl->inl ? &gl->st : nullptr;
@@ -1208,7 +1205,6 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
         if (qp.T == 0)
             return KVR_OK;
         GatherLaunch gl;
-        gl.values_only = true;
         if ((st = encode_gather_map(*p, p->d.v, &gl.mpv)) != KVR_OK ||
             (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK)
             return st;

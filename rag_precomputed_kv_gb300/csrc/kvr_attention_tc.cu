@@ -45,6 +45,15 @@
 // x 64 columns at a time in shared memory and writes them back as whole
 // 128-byte lines (row-per-thread stores touch one line per lane).
 //
+// Values-gathering variant (a prefill whose stitched prefix is not kept): the
+// keys come from the cache, stitched by a keys-only stitch; each value tile
+// that holds prefix rows is gathered from the pool through the span table
+// (runs of 32 consecutive pool rows as one box load, other rows as gather4),
+// which halves the stitch's traffic.  Warp 10 writes the first query rows
+// (from the cache) into the tile that also holds the last prefix rows, and
+// zeroes the rows past a request's keys where a tile reaches past its cache
+// block, whose value rows this variant does not write.
+//
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the CTA
 // records KVR_ERR_TIMEOUT in the pool's error word, all roles leave their
 // loops, in-flight copies and MMAs are drained (again bounded) and TMEM is
@@ -69,15 +78,6 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kRegsLaunchS = 168, kRegsSoftmaxS = 200, kRegsOtherS = 104;
 static_assert(2 * 128 * kRegsSoftmaxS + 128 * kRegsOtherS <= kThreads * kRegsLaunchS, "register split");
-// gathering variant: + 4 rotator warps (10-13, one per SM sub-partition) and
-// 2 idle warps completing the fourth warpgroup; launched at 128 registers a
-// thread, the softmax warpgroups take 152 and the other two give up to 104
-// (setmaxnreg): 2 x 128 x 152 + 2 x 128 x 104 = 512 x 128 (of the splits
-// measured, 168/88 .. 144/112, the fastest)
-constexpr int kThreadsG = 512;
-constexpr int kRotThreads = 128;
-constexpr int kRegsLaunchG = 128, kRegsSoftmaxG = 152, kRegsOtherG = 104;
-static_assert(2 * 128 * kRegsSoftmaxG + 2 * 128 * kRegsOtherG <= kThreadsG * kRegsLaunchG, "register split");
 constexpr int kTileM = 128;      // query rows per tile (two tiles per CTA)
 constexpr int kTileN = 128;      // keys per K/V tile
 constexpr int kD = 128;          // head dim
@@ -107,12 +107,11 @@ constexpr int kBarOEmpty = kBarOFull + 2;         // [2] O_x read by the epilogu
 constexpr int kBarQFull = kBarOEmpty + 2;         // Q tiles landed
 constexpr int kBarQEmpty = kBarQFull + 1;         // all S of the unit done with Q
 constexpr int kBarDrain = kBarQEmpty + 1;
-constexpr int kBarReady = kBarDrain + 1;          // [kSlots] gathered tile rotated / patched (64 arrivals)
 // split units (two-CTA cluster, half h on CTA rank h; rank x merges tile x):
 // the partner's half of this CTA's tile has landed in its shared memory (128
 // arrivals); the partner's MMAs are all done, so its K/V ring and Q tiles may
 // take this CTA's half of the partner's tile
-constexpr int kBarPeerData = kBarReady + kSlots;
+constexpr int kBarPeerData = kBarDrain + 1;
 constexpr int kBarPeerFree = kBarPeerData + 1;
 // the geometry of the CTA's next items, written by the producer warp (two
 // slots): full (1 arrival), read by every consumer warp (one arrival each)
@@ -127,8 +126,7 @@ constexpr int kBarPatched = kBarGeoEmpty + 2;     // [2]
 // wait on the slot's full barrier never runs ahead of the slot's previous load
 constexpr int kBarPatchJob = kBarPatched + 2;     // [2]
 constexpr int kNumBars = kBarPatchJob + 2;
-constexpr int kOffMeta = kOffBar + 8 * kNumBars;  // [2][128] int: rotation of each row of the K slots
-constexpr int kOffTmemAddr = kOffMeta + 2 * kTileN * 4;
+constexpr int kOffTmemAddr = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemAddr + 4;
 constexpr int kOffGeo = (kOffAbort + 4 + 15) & ~15;   // [2] Item
 constexpr int kGeoBytes = 128;
@@ -141,7 +139,6 @@ constexpr int kPeerOBytes = kTileM * kD * 2;
 constexpr int kOffPeerML = kOffQ;
 static_assert(kPeerOBytes <= kSlots * kTileBytes && 3 * kTileM * 4 <= 2 * kTileBytes, "peer state");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-constexpr int kNoRotation = INT32_MIN;            // meta value of a row that is not a pool row
 
 // instruction descriptors (kind::f16): D fp32, A and B bf16, M = 128, N = 128
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
@@ -699,12 +696,12 @@ __device__ __forceinline__ void geo_of(const Item &t, Geo &o)
     o.cap = t.w.rq.cap;
     o.kv_row0 = t.w.kv_row0;
 }
-// the kernel's variants: K and V from the stitched cache; both gathered from
-// the pool (keys re-rotated on chip); values gathered, keys from the cache
-constexpr int kModeStitched = 0, kModeGather = 1, kModeGatherV = 2;
-// softmax 8, MMA 1, and the rotators (4) or the patch warp (1)
+// the kernel's variants: K and V from the stitched cache; or K from the cache
+// and the prefix values gathered from the pool
+constexpr int kModeStitched = 0, kModeGatherV = 1;
+// softmax 8, MMA 1, and the patch warp (values-gathering variant)
 template <int kM>
-constexpr uint32_t geo_consumer_warps() { return kM == kModeGather ? 13u : kM == kModeGatherV ? 10u : 9u; }
+constexpr uint32_t geo_consumer_warps() { return kM == kModeGatherV ? 10u : 9u; }
 
 // The value tile j of a values-gathering item that is patched on chip: it
 // holds the first query rows after prefix rows from the pool, or it reaches
@@ -732,16 +729,15 @@ __device__ __forceinline__ Item item_at(const AttnArgs &a, const DevReq *reqs, i
 }  // namespace
 
 template <int kM>
-__global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     k_attention_tc(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnArgs a,
                    const __grid_constant__ ReqTable rt, const int n_blocks,
-                   const __grid_constant__ CUtensorMap tmpk, const __grid_constant__ CUtensorMap tmpv,
-                   const __grid_constant__ CUtensorMap tmbk, const __grid_constant__ CUtensorMap tmbv,
+                   const __grid_constant__ CUtensorMap tmpv, const __grid_constant__ CUtensorMap tmbv,
                    const __grid_constant__ GatherArgs g, const __grid_constant__ SpanTable st,
                    const __grid_constant__ CUtensorMap tmo)
 {
-    constexpr bool kG = kM == kModeGather, kV = kM == kModeGatherV;
+    constexpr bool kV = kM == kModeGatherV;
     const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -783,9 +779,8 @@ __global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
         for (int i = 0; i < kNumBars; ++i) {
             const bool wg = (i >= kBarPFull && i < kBarPFull + 2) || (i >= kBarOEmpty && i < kBarOEmpty + 2) ||
                             i == kBarPeerData;
-            const bool rot = i >= kBarReady && i < kBarReady + kSlots;
             const bool geo_empty = i >= kBarGeoEmpty && i < kBarGeoEmpty + 2;
-            mbar_init(bar(i), wg ? 128u : rot ? (uint32_t)kRotThreads : geo_empty ? geo_consumer_warps<kM>() : 1u);
+            mbar_init(bar(i), wg ? 128u : geo_empty ? geo_consumer_warps<kM>() : 1u);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -798,12 +793,7 @@ __global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
         prefetch_tmap(&tmv);
         if (a.out_tma)
             prefetch_tmap(&tmo);
-        if constexpr (kG) {
-            prefetch_tmap(&tmpk);
-            prefetch_tmap(&tmpv);
-            prefetch_tmap(&tmbk);
-            prefetch_tmap(&tmbv);
-        } else if constexpr (kV) {
+        if constexpr (kV) {
             prefetch_tmap(&tmpv);
             prefetch_tmap(&tmbv);
         }
@@ -814,20 +804,9 @@ __global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
     cluster_sync();   // the partner CTA's barriers are initialised before any remote arrive
     const uint32_t tmem = *tmem_slot;
     // each role's branch starts by setting its warp's register count, for
-    // whole warpgroups (0-1: softmax; 2: producer, MMA and rotators or idle
-    // warps; 3, gathering variant: rotators and two idle warps)
-    auto regs_softmax = [] {
-        if constexpr (kG)
-            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmaxG));
-        else
-            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmaxS));
-    };
-    auto regs_other = [] {
-        if constexpr (kG)
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOtherG));
-        else
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOtherS));
-    };
+    // whole warpgroups (0-1: softmax; 2: producer, MMA, patch or idle warps)
+    auto regs_softmax = [] { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmaxS)); };
+    auto regs_other = [] { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOtherS)); };
     // setup above overlaps the previous kernel's tail; its outputs (the
     // stitched cache, the rotated queries) are read only from here on
     pdl_wait_prerequisites();
@@ -1269,7 +1248,7 @@ __global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
                     while (!mbar_try_wait(bar(kBarQFull), (nq - 1) & 1) && globaltimer() - t0 < kWaitNs) {
                     }
             }
-        } else if constexpr (!kG) {
+        } else {
             // ====== stitched producer: the whole warp computes each item's
             // geometry (request table in registers), lane 0 waits and issues ======
             int tt = 0, nq = 0, gk = 0;
@@ -1362,150 +1341,6 @@ __global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
                     while (!mbar_try_wait(bar(kBarQFull), (nq - 1) & 1) && globaltimer() - t0 < kWaitNs) {
                     }
             }
-        } else {
-            // ====== gathering producer: Q as above (lane 0); each K/V tile is 128
-            // stitched rows resolved through the span table, lane i loading rows
-            // 4i..4i+3 with one gather4 per 64-column panel ======
-            int tt = 0, nq = 0, gk = 0;
-            bool ok = true;
-            const DevSpan *spans = g.spans ? g.spans : st.spans;
-            int *meta = reinterpret_cast<int *>(smem + kOffMeta);
-            const int64_t e_rows = (int64_t)a.n_layers * a.n_kv_heads * g.entry_len;   // pool rows per entry
-            ReqRegs rr;
-            rr.load(a, reqs, lane);
-            Item nxt;
-            if ((int)blockIdx.x < n_items) {
-                nxt = item_at(a, reqs, n_blocks, blockIdx.x, &rr, lane);
-                if (lane == 0)
-                    ok = geo_put(0, nxt);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-            }
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
-                const Item itm = nxt;
-                const Unit &w = itm.w;
-                // the next item's geometry once this item's loads are issued
-                // (published for the other roles, its Q brought into L2)
-                auto publish_next = [&]() -> bool {
-                    if (it + (int)gridDim.x >= n_items)
-                        return true;
-                    nxt = item_at(a, reqs, n_blocks, it + gridDim.x, &rr, lane);
-                    bool okp = true;
-                    if (lane == 0) {
-                        okp = geo_put(gk + 1, nxt);
-                        if (okp && nxt.je > nxt.jb)
-                            for (int x = 0; x < (nxt.w.n_t[1] > 0 ? 2 : 1); ++x) {
-                                tma_prefetch_2d(&tmq, 0, nxt.w.q_row0 + x * kTileM);
-                                tma_prefetch_2d(&tmq, 64, nxt.w.q_row0 + x * kTileM);
-                            }
-                    }
-                    return __shfl_sync(0xffffffffu, okp, 0);
-                };
-                if (itm.je <= itm.jb) {
-                    ok = publish_next();
-                    continue;
-                }
-                if (lane == 0) {
-                    if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
-                        ok = false;
-                    } else {
-                        const int nqt = w.n_t[1] > 0 ? 2 : 1;
-                        mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
-                        for (int x = 0; x < nqt; ++x) {
-                            const uint32_t dst = sbase + kOffQ + x * kTileBytes;
-                            tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
-                            tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
-                        }
-                    }
-                }
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    ok = false;
-                    break;
-                }
-                ++nq;
-                const int s_end = w.rq.span_end;
-                const int prefix = w.rq.prefix;   // per-row reads stay in a register
-                const int64_t lh_row = (int64_t)w.lh * g.entry_len;    // (layer, kv-head) block inside an entry
-                const bool maps = w.lh == 0 && w.row0[0] == 0 && (g.pos_ids || g.src_map);
-                int cur = w.rq.span0;
-                int rows[4] = {0, 0, 0, 0};
-                bool run32 = false;   // this lane's 32-row group is 32 consecutive pool rows
-                for (int i = 0; i < 2 * (itm.je - itm.jb); ++i, ++tt) {
-                    const int slot = tt % kSlots;
-                    bool okw = true;
-                    if (tt >= kSlots)
-                        okw = mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag);
-                    if (!__all_sync(0xffffffffu, okw)) {
-                        ok = false;
-                        break;
-                    }
-                    if ((i & 1) == 0) {
-                        // K tile j: resolve its rows (the V tile that follows reuses them)
-                        const int j = itm.jb + (i >> 1);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int rr = j * kTileN + 4 * lane + k;
-                            int d = kNoRotation;
-                            rows[k] = 0;   // rows past the prefix: any pool row (patched on chip)
-                            if (rr < prefix) {
-                                while (cur + 1 < s_end && spans[cur].row + spans[cur].len <= rr)
-                                    ++cur;
-                                const DevSpan &sp = spans[cur];
-                                const int off = rr - sp.row;
-                                rows[k] = (int)((int64_t)sp.src * e_rows + lh_row + sp.start + off);
-                                d = sp.dstep ? sp.delta + off : sp.delta;
-                                if (maps) {
-                                    if (g.pos_ids)
-                                        g.pos_ids[sp.flat0 + off] = sp.pos0 + off;
-                                    if (g.src_map) {
-                                        g.src_map[2 * (sp.flat0 + off)] = sp.src;
-                                        g.src_map[2 * (sp.flat0 + off) + 1] = sp.start + off;
-                                    }
-                                }
-                            }
-                            meta[(slot >> 1) * kTileN + 4 * lane + k] = d;
-                        }
-                        // a group of 8 lanes whose 32 rows are consecutive pool rows takes
-                        // one 32-row box load per panel instead of eight gather4s
-                        const int last = __shfl_up_sync(0xffffffffu, rows[3], 1);
-                        const bool mine = (j * kTileN + 4 * lane + 3 < prefix) && rows[1] == rows[0] + 1 &&
-                                          rows[2] == rows[0] + 2 && rows[3] == rows[0] + 3 &&
-                                          ((lane & 7) == 0 || rows[0] == last + 1);
-                        const unsigned ball = __ballot_sync(0xffffffffu, mine);
-                        run32 = ((ball >> (lane & ~7)) & 0xffu) == 0xffu;
-                    }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
-                    __syncwarp();
-                    const uint32_t dst = sbase + kOffKV + slot * kTileBytes + (uint32_t)(4 * lane) * 128u;
-                    if (run32) {
-                        if ((lane & 7) == 0) {
-                            const CUtensorMap *map = (i & 1) ? &tmbv : &tmbk;
-                            tma_load_2d(dst, map, 0, rows[0], bar(kBarFull + slot));
-                            tma_load_2d(dst + kPanelBytes, map, 64, rows[0], bar(kBarFull + slot));
-                        }
-                    } else {
-                        const CUtensorMap *map = (i & 1) ? &tmpv : &tmpk;
-                        tma_gather4(dst, map, 0, rows, bar(kBarFull + slot));
-                        tma_gather4(dst + kPanelBytes, map, 64, rows, bar(kBarFull + slot));
-                    }
-                }
-                if (ok)
-                    ok = publish_next();
-            }
-            if (!ok)
-                flag_timeout(a.err, abort_flag);
-            // drain: every issued copy lands before the CTA leaves
-            if (lane == 0) {
-                const uint64_t t0 = globaltimer();
-                for (int k = (tt > kSlots ? tt - kSlots : 0); k < tt; ++k)
-                    while (!mbar_try_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1) &&
-                           globaltimer() - t0 < kWaitNs) {
-                    }
-                if (nq > 0)
-                    while (!mbar_try_wait(bar(kBarQFull), (nq - 1) & 1) && globaltimer() - t0 < kWaitNs) {
-                    }
-            }
         }
     } else if (warp == 9) {
         regs_other();
@@ -1538,7 +1373,7 @@ __global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
                 umma_commit(lead, bar(kBarSFull + x));
             };
             auto wait_kv = [&](int k) -> bool {
-                if (!mbar_wait(bar((kG ? kBarReady : kBarFull) + k % kSlots), (k / kSlots) & 1, abort_flag))
+                if (!mbar_wait(bar(kBarFull + k % kSlots), (k / kSlots) & 1, abort_flag))
                     return false;
                 tc_fence_after();
                 return true;
@@ -1653,131 +1488,6 @@ __global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
             if (ok && drained && peer_wait >= 0 && lane == 0)
                 mbar_arrive_remote(mapa_rank(bar(kBarPeerFree), (uint32_t)(1 - peer_wait)));
         }
-    } else if (kG && warp < 14) {
-        regs_other();
-        // =================== rotator (gathering variant, warps 10-13) ===================
-        // Thread t owns 16-byte chunk p = t % 8 of each row half (elements
-        // [8p, 8p+8) and their RoPE partners [64 + 8p, ...)) in rows t / 8 + 16k.
-        // Pool rows of a K tile are turned by their span's delta (the same
-        // arithmetic as the stitch kernel); rows past the prefix are the query
-        // rows (already rotated and appended to the cache by the query
-        // prologue) and zero padding, in both the K and the V tile.
-        const int t = threadIdx.x - 10 * 32;
-        const int p = t & 7, r0 = t >> 3;
-        const int *meta = reinterpret_cast<const int *>(smem + kOffMeta);
-        const __nv_bfloat16 *ck = static_cast<const __nv_bfloat16 *>(a.cache_k);
-        const __nv_bfloat16 *cv = static_cast<const __nv_bfloat16 *>(a.cache_v);
-        int tt = 0;
-        bool ok = true;
-        // (cos, sin) of the rotation last used: a span's rows share one delta,
-        // so the tables are read again only where the delta changes
-        int d_cur = kNoRotation;
-        float c[8], sn[8];
-        int gk = 0;
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
-            // the few fields the loop needs, as scalars (the item struct would
-            // otherwise be read from the stack frame on every row)
-            int jb, je, prefix, n_valid;
-            int64_t kv_row0;
-            {
-                const Geo *gp = geo_wait(gk);
-                if (!gp) {
-                    ok = false;
-                    break;
-                }
-                jb = gp->jb;
-                je = gp->je;
-                prefix = gp->prefix;
-                n_valid = gp->n_valid;
-                kv_row0 = gp->kv_row0;
-                geo_done(gk);
-            }
-            for (int j = jb; j < je; ++j, tt += 2) {
-                const int sk = tt % kSlots, sv = (tt + 1) % kSlots;
-                if (!mbar_wait(bar(kBarFull + sk), (tt / kSlots) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t kb = sbase + kOffKV + sk * kTileBytes;
-                // four rows at a time: all loads first, then the rotations, then the stores
-                for (int k0 = 0; k0 < kTileN / 16; k0 += 4) {
-                    uint4 lo[4], hi[4];
-                    int dd[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int r = r0 + 16 * (k0 + q), rr = j * kTileN + r;
-                        const uint32_t lo_a = kb + r * 128 + ((p ^ (r & 7)) << 4);
-                        dd[q] = kNoRotation;
-                        if (rr < prefix) {
-                            dd[q] = meta[(sk >> 1) * kTileN + r];
-                            lo[q] = ld_shared_v4(lo_a);
-                            hi[q] = ld_shared_v4(lo_a + kPanelBytes);
-                        } else if (rr < n_valid) {
-                            const __nv_bfloat16 *src = ck + (kv_row0 + rr) * kD + 8 * p;
-                            lo[q] = __ldg(reinterpret_cast<const uint4 *>(src));
-                            hi[q] = __ldg(reinterpret_cast<const uint4 *>(src + kD / 2));
-                        } else {
-                            lo[q] = make_uint4(0u, 0u, 0u, 0u);
-                            hi[q] = lo[q];
-                        }
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (dd[q] == kNoRotation)
-                            continue;
-                        if (dd[q] != d_cur) {
-                            d_cur = dd[q];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float2 cs = rope_cs(a.rope, kD / 2, d_cur, rope_pair(a.interleaved, kD, 8, p, e));
-                                c[e] = cs.x;
-                                sn[e] = cs.y;
-                            }
-                        }
-                        if (a.interleaved)
-                            rotate_bf16x8_il(lo[q], hi[q], c, sn);
-                        else
-                            rotate_bf16x8(lo[q], hi[q], c, sn);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int r = r0 + 16 * (k0 + q);
-                        const uint32_t lo_a = kb + r * 128 + ((p ^ (r & 7)) << 4);
-                        st_shared_v4(lo_a, lo[q].x, lo[q].y, lo[q].z, lo[q].w);
-                        st_shared_v4(lo_a + kPanelBytes, hi[q].x, hi[q].y, hi[q].z, hi[q].w);
-                    }
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(bar(kBarReady + sk));
-                if (!mbar_wait(bar(kBarFull + sv), ((tt + 1) / kSlots) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t vb = sbase + kOffKV + sv * kTileBytes;
-                if ((j + 1) * kTileN > prefix) {
-                    for (int k = 0; k < kTileN / 16; ++k) {
-                        const int r = r0 + 16 * k, rr = j * kTileN + r;
-                        if (rr < prefix)
-                            continue;
-                        const uint32_t lo_a = vb + r * 128 + ((p ^ (r & 7)) << 4), hi_a = lo_a + kPanelBytes;
-                        if (rr < n_valid) {
-                            const __nv_bfloat16 *src = cv + (kv_row0 + rr) * kD + 8 * p;
-                            const uint4 lo = __ldg(reinterpret_cast<const uint4 *>(src));
-                            const uint4 hi = __ldg(reinterpret_cast<const uint4 *>(src + kD / 2));
-                            st_shared_v4(lo_a, lo.x, lo.y, lo.z, lo.w);
-                            st_shared_v4(hi_a, hi.x, hi.y, hi.z, hi.w);
-                        } else {
-                            st_shared_v4(lo_a, 0u, 0u, 0u, 0u);
-                            st_shared_v4(hi_a, 0u, 0u, 0u, 0u);
-                        }
-                    }
-                    fence_proxy_async_smem();
-                }
-                mbar_arrive(bar(kBarReady + sv));
-            }
-        }
-        if (!ok)
-            flag_timeout(a.err, abort_flag);
     } else if (kV && warp == 10) {
         regs_other();
         // ========== patch (values-gathering variant, warp 10) ==========
@@ -1844,7 +1554,7 @@ __global__ void __launch_bounds__(kM == kModeGather ? kThreadsG : kThreads, 1)
         if (!ok)
             flag_timeout(a.err, abort_flag);
     } else {
-        regs_other();   // warps 10-11 (stitched) or 14-15 (gathering): no role
+        regs_other();   // warps 10-11 (stitched) or 11 (values gathered): no role
     }
 
     tc_fence_before();
@@ -1875,7 +1585,7 @@ static cudaError_t set_smem_attr()
             cudaFuncAttributes fa{};
             if ((e = cudaFuncGetAttributes(&fa, k_attention_tc<kM>)) != cudaSuccess)
                 return e;
-            if (fa.numRegs != (kM == kModeGather ? kRegsLaunchG : kRegsLaunchS))
+            if (fa.numRegs != kRegsLaunchS)
                 return cudaErrorInvalidConfiguration;
         }
         e = cudaFuncSetAttribute(k_attention_tc<kM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -1901,7 +1611,7 @@ static bool pairs_fit(int n_sms)
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(n_sms);
-        cfg.blockDim = dim3(kM == kModeGather ? kThreadsG : kThreads);
+        cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = kSmemBytes;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -1919,16 +1629,13 @@ static bool pairs_fit(int n_sms)
     return fit[dev].load(std::memory_order_acquire) == 1;
 }
 
-bool attention_tc_pairs_fit(int n_sms, bool gather)
-{
-    // the values-gathering variant has the stitched variant's block and shared memory
-    return gather ? pairs_fit<kModeGather>(n_sms) : pairs_fit<kModeStitched>(n_sms);
-}
+// (the values-gathering variant has the same block and shared memory)
+bool attention_tc_pairs_fit(int n_sms) { return pairs_fit<kModeStitched>(n_sms); }
 
 template <int kM>
 static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool pairs, cudaStream_t s)
 {
-    constexpr bool kG = kM == kModeGather, kV = kM == kModeGatherV;
+    constexpr bool kV = kM == kModeGatherV;
     cudaError_t e = set_smem_attr<kM>();
     if (e != cudaSuccess)
         return e;
@@ -1937,7 +1644,7 @@ static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool
     static const SpanTable no_spans{};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kG ? kThreadsG : kThreads);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -1959,11 +1666,9 @@ static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool
     return cudaLaunchKernelEx(&cfg, k_attention_tc<kM>, *static_cast<const CUtensorMap *>(ta.tmap_q),
                               *static_cast<const CUtensorMap *>(ta.tmap_k),
                               *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base, *ta.rt, ta.n_m_blocks,
-                              kG ? *static_cast<const CUtensorMap *>(ta.tmap_pk) : no_map,
-                              kG || kV ? *static_cast<const CUtensorMap *>(ta.tmap_pv) : no_map,
-                              kG ? *static_cast<const CUtensorMap *>(ta.tmap_bk) : no_map,
-                              kG || kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv) : no_map,
-                              kG || kV ? ta.g : no_gather, (kG || kV) && ta.st ? *ta.st : no_spans,
+                              kV ? *static_cast<const CUtensorMap *>(ta.tmap_pv) : no_map,
+                              kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv) : no_map,
+                              kV ? ta.g : no_gather, kV && ta.st ? *ta.st : no_spans,
                               ta.base.out_tma ? *static_cast<const CUtensorMap *>(ta.tmap_out) : no_map);
 }
 
@@ -1982,9 +1687,8 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
     // CTAs 2i and 2i + 1 of the last round when n_full is a multiple of the grid
     if (pairs && ((grid & 1) || ta.base.n_full % grid != 0))
         return cudaErrorInvalidValue;
-    return ta.gather     ? launch_variant<kModeGather>(ta, grid, pdl, pairs, s)
-           : ta.gather_v ? launch_variant<kModeGatherV>(ta, grid, pdl, pairs, s)
-                         : launch_variant<kModeStitched>(ta, grid, pdl, pairs, s);
+    return ta.gather_v ? launch_variant<kModeGatherV>(ta, grid, pdl, pairs, s)
+                       : launch_variant<kModeStitched>(ta, grid, pdl, pairs, s);
 }
 
 }  // namespace kvr

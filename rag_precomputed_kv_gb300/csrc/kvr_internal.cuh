@@ -47,9 +47,8 @@ __device__ __forceinline__ float2 rope_cs(const float2 *__restrict__ tab, int ha
 }
 
 // RoPE rotation of 8 bf16 pairs: lo holds elements [8j, 8j+8) of a row, hi
-// their partners [D/2 + 8j, ...); (c, s) of each pair.  The one definition of
-// the key re-rotation (the stitch kernel and the gathering attention kernel
-// produce the same bits).
+// their partners [D/2 + 8j, ...); (c, s) of each pair.  The stitch kernel's
+// key re-rotation for bf16 caches.
 // Per pair: x' = fma(x, c, -(y s)), y' = fma(x, s, y c), rounded once to bf16;
 // computed two lanes at a time with the packed fp32 instructions (each lane
 // is the IEEE operation of the scalar form).
@@ -141,7 +140,7 @@ struct alignas(16) DevReq {
     int32_t q_off;       // first query token (token axis of q / out)
     int32_t q_len;       // Lq_b
     int32_t unit0;       // first (layer, kv-head, 256-row block) unit (tensor-core path)
-    int32_t span0;       // first non-empty span of this request (gathering attention)
+    int32_t span0;       // first non-empty span of this request (values-gathering attention)
     int32_t span_end;    // one past its last
     int32_t tile0;       // decode step over all SMs: the request's first 128-key tile
     int32_t pad_[2];
@@ -253,9 +252,9 @@ cudaError_t launch_attention_simt(const AttnArgs &a, const ReqTable &rt, int dty
 // Tensor-core attention (bf16, head_dim 128).  `tmaps` points to two
 // CUtensorMap objects (K then V) describing the cache as a 2-D
 // [rows, head_dim] bf16 tensor.
-// The tensor-core attention's gathering variant (kvr_prefill): K/V tiles are
-// gathered from the pool, seen as a 2-D [entries * L * H_kv * entry_len, D]
-// tensor, through the batch's span table; keys are re-rotated on chip.
+// The tensor-core attention's values-gathering variant (kvr_prefill): V tiles
+// of prefix rows are gathered from the pool, seen as a 2-D
+// [entries * L * H_kv * entry_len, D] tensor, through the batch's span table.
 struct SpanTable {
     DevSpan spans[kInlineEntries];
 };
@@ -263,8 +262,6 @@ struct GatherArgs {
     const DevSpan *spans;       // the batch's spans in global memory, or NULL: the SpanTable parameter
     int32_t n_spans;            // non-empty spans of the batch (request b's start at DevReq::span0)
     int32_t entry_len;          // pool tokens per entry
-    int32_t *pos_ids;           // optional position ids / source map, as kvr_assemble writes them
-    int32_t *src_map;
 };
 
 struct TcAttnArgs {
@@ -275,12 +272,9 @@ struct TcAttnArgs {
     const void *tmap_v;
     int32_t n_m_blocks;         // total 256-row query blocks over all requests
     int32_t n_sms;              // persistent grid size bound
-    bool gather;                // K/V from the pool (tmap_pk / tmap_pv, g, st) instead of the cache
     bool gather_v;              // V tiles of prefix rows from the pool (tmap_pv, tmap_bv, g, st), K from the cache
-    const void *tmap_pk;        // pool K and V as [rows, D] with a one-row box (gather4)
-    const void *tmap_pv;
-    const void *tmap_bk;        // the same with a 32-row box (runs of consecutive pool rows)
-    const void *tmap_bv;
+    const void *tmap_pv;        // pool V as [rows, D] with a one-row box (gather4)
+    const void *tmap_bv;        // the same with a 32-row box (runs of consecutive pool rows)
     GatherArgs g;
     const SpanTable *st;
     const void *tmap_out;       // out as [L*T][H_q][D] with a (64, G, 32 / G) box (base.out_tma)
@@ -329,8 +323,8 @@ int decode_stream_part_floats();
 cudaError_t launch_wait_selftest(int *err, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const void *tmap_k, const void *tmap_v,
                                     const DecodeIO &io, cudaStream_t s);
-// Whether `n_sms` CTAs of the attention kernel (gathering variant or not) can
-// be resident at once as two-CTA clusters.
-bool attention_tc_pairs_fit(int n_sms, bool gather);
+// Whether `n_sms` CTAs of the attention kernel (either variant) can be
+// resident at once as two-CTA clusters.
+bool attention_tc_pairs_fit(int n_sms);
 
 }  // namespace kvr

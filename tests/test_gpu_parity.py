@@ -268,8 +268,8 @@ def test_pool_keys_kept_before_rope(variant):
 def test_pool_with_interleaved_rope_pairs(variant):
     """A pool registered with KVR_POOL_ROPE_INTERLEAVED: every rotation
     (stitched keys, query keys, query heads; in the stitch kernel, the query
-    prologue, the CUDA-core attention and the gathering attention's rotator)
-    pairs (x_2i, x_2i+1)."""
+    prologue and the CUDA-core attention, and in the keys-only stitch of the
+    skip-prefix-cache prefill) pairs (x_2i, x_2i+1)."""
     import torch
     pid = EDGE_BASE.n_chunks
     lists = [[[pid, 0, 5], [0, 0, 1], [1, 95, 96], [2, 10, 50], [2, 30, 70]], [],
@@ -294,7 +294,7 @@ def test_pool_with_interleaved_rope_pairs(variant):
         cfg, reqs, prefill, skip = W.CONFIGS[2], None, True, True
     case = Case(cfg, reqs=reqs, keys_unrotated=unrot, rope_interleaved=True)
     _ok(run_parity_case(cfg=cfg, case=case, prefill=prefill, skip_prefix=skip, **kw))
-    if skip:    # the gathering attention rotates like the stitch kernel: same bits
+    if skip:    # keys from the same stitch kernel, values the pool's bytes: same bits
         got = case.out.clone()
         case.out.fill_(float("nan"))
         case.run(prefill=True)
@@ -331,7 +331,7 @@ def test_pool_in_pinned_host_memory(name):
         assert torch.equal(g_.view(torch.int16), w_.view(torch.int16))
     ok, mx, rel = attn_within_tolerance(to_np64(case.out), to_np64(want[0]), cfg.dtype)
     assert ok, (mx, rel)
-    with pytest.raises(kvr.KvrError) as e:      # the gathering attention wants device memory
+    with pytest.raises(kvr.KvrError) as e:      # the values-gathering attention wants device memory
         case.run(prefill=True, skip_prefix=True)
     assert e.value.status == 3
 
