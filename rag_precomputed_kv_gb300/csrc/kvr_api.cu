@@ -760,10 +760,10 @@ kvr_status encode_gather_map(const kvr_pool &p, const void *base, CUtensorMap *m
 }
 
 // What the values-gathering attention needs beyond a query-attention launch:
-// the pool's values as gather4 (one-row box) and 32-row box sources, and the
-// span table.
+// the pool's values as gather4 (one-row box) and 32-, 16- and 8-row box
+// sources, and the span table.
 struct GatherLaunch {
-    CUtensorMap mpv, mbv;
+    CUtensorMap mpv, mbv, mbv16, mbv8;
     GatherArgs g{};
     SpanTable st;
     bool inl = false;
@@ -1084,6 +1084,8 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
                     ta.gather_v = true;
                     ta.tmap_pv = &gl->mpv;
                     ta.tmap_bv = &gl->mbv;
+                    ta.tmap_bv16 = &gl->mbv16;
+                    ta.tmap_bv8 = &gl->mbv8;
                     ta.g = gl->g;
                     ta.st = gl->inl ? &gl->st : nullptr;
                 }
@@ -1206,7 +1208,9 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
             return KVR_OK;
         GatherLaunch gl;
         if ((st = encode_gather_map(*p, p->d.v, &gl.mpv)) != KVR_OK ||
-            (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK)
+            (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK ||
+            (st = encode_gather_map(*p, p->d.v, &gl.mbv16, 16)) != KVR_OK ||
+            (st = encode_gather_map(*p, p->d.v, &gl.mbv8, 8)) != KVR_OK)
             return st;
         for (int b = 0; b < batch; ++b) {
             qp.rq[b].span0 = ap.span0[b];

@@ -734,6 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnArgs a,
                    const __grid_constant__ ReqTable rt, const int n_blocks,
                    const __grid_constant__ CUtensorMap tmpv, const __grid_constant__ CUtensorMap tmbv,
+                   const __grid_constant__ CUtensorMap tmbv16, const __grid_constant__ CUtensorMap tmbv8,
                    const __grid_constant__ GatherArgs g, const __grid_constant__ SpanTable st,
                    const __grid_constant__ CUtensorMap tmo)
 {
@@ -796,6 +797,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kV) {
             prefetch_tmap(&tmpv);
             prefetch_tmap(&tmbv);
+            prefetch_tmap(&tmbv16);
+            prefetch_tmap(&tmbv8);
         }
     }
     tc_fence_before();
@@ -1099,10 +1102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kV) {
             // ====== values-gathering producer: Q and the K tiles as in the
             // stitched variant; a V tile with prefix rows comes from the pool
-            // (lane i: rows 4i..4i+3, resolved through the span table; a group
-            // of 8 lanes whose 32 rows are consecutive pool rows takes one
-            // 32-row box load per panel, other lanes a gather4 each), later V
-            // tiles from the cache block ======
+            // (lane i: rows 4i..4i+3, resolved through the span table; runs of
+            // consecutive pool rows as 32-, 16- or 8-row box loads, other lanes
+            // a gather4 each), later V tiles from the cache block ======
             int tt = 0, nq = 0, gk = 0;
             bool ok = true;
             const DevSpan *spans = g.spans ? g.spans : st.spans;
@@ -1141,7 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int n_loads = 2 * (itm.je - itm.jb);
                     int rows[4] = {0, 0, 0, 0};
-                    bool run32 = false;   // this lane's 32-row group is 32 consecutive pool rows
+                    int box_lanes = 1;    // lanes of this lane's box-load group (1: a gather4 of its own)
                     for (int i = 0; i <= n_loads; ++i) {
                         if (i == 2 && lane == 0) {   // Q after K_0 and V_0, as in the stitched variant
                             if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
@@ -1191,22 +1193,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         rows[k] = (int)((int64_t)sp.src * e_rows + lh_row + sp.start + (r - sp.row));
                                     }
                                 }
+                                // aligned groups of 8, 4 or 2 lanes whose rows are consecutive
+                                // pool rows take one 32-, 16- or 8-row box load per panel,
+                                // issued by the group's first lane; other lanes a gather4
                                 const int last = __shfl_up_sync(0xffffffffu, rows[3], 1);
-                                const bool mine = (j * kTileN + 4 * lane + 3 < prefix) && rows[1] == rows[0] + 1 &&
-                                                  rows[2] == rows[0] + 2 && rows[3] == rows[0] + 3 &&
-                                                  ((lane & 7) == 0 || rows[0] == last + 1);
-                                const unsigned ball = __ballot_sync(0xffffffffu, mine);
-                                run32 = ((ball >> (lane & ~7)) & 0xffu) == 0xffu;
+                                const unsigned b4 = __ballot_sync(
+                                    0xffffffffu, (j * kTileN + 4 * lane + 3 < prefix) && rows[1] == rows[0] + 1 &&
+                                                     rows[2] == rows[0] + 2 && rows[3] == rows[0] + 3);
+                                const unsigned bc = __ballot_sync(0xffffffffu, rows[0] == last + 1);
+                                box_lanes = 1;
+#pragma unroll
+                                for (int sz = 8; sz >= 2; sz >>= 1) {
+                                    const int g0 = lane & ~(sz - 1);
+                                    const unsigned m = ((1u << sz) - 1u) << g0, inner = m & ~(1u << g0);
+                                    if (box_lanes == 1 && (b4 & m) == m && (bc & inner) == inner)
+                                        box_lanes = sz;
+                                }
                             }
                         } else {
                             if (lane == 0)
                                 mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
                             __syncwarp();
                             const uint32_t d4 = dst + (uint32_t)(4 * lane) * 128u;
-                            if (run32) {
-                                if ((lane & 7) == 0) {
-                                    tma_load_2d(d4, &tmbv, 0, rows[0], bar(kBarFull + slot));
-                                    tma_load_2d(d4 + kPanelBytes, &tmbv, 64, rows[0], bar(kBarFull + slot));
+                            if (box_lanes > 1) {
+                                if ((lane & (box_lanes - 1)) == 0) {
+                                    const CUtensorMap *map = box_lanes == 8 ? &tmbv : box_lanes == 4 ? &tmbv16 : &tmbv8;
+                                    tma_load_2d(d4, map, 0, rows[0], bar(kBarFull + slot));
+                                    tma_load_2d(d4 + kPanelBytes, map, 64, rows[0], bar(kBarFull + slot));
                                 }
                             } else {
                                 tma_gather4(d4, &tmpv, 0, rows, bar(kBarFull + slot));
@@ -1668,6 +1681,8 @@ static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool
                               *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base, *ta.rt, ta.n_m_blocks,
                               kV ? *static_cast<const CUtensorMap *>(ta.tmap_pv) : no_map,
                               kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv) : no_map,
+                              kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv16) : no_map,
+                              kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv8) : no_map,
                               kV ? ta.g : no_gather, kV && ta.st ? *ta.st : no_spans,
                               ta.base.out_tma ? *static_cast<const CUtensorMap *>(ta.tmap_out) : no_map);
 }

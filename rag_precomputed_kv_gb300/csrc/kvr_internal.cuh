@@ -274,7 +274,9 @@ struct TcAttnArgs {
     int32_t n_sms;              // persistent grid size bound
     bool gather_v;              // V tiles of prefix rows from the pool (tmap_pv, tmap_bv, g, st), K from the cache
     const void *tmap_pv;        // pool V as [rows, D] with a one-row box (gather4)
-    const void *tmap_bv;        // the same with a 32-row box (runs of consecutive pool rows)
+    const void *tmap_bv;        // the same with a 32-, 16- and 8-row box (runs of consecutive pool rows)
+    const void *tmap_bv16;
+    const void *tmap_bv8;
     GatherArgs g;
     const SpanTable *st;
     const void *tmap_out;       // out as [L*T][H_q][D] with a (64, G, 32 / G) box (base.out_tma)
