@@ -281,12 +281,18 @@ def decode_timing(wl, cfg, dev, steps, warmup, flush):
         step()
     torch.cuda.synchronize()
     n_d = max(20, min(steps, 500))
-    # consecutive steps
+    # consecutive steps, enqueued while the GPU still runs a sleep kernel, so
+    # that they run back to back: a Python call (marshalling + the library's
+    # host work) takes about as long as a batch-1 step, and timed live the
+    # loop would measure the host instead
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     flush()
+    torch.cuda._sleep(DECODE_AHEAD_CYCLES)
     e0.record(stream)
+    h0 = time.perf_counter()
     for _ in range(n_d):
         step()
+    host_us = (time.perf_counter() - h0) / n_d * 1e6
     e1.record(stream)
     torch.cuda.synchronize()
     loop_ms = e0.elapsed_time(e1) / n_d
@@ -305,13 +311,15 @@ def decode_timing(wl, cfg, dev, steps, warmup, flush):
     dec_bytes = int((n_dec.astype(np.int64) + 1).sum()) * L * Hkv * Dh * elt * 2
     hbm = peaks()["hbm_gbs"]
     return {"workload": cfg.name, "us_per_step": round(loop_ms * 1e3, 2), "steps": n_d, "kv_bytes": dec_bytes,
+            "host_us_per_call": round(host_us, 2),
             "gbs": round(dec_bytes / (loop_ms * 1e-3) / 1e9, 1),
             "frac_hbm": round(dec_bytes / (loop_ms * 1e-3) / 1e9 / hbm, 4),
             "us_isolated": round(iso_ms * 1e3, 2),
             "frac_hbm_isolated": round(dec_bytes / (iso_ms * 1e-3) / 1e9 / hbm, 4),
             "what": "kvr_query_attention with one token per request (append at P_b + Lq, attend to all rows); "
-                    "bytes = K and V rows read once; us_per_step: consecutive steps (no flush: the step reads more "
-                    "than the L2 holds), us_isolated: one call after an L2 flush"}
+                    "bytes = K and V rows read once; us_per_step: consecutive steps on the device, enqueued ahead "
+                    "(no flush between them: the step reads more than the L2 holds); host_us_per_call: the Python "
+                    "call that enqueues one step; us_isolated: one call after an L2 flush"}
 
 
 def host_pool_timing(wl, cfg, steps, warmup, flush):
@@ -368,6 +376,10 @@ def host_pool_timing(wl, cfg, steps, warmup, flush):
                     "kvr_query_attention alone, and kvr_prefill (layer-group stitch on a second stream, each "
                     "group's attention beside the next group's stitch)"}
 
+
+# the decode loop's head start: ~30 ms of GPU sleep while the host enqueues
+# up to 500 steps
+DECODE_AHEAD_CYCLES = 1 << 26
 
 LATENCY_CONFIG = 2
 LATENCY_REPS = 200

@@ -45,13 +45,9 @@
  *          head_dim * 2 bytes of device memory (T = query tokens of the
  *          call).  A call with more than the scratch holds waits for the
  *          previous call's attention, frees it and allocates it larger.
- *       5. Decode workspace (a decode step over fewer cache blocks than two
- *          per SM, see kvr_query_attention): two partial-state slots per SM
- *          (16.6 KB each) and one 4-byte arrival count per block of the
- *          call; larger counts are allocated like 4.
- *       6. A pool in pinned host memory: the first kvr_prefill on it creates
+ *       5. A pool in pinned host memory: the first kvr_prefill on it creates
  *          an internal stream and its events (kept until unregister).
- *     kvr_pool_reserve makes 3, 4 and 5 happen up front: afterwards, calls
+ *     kvr_pool_reserve makes 3 and 4 happen up front: afterwards, calls
  *     within the reserved sizes allocate nothing and wait only in the one
  *     case of 3 (8 calls with uploaded tables still queued).  kvr_pool_unregister
  *     synchronizes the handle's work before it frees.
@@ -260,10 +256,7 @@ KVR_API kvr_status kvr_assemble(kvr_pool_t pool, int32_t batch, const int32_t *s
  * blog section 2.3: decoding continues normally on top of the stitched
  * cache) -- on a bf16 pool with head_dim 128 and at most 16 query heads per
  * kv head runs as a single kernel that rotates, appends and attends, each
- * (request, layer, kv-head) block streamed once: one CTA per block, or, with
- * fewer blocks than two per SM, one CTA per SM over equal shares of all the
- * blocks' key tiles (blocks split between CTAs are merged in a fixed order,
- * in the decode workspace).  Other calls on the
+ * (request, layer, kv-head) block streamed once by one CTA.  Other calls on the
  * tensor-core path (bf16, head_dim 128) also write zeros into the V rows
  * between a block's last query row and the end of its last 128-row key tile
  * (rows of the block, never past R_b); a decode step leaves those rows as

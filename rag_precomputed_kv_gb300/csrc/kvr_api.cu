@@ -121,14 +121,6 @@ struct kvr_pool {
     size_t q_rot_cap = 0;
     cudaEvent_t q_rot_done = nullptr;
     bool q_rot_used = false;
-    // decode steps over few blocks (all SMs): partial states of split blocks
-    // and one arrival count per block (zero between calls); dec_done orders
-    // their reuse after the last such step
-    float *dec_ws = nullptr;
-    int *dec_cnt = nullptr;
-    size_t dec_cnt_cap = 0;      // blocks
-    cudaEvent_t dec_done = nullptr;
-    bool dec_used = false;
     // a pool in pinned host memory: kvr_prefill stitches it by layer groups on
     // a second stream, each group's attention overlapping the next group's
     // stitch (which reads over the CPU-GPU link)
@@ -197,37 +189,6 @@ struct kvr_pool {
         }
         if (!s.done && (e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming)) != cudaSuccess)
             return cuda_fail(e, "staging event");
-        return KVR_OK;
-    }
-
-    // The decode workspace for `blocks` cache blocks: the partial-state slots
-    // (two per SM) once, and the arrival counts, zeroed; smaller counts are
-    // freed (after the last step that used them) and allocated again.
-    kvr_status grow_decode_workspace(size_t blocks)
-    {
-        cudaError_t e;
-        if (!dec_ws) {
-            NvtxRange r("kvr.decode_workspace_alloc");
-            if ((e = cudaMalloc(&dec_ws, sizeof(float) * 2 * (size_t)n_sms * decode_stream_part_floats())) !=
-                cudaSuccess)
-                return cuda_fail(e, "decode workspace");
-        }
-        if (dec_cnt_cap < blocks) {
-            NvtxRange r("kvr.decode_workspace_alloc");
-            if (dec_used && (e = cudaEventSynchronize(dec_done)) != cudaSuccess)
-                return cuda_fail(e, "decode workspace wait");
-            if (dec_cnt)
-                cudaFree(dec_cnt);
-            dec_cnt = nullptr;
-            dec_cnt_cap = 0;
-            dec_used = false;
-            if ((e = cudaMalloc(&dec_cnt, sizeof(int) * blocks)) != cudaSuccess ||
-                (e = cudaMemset(dec_cnt, 0, sizeof(int) * blocks)) != cudaSuccess)
-                return cuda_fail(e, "decode workspace counts");
-            dec_cnt_cap = blocks;
-        }
-        if (!dec_done && (e = cudaEventCreateWithFlags(&dec_done, cudaEventDisableTiming)) != cudaSuccess)
-            return cuda_fail(e, "decode workspace event");
         return KVR_OK;
     }
 
@@ -361,10 +322,6 @@ extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
     }
     if (p->q_rot)
         cudaFree(p->q_rot);
-    if (p->dec_done) {
-        cudaEventSynchronize(p->dec_done);
-        cudaEventDestroy(p->dec_done);
-    }
     if (p->side) {
         cudaStreamSynchronize(p->side);
         cudaStreamDestroy(p->side);
@@ -374,10 +331,6 @@ extern "C" kvr_status kvr_pool_unregister(kvr_pool_t p)
     for (cudaEvent_t e : p->part_ev)
         if (e)
             cudaEventDestroy(e);
-    if (p->dec_ws)
-        cudaFree(p->dec_ws);
-    if (p->dec_cnt)
-        cudaFree(p->dec_cnt);
     if (p->rope)
         cudaFree(p->rope);
     if (p->err)
@@ -419,9 +372,6 @@ extern "C" kvr_status kvr_pool_reserve(kvr_pool_t p, int32_t max_batch, int32_t 
     if (use_tensor_cores(*p)) {
         const size_t q_bytes = (size_t)p->d.n_layers * (size_t)max_query_tokens * p->d.n_q_heads * p->d.head_dim * 2;
         if (q_bytes > 0 && (st = p->grow_query_scratch(q_bytes)) != KVR_OK)
-            return st;
-        if (max_batch > 0 &&
-            (st = p->grow_decode_workspace((size_t)max_batch * p->d.n_layers * p->d.n_kv_heads)) != KVR_OK)
             return st;
     }
     return KVR_OK;
@@ -783,9 +733,7 @@ struct QaPlan {
     std::vector<DevSpan> ap;     // the query keys / values as append spans (CUDA-core path)
     std::vector<DevLocal> al;
     bool tc = false, inl = false;
-    bool dec_stream = false;     // decode step over all SMs (k_decode_stream)
     int32_t parts = 1;           // layer groups of a host-pool prefill (attention per group)
-    int64_t dec_tiles = 0;
     CUtensorMap mq, mk, mv, mo;
     ReqTable rt_inl;
     AssembleTables tab;
@@ -931,28 +879,6 @@ static kvr_status qa_stage(kvr_pool *p, QaPlan &pl, cudaStream_t s)
             r.unit0 = (int32_t)u0;
             u0 += ((int64_t)(Hq / Hkv) * r.q_len + 255) / 256 * (LH / pl.parts);
         }
-        // a decode step over fewer blocks than two per SM spreads its 128-key
-        // tiles over every SM (k_decode_stream); the request table holds each
-        // request's first tile
-        if (pl.max_lq == 1 && decode_supported(p->d.dtype, D, Hq / Hkv)) {
-            int64_t tiles = 0, blocks = 0;
-            for (DevReq &r : pl.rq) {
-                r.tile0 = (int32_t)tiles;
-                if (r.q_len > 0) {
-                    tiles += (int64_t)LH * ((r.prefix + 1 + 127) / 128);
-                    blocks += LH;
-                }
-            }
-            if (blocks > 0 && blocks < 2 * (int64_t)p->n_sms && tiles <= INT32_MAX) {
-                if ((st = p->grow_decode_workspace((size_t)batch * LH)) != KVR_OK)
-                    return st;
-                pl.dec_stream = true;
-                pl.dec_tiles = tiles;
-                // the previous stream step's counts are reset by its own kernel
-                if (p->dec_used && (e = cudaStreamWaitEvent(s, p->dec_done, 0)) != cudaSuccess)
-                    return cuda_fail(e, "decode workspace ordering");
-            }
-        }
     }
 
     pl.inl = batch <= kInlineEntries;   // then ap, al have <= batch entries too
@@ -1055,15 +981,7 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
         if (e == cudaSuccess && decode) {
             const DecodeIO io{pl.kq, pl.vq, pl.cache_k, pl.cache_v, pl.at.interleaved};
             p->mark(4, s);
-            if (pl.dec_stream) {
-                NvtxRange r("kvr.k_decode_stream");
-                const DecodeStream ds{p->dec_ws, p->dec_cnt, pl.dec_tiles,
-                                      (int32_t)std::min<int64_t>(p->n_sms, pl.dec_tiles),
-                                      p->d.n_layers * p->d.n_kv_heads};
-                e = launch_decode_stream(pl.at, rt, &pl.mk, &pl.mv, io, ds, s);
-                cudaEventRecord(p->dec_done, s);
-                p->dec_used = true;
-            } else {
+            {
                 NvtxRange r("kvr.k_decode_attention");
                 e = launch_decode_attention(pl.at, rt, &pl.mk, &pl.mv, io, s);
             }
@@ -1330,12 +1248,8 @@ extern "C" kvr_status kvr_check(kvr_pool_t p, void *stream)
     if (w == kDevOk)
         return KVR_OK;
     cudaMemset(p->err, 0, sizeof(int));
-    if (w == kDevTimeout) {
-        // a decode step that gave up may have left arrival counts behind
-        if (p->dec_cnt)
-            cudaMemset(p->dec_cnt, 0, sizeof(int) * p->dec_cnt_cap);
+    if (w == kDevTimeout)
         return fail(KVR_ERR_TIMEOUT, "a kernel's bounded wait ran out");
-    }
     if (w == kDevBadInput)
         return fail(KVR_ERR_DEVICE_CHECK, "an attention row's softmax denominator was not finite and positive "
                                           "(NaN or infinity in the query heads or the keys it attends to)");

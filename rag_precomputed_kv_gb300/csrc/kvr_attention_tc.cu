@@ -648,8 +648,7 @@ __device__ __forceinline__ Unit unit_at_warp(const AttnArgs &a, const ReqRegs &r
     rq.unit0 = __shfl_sync(0xffffffffu, k ? rr.r[1].unit0 : rr.r[0].unit0, src);
     rq.span0 = __shfl_sync(0xffffffffu, k ? rr.r[1].span0 : rr.r[0].span0, src);
     rq.span_end = __shfl_sync(0xffffffffu, k ? rr.r[1].span_end : rr.r[0].span_end, src);
-    rq.tile0 = 0;
-    rq.pad_[0] = rq.pad_[1] = 0;
+    rq.pad_[0] = rq.pad_[1] = rq.pad_[2] = 0;
     return unit_geometry(a, rq, b, u);
 }
 

@@ -1,6 +1,6 @@
-// kvr_decode_common.cuh -- pieces shared by the decode-step kernels: tile
-// geometry, bounded mbarrier waits, TMA loads, and the warp-level bf16 MMA
-// (mma.sync m16n8k16 with ldmatrix operands) they stream tiles through.
+// kvr_decode_common.cuh -- pieces of the decode-step kernel: tile geometry,
+// bounded mbarrier waits, TMA loads, and the warp-level bf16 MMA (mma.sync
+// m16n8k16 with ldmatrix operands) it streams tiles through.
 #pragma once
 
 #include <cuda.h>

@@ -142,8 +142,7 @@ struct alignas(16) DevReq {
     int32_t unit0;       // first (layer, kv-head, 256-row block) unit (tensor-core path)
     int32_t span0;       // first non-empty span of this request (values-gathering attention)
     int32_t span_end;    // one past its last
-    int32_t tile0;       // decode step over all SMs: the request's first 128-key tile
-    int32_t pad_[2];
+    int32_t pad_[3];
 };
 static_assert(sizeof(DevReq) == 48, "request table layout");
 
@@ -303,23 +302,6 @@ struct DecodeIO {
     int32_t interleaved;        // RoPE pairs (x_2i, x_2i+1)
 };
 bool decode_supported(int dtype, int head_dim, int group);
-// A decode step over few blocks as a persistent grid of n_cta CTAs, each
-// taking an equal contiguous share of the step's `total` 128-key tiles (the
-// tiles of request table entry b start at DevReq::tile0; its L * H_kv blocks
-// of ceil((P_b + 1) / 128) tiles each follow one another).  A block split
-// between CTAs leaves each part in `ws` (2 slots of decode_stream_part_floats()
-// floats per CTA); `cnt` holds one zero-initialised arrival count per block
-// (request-major, L * H_kv per request), reset by the CTA that merges.
-struct DecodeStream {
-    float *ws;
-    int *cnt;
-    int64_t total;
-    int32_t n_cta;
-    int32_t LH;
-};
-cudaError_t launch_decode_stream(const AttnArgs &a, const ReqTable &rt, const void *tmap_k, const void *tmap_v,
-                                 const DecodeIO &io, const DecodeStream &ds, cudaStream_t s);
-int decode_stream_part_floats();
 // One CTA whose only wait (bounded by limit_ns) is on a barrier nothing
 // completes: records kDevTimeout in *err when the limit runs out.
 cudaError_t launch_wait_selftest(int *err, unsigned long long limit_ns, cudaStream_t s);
