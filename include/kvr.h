@@ -366,8 +366,8 @@ KVR_API kvr_status kvr_selftest_wait(kvr_pool_t pool, uint64_t limit_ns, void *s
  * Limits: at most 4096 non-empty spans and 256 local sources per call, and
  * head_dim <= 128; beyond them the call returns KVR_ERR_INVALID_ARG before
  * any GPU work, with the reason in kvr_last_error().  The first call on a
- * device looks up the scratch address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  A call with at
+ * device looks up the scratch address (cudaGetSymbolAddress, a synchronous
+ * runtime call) with that device current.  A call with at
  * most 64 spans and 64 local sources passes its tables inside the kernel's
  * parameters; a larger one copies them from the library's fixed host tables
  * into the scratch on the caller's stream.  All calls share the scratch and
