@@ -691,8 +691,8 @@ kvr_status encode_out_map(const kvr_pool &p, void *base, int64_t tokens, CUtenso
 }
 
 // The pool as a 2-D [entries * L * H_kv * entry_len, D] tensor with a box of
-// one row (64 columns): the attention kernel's gather4 source.
-kvr_status encode_gather_map(const kvr_pool &p, const void *base, CUtensorMap *m, uint32_t box_rows = 1)
+// `box_rows` rows (64 columns): the values-gathering attention's TMA source.
+kvr_status encode_gather_map(const kvr_pool &p, const void *base, CUtensorMap *m, uint32_t box_rows)
 {
     if (!p.encode)
         return fail(KVR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled not available");
@@ -705,15 +705,15 @@ kvr_status encode_gather_map(const kvr_pool &p, const void *base, CUtensorMap *m
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
-        return fail(KVR_ERR_CUDA, "cuTensorMapEncodeTiled (pool gather) failed (%d)", (int)r);
+        return fail(KVR_ERR_CUDA, "cuTensorMapEncodeTiled (pool values) failed (%d)", (int)r);
     return KVR_OK;
 }
 
 // What the values-gathering attention needs beyond a query-attention launch:
-// the pool's values as gather4 (one-row box) and 32-, 16- and 8-row box
-// sources, and the span table.
+// the pool's values (as a pointer, and as gather4 / 32-row box TMA sources)
+// and the span table.
 struct GatherLaunch {
-    CUtensorMap mpv, mbv, mbv16, mbv8;
+    CUtensorMap mpv, mbv;
     GatherArgs g{};
     SpanTable st;
     bool inl = false;
@@ -1002,8 +1002,6 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
                     ta.gather_v = true;
                     ta.tmap_pv = &gl->mpv;
                     ta.tmap_bv = &gl->mbv;
-                    ta.tmap_bv16 = &gl->mbv16;
-                    ta.tmap_bv8 = &gl->mbv8;
                     ta.g = gl->g;
                     ta.st = gl->inl ? &gl->st : nullptr;
                 }
@@ -1125,14 +1123,19 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
         if (qp.T == 0)
             return KVR_OK;
         GatherLaunch gl;
-        if ((st = encode_gather_map(*p, p->d.v, &gl.mpv)) != KVR_OK ||
-            (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK ||
-            (st = encode_gather_map(*p, p->d.v, &gl.mbv16, 16)) != KVR_OK ||
-            (st = encode_gather_map(*p, p->d.v, &gl.mbv8, 8)) != KVR_OK)
+        gl.g.pool_v = p->d.v;
+        if ((st = encode_gather_map(*p, p->d.v, &gl.mpv, 1)) != KVR_OK ||
+            (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK)
             return st;
         for (int b = 0; b < batch; ++b) {
-            qp.rq[b].span0 = ap.span0[b];
-            qp.rq[b].span_end = b + 1 < batch ? ap.span0[b + 1] : (int32_t)ap.ds.size();
+            DevReq &r = qp.rq[b];
+            r.span0 = ap.span0[b];
+            r.span_end = b + 1 < batch ? ap.span0[b + 1] : (int32_t)ap.ds.size();
+            // spans of 96 rows or more on average: the prefix value tiles go
+            // through TMA box loads (runs of 32 pool rows), else through the
+            // attention's gather warps
+            const int64_t n_sp = r.span_end - r.span0;
+            r.flags = n_sp > 0 && (int64_t)ap.plen[b] >= 96 * n_sp ? kReqValuesTma : 0;
         }
         if ((stitch && (st = asm_stage(p, ap, s)) != KVR_OK) || (st = qa_stage(p, qp, s)) != KVR_OK)
             return st;

@@ -117,15 +117,14 @@ constexpr int kBarPeerFree = kBarPeerData + 1;
 // slots): full (1 arrival), read by every consumer warp (one arrival each)
 constexpr int kBarGeoFull = kBarPeerFree + 1;     // [2]
 constexpr int kBarGeoEmpty = kBarGeoFull + 2;     // [2]
-// values-gathering variant: a V tile patched on chip is complete (1 arrival);
-// one per V ring slot (odd slots), so that none runs more than a phase ahead
-// of its waiter (a slot is refilled only after the MMAs consumed it)
-constexpr int kBarPatched = kBarGeoEmpty + 2;     // [2]
-// ... and the producer has issued that tile's copies (1 arrival): the patch
-// warp waits for this before it waits for the copies, so that its parity
-// wait on the slot's full barrier never runs ahead of the slot's previous load
-constexpr int kBarPatchJob = kBarPatched + 2;     // [2]
-constexpr int kNumBars = kBarPatchJob + 2;
+// values-gathering variant, one of each per V ring slot (odd slots), so that
+// none runs more than a phase ahead of its waiters (a slot is refilled only
+// after the MMAs consumed it): the slot is free for the gather warps' next
+// tile (1 arrival, the producer); the gather warps' tile has landed (2
+// arrivals, one a gather warp)
+constexpr int kBarGatherJob = kBarGeoEmpty + 2;   // [2]
+constexpr int kBarGathered = kBarGatherJob + 2;   // [2]
+constexpr int kNumBars = kBarGathered + 2;
 constexpr int kOffTmemAddr = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemAddr + 4;
 constexpr int kOffGeo = (kOffAbort + 4 + 15) & ~15;   // [2] Item
@@ -206,19 +205,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Four rows (given by row coordinate) x 64 columns of a 2-D tensor whose box
-// is one row high, into four consecutive 128-byte rows of shared memory.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, const int *rows,
-                                            uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-        "%4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(rows[0]), "r"(rows[1]), "r"(rows[2]), "r"(rows[3]),
-        "r"(bar)
-        : "memory");
-}
-
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (the tensor core reads its operands through it).
 // Fetch a tensor map (a kernel parameter) ahead of its first copy.
@@ -264,13 +250,23 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t sr
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // 16 bytes global -> shared, asynchronous (this thread's copies complete at
 // cp_async_wait_all); no register holds the data
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+// Four rows (given by row coordinate) x 64 columns of a 2-D tensor whose box
+// is one row high, into four consecutive 128-byte rows of shared memory.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, const int *rows,
+                                            uint32_t bar)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(rows[0]), "r"(rows[1]), "r"(rows[2]), "r"(rows[3]),
+        "r"(bar)
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all()
+
+// (src_bytes 0: the 16 bytes are zero-filled and nothing is read)
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, int src_bytes)
 {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -648,7 +644,8 @@ __device__ __forceinline__ Unit unit_at_warp(const AttnArgs &a, const ReqRegs &r
     rq.unit0 = __shfl_sync(0xffffffffu, k ? rr.r[1].unit0 : rr.r[0].unit0, src);
     rq.span0 = __shfl_sync(0xffffffffu, k ? rr.r[1].span0 : rr.r[0].span0, src);
     rq.span_end = __shfl_sync(0xffffffffu, k ? rr.r[1].span_end : rr.r[0].span_end, src);
-    rq.pad_[0] = rq.pad_[1] = rq.pad_[2] = 0;
+    rq.flags = __shfl_sync(0xffffffffu, k ? rr.r[1].flags : rr.r[0].flags, src);
+    rq.pad_[0] = rq.pad_[1] = 0;
     return unit_geometry(a, rq, b, u);
 }
 
@@ -671,10 +668,15 @@ struct Geo {
     int n_t[2], row0[2];
     int m_rows, q_len, prefix, q_off;
     int l, h, n_valid, cap;
+    int span0, span_end;   // the request's spans (values-gathering variant)
+    int tma_v, pad2_;      // prefix value tiles through TMA (values-gathering variant)
     int64_t kv_row0;
 };
 static_assert(sizeof(Geo) <= kGeoBytes, "geometry slot");
 
+// (the span range and value mode only for the values-gathering variant: in
+// the stitched one those request fields stay dead and cost no registers)
+template <bool kV>
 __device__ __forceinline__ void geo_of(const Item &t, Geo &o)
 {
     o.jb = t.jb;
@@ -693,21 +695,31 @@ __device__ __forceinline__ void geo_of(const Item &t, Geo &o)
     o.h = t.w.h;
     o.n_valid = t.w.n_valid;
     o.cap = t.w.rq.cap;
+    if constexpr (kV) {
+        o.span0 = t.w.rq.span0;
+        o.span_end = t.w.rq.span_end;
+        o.tma_v = (t.w.rq.flags & kReqValuesTma) != 0;
+    }
     o.kv_row0 = t.w.kv_row0;
 }
 // the kernel's variants: K and V from the stitched cache; or K from the cache
 // and the prefix values gathered from the pool
 constexpr int kModeStitched = 0, kModeGatherV = 1;
-// softmax 8, MMA 1, and the patch warp (values-gathering variant)
+// softmax 8, MMA 1, and the two gather warps (values-gathering variant)
 template <int kM>
-constexpr uint32_t geo_consumer_warps() { return kM == kModeGatherV ? 10u : 9u; }
+constexpr uint32_t geo_consumer_warps() { return kM == kModeGatherV ? 11u : 9u; }
 
-// The value tile j of a values-gathering item that is patched on chip: it
-// holds the first query rows after prefix rows from the pool, or it reaches
-// past the cache block (into rows this variant does not write).
-__device__ __forceinline__ bool v_patched(int j, int prefix, int cap)
+// The value tile j of a values-gathering item that the gather warps fill: a
+// tile that reaches past the cache block (into rows this variant does not
+// write); and a tile with prefix rows -- every one for a request of short
+// spans, only the one that also holds the first query rows for a request of
+// long spans (`tma_v`: its other prefix tiles come from the pool through TMA
+// box loads, whose runs of 32 consecutive pool rows move a tile in a few
+// instructions).
+__device__ __forceinline__ bool v_gathered(int j, int prefix, int cap, bool tma_v)
 {
-    return (j * kTileN < prefix && prefix < (j + 1) * kTileN) || (j + 1) * kTileN > cap;
+    const bool has_prefix = j * kTileN < prefix;
+    return (j + 1) * kTileN > cap || (has_prefix && (!tma_v || prefix < (j + 1) * kTileN));
 }
 
 // `rr`: the producer warp's register copy of the request table (all 32
@@ -733,7 +745,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ AttnArgs a,
                    const __grid_constant__ ReqTable rt, const int n_blocks,
                    const __grid_constant__ CUtensorMap tmpv, const __grid_constant__ CUtensorMap tmbv,
-                   const __grid_constant__ CUtensorMap tmbv16, const __grid_constant__ CUtensorMap tmbv8,
                    const __grid_constant__ GatherArgs g, const __grid_constant__ SpanTable st,
                    const __grid_constant__ CUtensorMap tmo)
 {
@@ -770,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto geo_put = [&](int k, const Item &gm) -> bool {
         if (k >= 2 && !mbar_wait(bar(kBarGeoEmpty + (k & 1)), (uint32_t)((k >> 1) - 1) & 1u, abort_flag))
             return false;
-        geo_of(gm, *geo_slot(k));
+        geo_of<kV>(gm, *geo_slot(k));
         mbar_arrive(bar(kBarGeoFull + (k & 1)));   // release: the record is visible to the waiters
         return true;
     };
@@ -780,7 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool wg = (i >= kBarPFull && i < kBarPFull + 2) || (i >= kBarOEmpty && i < kBarOEmpty + 2) ||
                             i == kBarPeerData;
             const bool geo_empty = i >= kBarGeoEmpty && i < kBarGeoEmpty + 2;
-            mbar_init(bar(i), wg ? 128u : geo_empty ? geo_consumer_warps<kM>() : 1u);
+            const bool gathered = i >= kBarGathered && i < kBarGathered + 2;
+            mbar_init(bar(i), wg ? 128u : geo_empty ? geo_consumer_warps<kM>() : gathered ? 2u : 1u);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -791,14 +803,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmq);
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
-        if (a.out_tma)
-            prefetch_tmap(&tmo);
         if constexpr (kV) {
             prefetch_tmap(&tmpv);
             prefetch_tmap(&tmbv);
-            prefetch_tmap(&tmbv16);
-            prefetch_tmap(&tmbv8);
         }
+        if (a.out_tma)
+            prefetch_tmap(&tmo);
     }
     tc_fence_before();
     __syncthreads();
@@ -1099,11 +1109,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 8) {
         regs_other();
         if constexpr (kV) {
-            // ====== values-gathering producer: Q and the K tiles as in the
-            // stitched variant; a V tile with prefix rows comes from the pool
-            // (lane i: rows 4i..4i+3, resolved through the span table; runs of
-            // consecutive pool rows as 32-, 16- or 8-row box loads, other lanes
-            // a gather4 each), later V tiles from the cache block ======
+            // ====== values-gathering producer: Q, the K tiles and the V tiles
+            // past the prefix as in the stitched variant (lane 0); a request of
+            // long spans has its other prefix value tiles loaded from the pool
+            // here (lane i: rows 4i..4i+3, resolved through the span table; a
+            // group of 8 lanes whose 32 rows are consecutive pool rows takes one
+            // 32-row box load per panel, other lanes a gather4 each); a V tile
+            // that the gather warps fill (v_gathered) is announced to them once
+            // its ring slot is free ======
             int tt = 0, nq = 0, gk = 0;
             bool ok = true;
             const DevSpan *spans = g.spans ? g.spans : st.spans;
@@ -1123,13 +1136,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool more = it + (int)gridDim.x < n_items;
                 if (more && gk > 0)
                     nxt = item_at(a, reqs, n_blocks, it + gridDim.x, &rr, lane);
-                if (itm.je > itm.jb) {
-                    const int prefix = w.rq.prefix, s_end = w.rq.span_end;
+                const bool tma_v = (w.rq.flags & kReqValuesTma) != 0;
+                if (itm.je > itm.jb && !tma_v && lane == 0) {
+                    // a request of short spans: lane 0 alone, as in the stitched variant
+                    const int n_loads = 2 * (itm.je - itm.jb);
+                    for (int i = 0; i <= n_loads && ok; ++i) {
+                        if (i == 2) {
+                            if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            const int nqt = w.n_t[1] > 0 ? 2 : 1;
+                            mbar_expect_tx(bar(kBarQFull), nqt * kTileBytes);
+                            for (int x = 0; x < nqt; ++x) {
+                                const uint32_t dst = sbase + kOffQ + x * kTileBytes;
+                                tma_load_2d(dst, &tmq, 0, w.q_row0 + x * kTileM, bar(kBarQFull));
+                                tma_load_2d(dst + kPanelBytes, &tmq, 64, w.q_row0 + x * kTileM, bar(kBarQFull));
+                            }
+                            ++nq;
+                        }
+                        if (i == n_loads)
+                            break;
+                        const int slot = tt % kSlots;
+                        if (tt >= kSlots && !mbar_wait(bar(kBarEmpty + slot), ((tt / kSlots) - 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const int j = itm.jb + (i >> 1);
+                        if ((i & 1) == 1 && v_gathered(j, w.rq.prefix, w.rq.cap, false)) {
+                            mbar_arrive(bar(kBarFull + slot));
+                            mbar_arrive(bar(kBarGatherJob + (slot >> 1)));
+                        } else {
+                            const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
+                            const CUtensorMap *map = (i & 1) ? &tmv : &tmk;
+                            const int row = (int)(w.kv_row0 + (int64_t)j * kTileN);
+                            mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
+                            tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
+                            tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
+                        }
+                        ++tt;
+                    }
+                } else if (itm.je > itm.jb && tma_v) {
+                    const int prefix = w.rq.prefix, cap = w.rq.cap, s_end = w.rq.span_end;
                     const int64_t lh_row = (int64_t)w.lh * g.entry_len;   // (layer, kv-head) block inside an entry
-                    // the span holding the item's first row (a request's spans are in
-                    // stitched-row order); each lane's cursor then only moves forward
+                    // the span holding the item's first row; each lane's cursor
+                    // then only moves forward
                     int cur = w.rq.span0;
-                    if (itm.jb * kTileN < prefix) {
+                    if (tma_v && itm.jb * kTileN < prefix) {
                         int lo = w.rq.span0, hi = s_end - 1;
                         while (lo < hi) {
                             const int mid = (lo + hi + 1) >> 1;
@@ -1142,7 +1195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int n_loads = 2 * (itm.je - itm.jb);
                     int rows[4] = {0, 0, 0, 0};
-                    int box_lanes = 1;    // lanes of this lane's box-load group (1: a gather4 of its own)
+                    bool run32 = false;   // this lane's 32-row group is 32 consecutive pool rows
                     for (int i = 0; i <= n_loads; ++i) {
                         if (i == 2 && lane == 0) {   // Q after K_0 and V_0, as in the stitched variant
                             if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag)) {
@@ -1169,68 +1222,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         const int j = itm.jb + (i >> 1);
                         const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
-                        if ((i & 1) == 0 || j * kTileN >= prefix) {
-                            // a K tile, or a V tile past the prefix: the cache block's rows
+                        const bool v = (i & 1) == 1;
+                        if (v && v_gathered(j, prefix, cap, tma_v)) {
+                            // the slot's full barrier still completes a phase for this
+                            // load (its parity then stays the load count's), with no bytes
                             if (lane == 0) {
-                                const CUtensorMap *map = (i & 1) ? &tmv : &tmk;
-                                const int row = (int)(w.kv_row0 + (int64_t)j * kTileN);
-                                mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
-                                tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
-                                tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
+                                mbar_arrive(bar(kBarFull + slot));
+                                mbar_arrive(bar(kBarGatherJob + (slot >> 1)));
                             }
-                            // V tile j's pool rows, resolved while its slot drains (rows
-                            // past the prefix: any pool row, which the patch warp replaces)
-                            if ((i & 1) == 0 && j * kTileN < prefix) {
-#pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    const int r = j * kTileN + 4 * lane + k;
-                                    rows[k] = 0;
-                                    if (r < prefix) {
-                                        while (cur + 1 < s_end && spans[cur].row + spans[cur].len <= r)
-                                            ++cur;
-                                        const DevSpan &sp = spans[cur];
-                                        rows[k] = (int)((int64_t)sp.src * e_rows + lh_row + sp.start + (r - sp.row));
-                                    }
-                                }
-                                // aligned groups of 8, 4 or 2 lanes whose rows are consecutive
-                                // pool rows take one 32-, 16- or 8-row box load per panel,
-                                // issued by the group's first lane; other lanes a gather4
-                                const int last = __shfl_up_sync(0xffffffffu, rows[3], 1);
-                                const unsigned b4 = __ballot_sync(
-                                    0xffffffffu, (j * kTileN + 4 * lane + 3 < prefix) && rows[1] == rows[0] + 1 &&
-                                                     rows[2] == rows[0] + 2 && rows[3] == rows[0] + 3);
-                                const unsigned bc = __ballot_sync(0xffffffffu, rows[0] == last + 1);
-                                box_lanes = 1;
-#pragma unroll
-                                for (int sz = 8; sz >= 2; sz >>= 1) {
-                                    const int g0 = lane & ~(sz - 1);
-                                    const unsigned m = ((1u << sz) - 1u) << g0, inner = m & ~(1u << g0);
-                                    if (box_lanes == 1 && (b4 & m) == m && (bc & inner) == inner)
-                                        box_lanes = sz;
-                                }
-                            }
-                        } else {
+                        } else if (v && j * kTileN < prefix) {
+                            // a long-span request's prefix value tile, from the pool
                             if (lane == 0)
                                 mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
                             __syncwarp();
                             const uint32_t d4 = dst + (uint32_t)(4 * lane) * 128u;
-                            if (box_lanes > 1) {
-                                if ((lane & (box_lanes - 1)) == 0) {
-                                    const CUtensorMap *map = box_lanes == 8 ? &tmbv : box_lanes == 4 ? &tmbv16 : &tmbv8;
-                                    tma_load_2d(d4, map, 0, rows[0], bar(kBarFull + slot));
-                                    tma_load_2d(d4 + kPanelBytes, map, 64, rows[0], bar(kBarFull + slot));
+                            if (run32) {
+                                if ((lane & 7) == 0) {
+                                    tma_load_2d(d4, &tmbv, 0, rows[0], bar(kBarFull + slot));
+                                    tma_load_2d(d4 + kPanelBytes, &tmbv, 64, rows[0], bar(kBarFull + slot));
                                 }
                             } else {
                                 tma_gather4(d4, &tmpv, 0, rows, bar(kBarFull + slot));
                                 tma_gather4(d4 + kPanelBytes, &tmpv, 64, rows, bar(kBarFull + slot));
                             }
+                        } else if (lane == 0) {
+                            // a K tile, or a V tile past the prefix: the cache block's rows
+                            const CUtensorMap *map = v ? &tmv : &tmk;
+                            const int row = (int)(w.kv_row0 + (int64_t)j * kTileN);
+                            mbar_expect_tx(bar(kBarFull + slot), kTileBytes);
+                            tma_load_2d(dst, map, 0, row, bar(kBarFull + slot));
+                            tma_load_2d(dst + kPanelBytes, map, 64, row, bar(kBarFull + slot));
                         }
-                        if ((i & 1) == 1 && lane == 0 && v_patched(j, prefix, w.rq.cap))
-                            mbar_arrive(bar(kBarPatchJob + (slot >> 1)));
+                        // after K tile j: the pool rows of V tile j, if the producer loads it
+                        if (!v && tma_v && j * kTileN < prefix && !v_gathered(j, prefix, cap, tma_v)) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int r = j * kTileN + 4 * lane + k;
+                                while (cur + 1 < s_end && spans[cur].row + spans[cur].len <= r)
+                                    ++cur;
+                                const DevSpan &sp = spans[cur];
+                                rows[k] = (int)((int64_t)sp.src * e_rows + lh_row + sp.start + (r - sp.row));
+                            }
+                            const int last = __shfl_up_sync(0xffffffffu, rows[3], 1);
+                            const bool mine = rows[1] == rows[0] + 1 && rows[2] == rows[0] + 2 &&
+                                              rows[3] == rows[0] + 3 && ((lane & 7) == 0 || rows[0] == last + 1);
+                            const unsigned ball = __ballot_sync(0xffffffffu, mine);
+                            run32 = ((ball >> (lane & ~7)) & 0xffu) == 0xffu;
+                        }
                         ++tt;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
+                tt = __shfl_sync(0xffffffffu, tt, 0);
+                nq = __shfl_sync(0xffffffffu, nq, 0);
                 // the next item's geometry, published for the other roles; its Q
                 // brought into L2 ahead of its load
                 if (ok && more) {
@@ -1390,14 +1434,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 return true;
             };
-            // values-gathering variant: a patched V tile is complete once the
-            // patch warp has written it (it waited for the tile's copies)
+            // values-gathering variant: a gathered V tile is complete once both
+            // gather warps have released it
             int np[2] = {0, 0}, prefix_v = 0, cap_v = 0;
+            bool tma_v = false;
             auto wait_v = [&](int k, int j) -> bool {
                 if constexpr (kV) {
-                    if (v_patched(j, prefix_v, cap_v)) {
+                    if (v_gathered(j, prefix_v, cap_v, tma_v)) {
                         const int b = (k % kSlots) >> 1;   // V tiles sit in slots 1 and 3
-                        if (!mbar_wait(bar(kBarPatched + b), np[b] & 1, abort_flag))
+                        if (!mbar_wait(bar(kBarGathered + b), np[b] & 1, abort_flag))
                             return false;
                         ++np[b];
                         tc_fence_after();
@@ -1418,6 +1463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (kV) {
                     prefix_v = gp->prefix;
                     cap_v = gp->cap;
+                    tma_v = gp->tma_v != 0;
                 }
                 geo_done(gk);
                 if (je <= jb)
@@ -1500,21 +1546,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && drained && peer_wait >= 0 && lane == 0)
                 mbar_arrive_remote(mapa_rank(bar(kBarPeerFree), (uint32_t)(1 - peer_wait)));
         }
-    } else if (kV && warp == 10) {
+    } else if (kV && warp >= 10) {
         regs_other();
-        // ========== patch (values-gathering variant, warp 10) ==========
-        // A V tile that holds prefix rows came from the pool, with pool row 0
-        // in place of its query rows: copy those from the cache block (the
-        // query prologue appended them there).  Rows past the request's keys
-        // are zeroed (a masked key has weight 0, but 0 x NaN is NaN, and a
-        // tile that reaches past the cache block reads rows this variant does
-        // not write).  Lane l owns 16-byte chunk l % 8 of rows l / 8 + 4k.
-        const int c8 = lane & 7;
+        // ========== gather (values-gathering variant, warps 10-11) ==========
+        // Each V tile that v_gathered names (for a request of short spans every
+        // tile with prefix rows; for one of long spans the tile that also holds
+        // the first query rows; and any tile that reaches past its cache block,
+        // whose value rows this variant does not write) is filled here with
+        // 16-byte asynchronous copies: prefix rows from the pool
+        // (resolved through the span table), query rows from the cache block
+        // (the query prologue appended them there), zeros past the request's
+        // keys (a masked key has weight 0, but 0 x NaN is NaN).  Warp 10 takes
+        // rows 0-63 of the tile, warp 11 rows 64-127; lane l resolves rows
+        // 2l and 2l + 1 of its warp's half, and in copy i the warp moves rows
+        // 2i and 2i + 1 (lanes 0-15 and 16-31, one 16-byte chunk each of the
+        // two 64-column panels' 8).  A tile's copies are one group; the tile
+        // is released to the MMA warp once the next tile's copies are issued
+        // and its own have landed.
+        const int rb = 64 * (warp - 10);
+        const int q16 = lane & 15, half_sel = lane >> 4;
+        const uint32_t chunk_off = (uint32_t)((q16 >> 3) * kPanelBytes);
+        const int c8 = q16 & 7;
+        const DevSpan *spans = g.spans ? g.spans : st.spans;
+        const int64_t e_rows = (int64_t)a.n_layers * a.n_kv_heads * g.entry_len;   // pool rows per entry
+        const __nv_bfloat16 *pv = static_cast<const __nv_bfloat16 *>(g.pool_v);
         const __nv_bfloat16 *cv = static_cast<const __nv_bfloat16 *>(a.cache_v);
-        int tt = 0, gk = 0, nj[2] = {0, 0};
+        int tt = 0, gk = 0, nj[2] = {0, 0}, prev_b = -1;
         bool ok = true;
+        // release the tile whose copies were issued last (all of this thread's
+        // copies land first, then the async proxy sees them)
+        auto release = [&](int wait_all) {
+            if (prev_b < 0)
+                return;
+            if (wait_all)
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            else
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(kBarGathered + prev_b));
+            prev_b = -1;
+        };
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
-            int jb, je, prefix, n_valid, cap;
+            int jb, je, prefix, n_valid, cap, lh, s0, s_end;
+            bool tma_v;
             int64_t kv_row0;
             {
                 const Geo *gp = geo_wait(gk);
@@ -1528,41 +1604,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 n_valid = gp->n_valid;
                 cap = gp->cap;
                 kv_row0 = gp->kv_row0;
+                lh = gp->l * a.n_kv_heads + gp->h;
+                s0 = gp->span0;
+                s_end = gp->span_end;
+                tma_v = gp->tma_v != 0;
                 geo_done(gk);
             }
-            for (int j = jb; j < je; ++j, tt += 2) {
-                if (!v_patched(j, prefix, cap))
+            const int64_t lh_row = (int64_t)lh * g.entry_len;   // (layer, kv-head) block inside an entry
+            // this lane's span cursor: the span holding its first prefix row of
+            // the item (a request's spans are in stitched-row order)
+            int cur = s0;
+            {
+                const int r0 = jb * kTileN + rb + 2 * lane;
+                if (r0 < prefix) {
+                    int lo = s0, hi = s_end - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (spans[mid].row <= r0)
+                            lo = mid;
+                        else
+                            hi = mid - 1;
+                    }
+                    cur = lo;
+                }
+            }
+            for (int j = jb; j < je && ok; ++j, tt += 2) {
+                if (!v_gathered(j, prefix, cap, tma_v))
                     continue;
+                // the source of this lane's two rows (0: zeros)
+                const __nv_bfloat16 *src[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int r = j * kTileN + rb + 2 * lane + k;
+                    src[k] = nullptr;
+                    if (r < prefix) {
+                        while (cur + 1 < s_end && spans[cur].row + spans[cur].len <= r)
+                            ++cur;
+                        const DevSpan &sp = spans[cur];
+                        src[k] = pv + ((int64_t)sp.src * e_rows + lh_row + sp.start + (r - sp.row)) * kD;
+                    } else if (r < n_valid) {
+                        src[k] = cv + (kv_row0 + r) * kD;
+                    }
+                }
                 const int sv = (tt + 1) % kSlots, b = sv >> 1;
-                if (!mbar_wait(bar(kBarPatchJob + b), nj[b] & 1, abort_flag) ||
-                    !mbar_wait(bar(kBarFull + sv), ((tt + 1) / kSlots) & 1, abort_flag)) {
+                if (!mbar_wait(bar(kBarGatherJob + b), nj[b] & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 ++nj[b];
-                const uint32_t vb = sbase + kOffKV + sv * kTileBytes;
-                // from the pool: rows from the prefix on; from the cache: rows past the keys
-                const int first = max(j * kTileN < prefix ? prefix : n_valid, j * kTileN) - j * kTileN;
-                // every copy of the warp in flight at once, then one wait
-                for (int r = first + (lane >> 3); r < kTileN; r += 4) {
-                    const int rr = j * kTileN + r;
-                    const uint32_t lo_a = vb + r * 128 + ((c8 ^ (r & 7)) << 4);
-                    if (rr < n_valid) {
-                        const __nv_bfloat16 *src = cv + (kv_row0 + rr) * kD + 8 * c8;
-                        cp_async16(lo_a, src);
-                        cp_async16(lo_a + kPanelBytes, src + kD / 2);
-                    } else {
-                        st_shared_v4(lo_a, 0u, 0u, 0u, 0u);
-                        st_shared_v4(lo_a + kPanelBytes, 0u, 0u, 0u, 0u);
-                    }
+                const uint32_t vb = sbase + kOffKV + sv * kTileBytes + chunk_off;
+#pragma unroll 4
+                for (int i = 0; i < 32; ++i) {
+                    const __nv_bfloat16 *s_lo = (const __nv_bfloat16 *)__shfl_sync(0xffffffffu, (uintptr_t)src[0], i);
+                    const __nv_bfloat16 *s_hi = (const __nv_bfloat16 *)__shfl_sync(0xffffffffu, (uintptr_t)src[1], i);
+                    const __nv_bfloat16 *sp = half_sel ? s_hi : s_lo;
+                    const int r = rb + 2 * i + half_sel;   // row of the tile
+                    cp_async16_zfill(vb + r * 128 + ((c8 ^ (r & 7)) << 4),
+                                     sp ? sp + (q16 >> 3) * 64 + 8 * c8 : cv, sp ? 16 : 0);
                 }
-                cp_async_wait_all();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(kBarPatched + b));
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                release(0);
+                prev_b = b;
             }
+            release(1);
         }
+        release(1);
         if (!ok)
             flag_timeout(a.err, abort_flag);
     } else {
@@ -1680,8 +1786,6 @@ static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool
                               *static_cast<const CUtensorMap *>(ta.tmap_v), ta.base, *ta.rt, ta.n_m_blocks,
                               kV ? *static_cast<const CUtensorMap *>(ta.tmap_pv) : no_map,
                               kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv) : no_map,
-                              kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv16) : no_map,
-                              kV ? *static_cast<const CUtensorMap *>(ta.tmap_bv8) : no_map,
                               kV ? ta.g : no_gather, kV && ta.st ? *ta.st : no_spans,
                               ta.base.out_tma ? *static_cast<const CUtensorMap *>(ta.tmap_out) : no_map);
 }

@@ -142,9 +142,14 @@ struct alignas(16) DevReq {
     int32_t unit0;       // first (layer, kv-head, 256-row block) unit (tensor-core path)
     int32_t span0;       // first non-empty span of this request (values-gathering attention)
     int32_t span_end;    // one past its last
-    int32_t pad_[3];
+    int32_t flags;       // kReqValuesTma (values-gathering attention)
+    int32_t pad_[2];
 };
 static_assert(sizeof(DevReq) == 48, "request table layout");
+// DevReq::flags: the values-gathering attention loads this request's prefix
+// value tiles through TMA box loads (its spans are long) rather than with the
+// gather warps' copies
+constexpr int32_t kReqValuesTma = 1;
 
 // Device error word codes (first error wins).  kDevBadInput: an attention
 // row's softmax denominator came out non-finite or zero (a NaN or infinity in
@@ -261,6 +266,7 @@ struct GatherArgs {
     const DevSpan *spans;       // the batch's spans in global memory, or NULL: the SpanTable parameter
     int32_t n_spans;            // non-empty spans of the batch (request b's start at DevReq::span0)
     int32_t entry_len;          // pool tokens per entry
+    const void *pool_v;         // the pool's values: [entries * L * H_kv * entry_len, D] bf16
 };
 
 struct TcAttnArgs {
@@ -271,11 +277,9 @@ struct TcAttnArgs {
     const void *tmap_v;
     int32_t n_m_blocks;         // total 256-row query blocks over all requests
     int32_t n_sms;              // persistent grid size bound
-    bool gather_v;              // V tiles of prefix rows from the pool (tmap_pv, tmap_bv, g, st), K from the cache
-    const void *tmap_pv;        // pool V as [rows, D] with a one-row box (gather4)
-    const void *tmap_bv;        // the same with a 32-, 16- and 8-row box (runs of consecutive pool rows)
-    const void *tmap_bv16;
-    const void *tmap_bv8;
+    bool gather_v;              // V tiles of prefix rows from the pool (g, st), K from the cache
+    const void *tmap_pv;        // the pool's values as [rows, D] with a one-row box (gather4)
+    const void *tmap_bv;        // the same with a 32-row box (runs of consecutive pool rows)
     GatherArgs g;
     const SpanTable *st;
     const void *tmap_out;       // out as [L*T][H_q][D] with a (64, G, 32 / G) box (base.out_tma)
