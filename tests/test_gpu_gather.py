@@ -48,6 +48,16 @@ def _case(name):
                             [[], [[pid, 0, 5]], [[0, 95, 96], [1, 0, 1], [2, 10, 96]],
                              [[3, 3, 50], [3, 20, 60], [pid, 0, 5]]])
         return cfg, reqs, {}
+    if name == "mixed_long_short":
+        # requests whose spans average 96 rows or more (value tiles through TMA
+        # box loads) beside requests of short spans (through the gather warps),
+        # in one batch; cache blocks with spare rows
+        pid = EDGE.n_chunks
+        cfg, reqs = _custom(dataclasses.replace(EDGE, query_len=21),
+                            [[[0, 0, 96], [1, 0, 96], [2, 0, 96]], [[3, 5, 20], [0, 1, 9]],
+                             [[pid, 0, 5], [1, 0, 96], [2, 0, 96], [3, 0, 96]], [[2, 0, 96], [3, 0, 96]],
+                             [[1, 50, 96], [0, 0, 96]]])
+        return cfg, reqs, {"spare_rows": 3}
     if name == "many_requests":
         base = dataclasses.replace(EDGE, prompt_len=0, query_len=3)
         rng = np.random.default_rng(3)
@@ -58,12 +68,13 @@ def _case(name):
     raise ValueError(name)
 
 
-@pytest.mark.parametrize("name", ["cfg2", "cfg2_composite", "cfg3", "cfg5", "edges", "many_requests"])
+@pytest.mark.parametrize("name", ["cfg2", "cfg2_composite", "cfg3", "cfg5", "edges", "mixed_long_short",
+                                  "many_requests"])
 def test_gathering_prefill_matches_oracle_and_stitched_path(name):
     import torch
     cfg, reqs, kw = _case(name)
     composite = kw.pop("composite", False)
-    case = Case(cfg, reqs=reqs, composite=composite)
+    case = Case(cfg, reqs=reqs, composite=composite, spare_rows=kw.pop("spare_rows", 0))
     res = run_parity_case(cfg=cfg, case=case, prefill=True, skip_prefix=True, composite=composite, **kw)
     assert res["ok"], res
     got = [case.out.clone(), case.pos_ids.clone(), case.src_map.clone()]
