@@ -983,7 +983,7 @@ static kvr_status qa_launch(kvr_pool *p, QaPlan &pl, cudaStream_t s, bool after_
             p->mark(4, s);
             {
                 NvtxRange r("kvr.k_decode_attention");
-                e = launch_decode_attention(pl.at, rt, &pl.mk, &pl.mv, io, s);
+                e = launch_decode_attention(pl.at, rt, &pl.mk, &pl.mv, io, !p->timed, s);
             }
             p->mark(5, s);
         } else if (e == cudaSuccess) {

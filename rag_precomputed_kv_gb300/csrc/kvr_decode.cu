@@ -80,7 +80,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
     __syncthreads();
-    // the query prologue's rotated heads and appended rows are read from here on
+    // a decode step launched after this one (programmatic launch) may now take
+    // the SMs this grid leaves free and set up there: it reads and writes
+    // nothing before its own wait below, which returns once this grid is done
+    pdl_launch_dependents();
+    // nothing the kernel before it on the stream writes (the step's query,
+    // key and value, the cache rows, the request table) is read before this
     pdl_wait_prerequisites();
 
     const DevReq rq = reqs[b];
@@ -402,7 +407,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 bool decode_supported(int dtype, int head_dim, int group) { return dtype == KVR_DTYPE_BF16 && head_dim == kDecD && group <= 16; }
 
 cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const void *tmap_k, const void *tmap_v,
-                                    const DecodeIO &io, cudaStream_t s)
+                                    const DecodeIO &io, bool pdl, cudaStream_t s)
 {
     const int64_t ctas = (int64_t)a.n_reqs * a.n_layers * a.n_kv_heads;
     if (ctas == 0)
@@ -421,9 +426,18 @@ cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const
         if (dev < 64)
             attr_set[dev].store(true, std::memory_order_release);
     }
-    k_decode_attention<<<(unsigned)ctas, kDecThreads, kDecSmem, s>>>(*static_cast<const CUtensorMap *>(tmap_k),
-                                                                     *static_cast<const CUtensorMap *>(tmap_v), a, rt, io);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = kDecSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_decode_attention, *static_cast<const CUtensorMap *>(tmap_k),
+                              *static_cast<const CUtensorMap *>(tmap_v), a, rt, io);
 }
 
 }  // namespace kvr

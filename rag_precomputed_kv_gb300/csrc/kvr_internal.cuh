@@ -309,8 +309,11 @@ bool decode_supported(int dtype, int head_dim, int group);
 // One CTA whose only wait (bounded by limit_ns) is on a barrier nothing
 // completes: records kDevTimeout in *err when the limit runs out.
 cudaError_t launch_wait_selftest(int *err, unsigned long long limit_ns, cudaStream_t s);
+// `pdl`: programmatic launch (the kernel sets up while the kernel before it
+// finishes, and reads nothing before that kernel is done); a decode step lets
+// the next one launch that way
 cudaError_t launch_decode_attention(const AttnArgs &a, const ReqTable &rt, const void *tmap_k, const void *tmap_v,
-                                    const DecodeIO &io, cudaStream_t s);
+                                    const DecodeIO &io, bool pdl, cudaStream_t s);
 // Whether `n_sms` CTAs of the attention kernel (either variant) can be
 // resident at once as two-CTA clusters.
 bool attention_tc_pairs_fit(int n_sms);
