@@ -503,11 +503,11 @@ def run_kvr(args):
     att_ms = [e[4].elapsed_time(e[5]) for e in ev]
     ser_ms = [e[0].elapsed_time(e[5]) for e in ev]
 
-    # ---- the same prefill with KVR_PREFILL_SKIP_PREFIX_CACHE (the attention
-    # gathers the prefix from the pool; no stitched cache is written), when the
-    # pool and spans allow it ----
+    # ---- the same prefill with KVR_PREFILL_SKIP_PREFIX_CACHE (a keys-only
+    # stitch; the attention gathers the prefix values from the pool), on the
+    # tensor-core path ----
     gather = None
-    if wl.pool.attention_path == K.PATH_TCGEN05 and not wl.locals:
+    if wl.pool.attention_path == K.PATH_TCGEN05:
         n_g = min(args.steps, 500)
         g0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_g)]
         g1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_g)]

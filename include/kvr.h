@@ -302,10 +302,9 @@ KVR_API kvr_status kvr_query_attention(kvr_pool_t pool, int32_t batch, const int
  * order (the attention's last round of units splits differently on fewer SMs).
  *
  * flags: KVR_POSITIONS_COMPOSITE as in kvr_assemble; KVR_PREFILL_SKIP_PREFIX_CACHE
- * (above) needs a bf16 pool in device memory with head_dim 128, laid out contiguously
- * ([entries][L][H_kv][entry_len][D], fewer than 2^31 rows), spans from the
- * pool only (n_locals = 0) and the tensor-core attention; otherwise the call
- * returns KVR_ERR_UNSUPPORTED before any work.
+ * (above) needs a bf16 pool in device memory with head_dim 128 and the
+ * tensor-core attention (any strides, request-local sources allowed);
+ * otherwise the call returns KVR_ERR_UNSUPPORTED before any work.
  * Errors: those of the two calls; nothing is enqueued when a check fails.
  */
 KVR_API kvr_status kvr_prefill(kvr_pool_t pool, int32_t batch, const int32_t *span_offsets,

@@ -446,6 +446,7 @@ struct AsmPlan {
     int32_t *pos_ids = nullptr, *src_map = nullptr;
     AssembleArgs a{};
     bool inl = false;
+    bool upload = false;   // upload the tables even for a small call (a later kernel reads them)
     AssembleTables tab;
     Slot *slot = nullptr;
 };
@@ -570,7 +571,7 @@ static kvr_status asm_stage(kvr_pool *p, AsmPlan &pl, cudaStream_t s)
     a.interleaved = (p->d.flags & KVR_POOL_ROPE_INTERLEAVED) ? 1 : 0;
     const int n_locals = pl.n_locals;
     const kvr_local_src *locals = pl.locals;
-    pl.inl = (int)pl.ds.size() <= kInlineEntries && n_locals <= kInlineEntries;
+    pl.inl = !pl.upload && (int)pl.ds.size() <= kInlineEntries && n_locals <= kInlineEntries;
     if (pl.inl) {
         // small call: the tables travel inside the kernel parameters
         std::memcpy(pl.tab.spans, pl.ds.data(), pl.ds.size() * sizeof(DevSpan));
@@ -713,7 +714,7 @@ kvr_status encode_gather_map(const kvr_pool &p, const void *base, CUtensorMap *m
 // the pool's values (as a pointer, and as gather4 / 32-row box TMA sources)
 // and the span table.
 struct GatherLaunch {
-    CUtensorMap mpv, mbv;
+    CUtensorMap mpv{}, mbv{};
     GatherArgs g{};
     SpanTable st;
     bool inl = false;
@@ -1079,16 +1080,16 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
     NvtxRange call("kvr_prefill");
     // every check of both halves before anything is enqueued
     const bool gather = flags & KVR_PREFILL_SKIP_PREFIX_CACHE;
+    // the pool seen as one 2-D [rows, D] tensor for TMA box loads of value tiles
+    bool tma_pool = false;
     if (gather) {
         const kvr_pool_desc &d = p->d;
         const int64_t E = d.entry_len, D = d.head_dim;
-        const bool contiguous = d.stride[3] == D && d.stride[2] == E * D && d.stride[1] == d.n_kv_heads * E * D &&
-                                d.stride[0] == (int64_t)d.n_layers * d.n_kv_heads * E * D;
-        if (d.dtype != KVR_DTYPE_BF16 || D != 128 || n_locals != 0 || !contiguous ||
-            d.n_entries * d.n_layers * d.n_kv_heads * E > INT32_MAX)
-            return fail(KVR_ERR_UNSUPPORTED,
-                        "KVR_PREFILL_SKIP_PREFIX_CACHE needs a contiguous bf16 pool with head_dim 128 "
-                        "(< 2^31 rows) and pool spans only");
+        tma_pool = d.stride[3] == D && d.stride[2] == E * D && d.stride[1] == d.n_kv_heads * E * D &&
+                   d.stride[0] == (int64_t)d.n_layers * d.n_kv_heads * E * D &&
+                   d.n_entries * d.n_layers * d.n_kv_heads * E <= INT32_MAX;
+        if (d.dtype != KVR_DTYPE_BF16 || D != 128)
+            return fail(KVR_ERR_UNSUPPORTED, "KVR_PREFILL_SKIP_PREFIX_CACHE needs a bf16 pool with head_dim 128");
     }
     AsmPlan ap;
     QaPlan qp;
@@ -1124,25 +1125,36 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
             return KVR_OK;
         GatherLaunch gl;
         gl.g.pool_v = p->d.v;
-        if ((st = encode_gather_map(*p, p->d.v, &gl.mpv, 1)) != KVR_OK ||
-            (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK)
+        gl.g.ps_entry = p->d.stride[0];
+        gl.g.ps_layer = p->d.stride[1];
+        gl.g.ps_head = p->d.stride[2];
+        gl.g.ps_tok = p->d.stride[3];
+        gl.g.tma_pool = tma_pool ? 1 : 0;
+        if (tma_pool && ((st = encode_gather_map(*p, p->d.v, &gl.mpv, 1)) != KVR_OK ||
+                         (st = encode_gather_map(*p, p->d.v, &gl.mbv, 32)) != KVR_OK))
             return st;
         for (int b = 0; b < batch; ++b) {
             DevReq &r = qp.rq[b];
             r.span0 = ap.span0[b];
             r.span_end = b + 1 < batch ? ap.span0[b + 1] : (int32_t)ap.ds.size();
-            // spans of 96 rows or more on average: the prefix value tiles go
-            // through TMA box loads (runs of 32 pool rows), else through the
-            // attention's gather warps
+            // spans of 96 rows or more on average, all from a pool that TMA can
+            // address as one tensor: the prefix value tiles go through TMA box
+            // loads (runs of 32 pool rows), else through the gather warps
             const int64_t n_sp = r.span_end - r.span0;
-            r.flags = n_sp > 0 && (int64_t)ap.plen[b] >= 96 * n_sp ? kReqValuesTma : 0;
+            bool long_pool_spans = tma_pool && n_sp > 0 && (int64_t)ap.plen[b] >= 96 * n_sp;
+            for (int i = r.span0; long_pool_spans && i < r.span_end; ++i)
+                long_pool_spans = (ap.ds[i].src & KVR_SRC_LOCAL) == 0;
+            r.flags = long_pool_spans ? kReqValuesTma : 0;
         }
+        // the attention reads the local-source table from device memory
+        ap.upload = n_locals > 0;
         if ((stitch && (st = asm_stage(p, ap, s)) != KVR_OK) || (st = qa_stage(p, qp, s)) != KVR_OK)
             return st;
         gl.inl = !stitch || ap.inl;
         if (stitch && ap.inl)
             std::memcpy(gl.st.spans, ap.tab.spans, ap.ds.size() * sizeof(DevSpan));
         gl.g.spans = gl.inl ? nullptr : ap.a.spans;
+        gl.g.locals = gl.inl ? nullptr : ap.a.locals;
         gl.g.n_spans = (int32_t)ap.ds.size();
         gl.g.entry_len = (int32_t)p->d.entry_len;
         if (stitch) {

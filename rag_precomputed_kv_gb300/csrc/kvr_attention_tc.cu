@@ -804,8 +804,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
         if constexpr (kV) {
-            prefetch_tmap(&tmpv);
-            prefetch_tmap(&tmbv);
+            if (g.tma_pool) {
+                prefetch_tmap(&tmpv);
+                prefetch_tmap(&tmbv);
+            }
         }
         if (a.out_tma)
             prefetch_tmap(&tmo);
@@ -1562,16 +1564,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 2i and 2i + 1 (lanes 0-15 and 16-31, one 16-byte chunk each of the
         // two 64-column panels' 8).  A tile's copies are one group; the tile
         // is released to the MMA warp once the next tile's copies are issued
-        // and its own have landed.
+        // and its own have landed, or before waiting for any tile but the
+        // very next one.
         const int rb = 64 * (warp - 10);
         const int q16 = lane & 15, half_sel = lane >> 4;
         const uint32_t chunk_off = (uint32_t)((q16 >> 3) * kPanelBytes);
         const int c8 = q16 & 7;
         const DevSpan *spans = g.spans ? g.spans : st.spans;
-        const int64_t e_rows = (int64_t)a.n_layers * a.n_kv_heads * g.entry_len;   // pool rows per entry
         const __nv_bfloat16 *pv = static_cast<const __nv_bfloat16 *>(g.pool_v);
         const __nv_bfloat16 *cv = static_cast<const __nv_bfloat16 *>(a.cache_v);
-        int tt = 0, gk = 0, nj[2] = {0, 0}, prev_b = -1;
+        int tt = 0, gk = 0, nj[2] = {0, 0}, prev_b = -1, prev_j = -1;
         bool ok = true;
         // release the tile whose copies were issued last (all of this thread's
         // copies land first, then the async proxy sees them)
@@ -1589,7 +1591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prev_b = -1;
         };
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++gk) {
-            int jb, je, prefix, n_valid, cap, lh, s0, s_end;
+            int jb, je, prefix, n_valid, cap, l, h, s0, s_end;
             bool tma_v;
             int64_t kv_row0;
             {
@@ -1604,13 +1606,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 n_valid = gp->n_valid;
                 cap = gp->cap;
                 kv_row0 = gp->kv_row0;
-                lh = gp->l * a.n_kv_heads + gp->h;
+                l = gp->l;
+                h = gp->h;
                 s0 = gp->span0;
                 s_end = gp->span_end;
                 tma_v = gp->tma_v != 0;
                 geo_done(gk);
             }
-            const int64_t lh_row = (int64_t)lh * g.entry_len;   // (layer, kv-head) block inside an entry
             // this lane's span cursor: the span holding its first prefix row of
             // the item (a request's spans are in stitched-row order)
             int cur = s0;
@@ -1641,12 +1643,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         while (cur + 1 < s_end && spans[cur].row + spans[cur].len <= r)
                             ++cur;
                         const DevSpan &sp = spans[cur];
-                        src[k] = pv + ((int64_t)sp.src * e_rows + lh_row + sp.start + (r - sp.row)) * kD;
+                        const int64_t tok = sp.start + (r - sp.row);
+                        if (sp.src & KVR_SRC_LOCAL) {   // a request-local source
+                            const DevLocal &lc = g.locals[sp.src & ~KVR_SRC_LOCAL];
+                            src[k] = static_cast<const __nv_bfloat16 *>(lc.v) + l * lc.s_layer + h * lc.s_head +
+                                     tok * lc.s_tok;
+                        } else {
+                            src[k] = pv + sp.src * g.ps_entry + l * g.ps_layer + h * g.ps_head + tok * g.ps_tok;
+                        }
                     } else if (r < n_valid) {
                         src[k] = cv + (kv_row0 + r) * kD;
                     }
                 }
                 const int sv = (tt + 1) % kSlots, b = sv >> 1;
+                // a tile held back that is not the one just before this: the MMAs
+                // reach this tile's slot only after consuming it (and the tiles
+                // the producer loads in between), so release it first
+                if (prev_b >= 0 && j != prev_j + 1)
+                    release(1);
                 if (!mbar_wait(bar(kBarGatherJob + b), nj[b] & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -1665,6 +1679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("cp.async.commit_group;" ::: "memory");
                 release(0);
                 prev_b = b;
+                prev_j = j;
             }
             release(1);
         }

@@ -147,8 +147,8 @@ struct alignas(16) DevReq {
 };
 static_assert(sizeof(DevReq) == 48, "request table layout");
 // DevReq::flags: the values-gathering attention loads this request's prefix
-// value tiles through TMA box loads (its spans are long) rather than with the
-// gather warps' copies
+// value tiles through TMA box loads (its spans are long and all from a
+// contiguous pool) rather than with the gather warps' copies
 constexpr int32_t kReqValuesTma = 1;
 
 // Device error word codes (first error wins).  kDevBadInput: an attention
@@ -264,9 +264,12 @@ struct SpanTable {
 };
 struct GatherArgs {
     const DevSpan *spans;       // the batch's spans in global memory, or NULL: the SpanTable parameter
+    const DevLocal *locals;     // the batch's request-local sources in global memory (calls with any)
     int32_t n_spans;            // non-empty spans of the batch (request b's start at DevReq::span0)
     int32_t entry_len;          // pool tokens per entry
-    const void *pool_v;         // the pool's values: [entries * L * H_kv * entry_len, D] bf16
+    const void *pool_v;         // the pool's values (bf16)
+    int64_t ps_entry, ps_layer, ps_head, ps_tok;   // their strides, in elements
+    int32_t tma_pool;           // the TMA maps of the pool's values are set (a contiguous pool)
 };
 
 struct TcAttnArgs {

@@ -21,8 +21,10 @@ pytestmark = pytest.mark.gpu
 EDGE = W.Config("edge", 2, 8, 2, 128, "bf16", 1e4, 4, 96, 5, 7, 1, 77, "random")
 
 
-def _custom(cfg, span_lists):
-    reqs = [W.Request(np.asarray(rows, np.int32).reshape(-1, 3), 0) for rows in span_lists]
+def _custom(cfg, span_lists, local_lens=None):
+    local_lens = local_lens or {}
+    reqs = [W.Request(np.asarray(rows, np.int32).reshape(-1, 3), local_lens.get(b, 0))
+            for b, rows in enumerate(span_lists)]
     return dataclasses.replace(cfg, batch=len(reqs)), reqs
 
 
@@ -58,6 +60,17 @@ def _case(name):
                              [[pid, 0, 5], [1, 0, 96], [2, 0, 96], [3, 0, 96]], [[2, 0, 96], [3, 0, 96]],
                              [[1, 50, 96], [0, 0, 96]]])
         return cfg, reqs, {"spare_rows": 3}
+    if name == "local_sources":
+        # request-local sources (inline tokens) between pool spans
+        F = W.LOCAL_FLAG
+        cfg, reqs = _custom(dataclasses.replace(EDGE, prompt_len=0, query_len=13),
+                            [[[0, 0, 96], [F | 0, 0, 8], [1, 0, 96], [2, 0, 96]],
+                             [[3, 10, 40], [F | 1, 0, 8], [0, 5, 20]]], local_lens={0: 8, 1: 8})
+        return cfg, reqs, {}
+    if name == "docs_inline":
+        # per-document caches with inline tokens between them (Llama-3.1-8B
+        # shape, 16 documents, 2 layers)
+        return dataclasses.replace(W.CONFIGS[4], batch=1, n_layers=2, n_chunks=16), None, {"sample_units": 4}
     if name == "many_requests":
         base = dataclasses.replace(EDGE, prompt_len=0, query_len=3)
         rng = np.random.default_rng(3)
@@ -68,13 +81,38 @@ def _case(name):
     raise ValueError(name)
 
 
+def _strided(case):
+    """The same pool seen through views whose token axis has 8 rows of
+    padding after each (entry, layer, kv-head) block: strides no longer those
+    of a contiguous pool."""
+    import torch
+    from rag_precomputed_kv_gb300 import kvr
+
+    def pad(x):
+        E, L, H, T, D = x.shape
+        big = torch.full((E, L, H, T + 8, D), float("nan"), dtype=x.dtype, device=x.device)
+        big[:, :, :, :T] = x
+        return big[:, :, :, :T]
+
+    case.t.pool_k, case.t.pool_v = pad(case.t.pool_k), pad(case.t.pool_v)
+    assert not case.t.pool_v.is_contiguous()
+    case.pool.close()
+    case.pool = kvr.Pool(case.t.pool_k, case.t.pool_v, case.cfg.n_q_heads, case.cfg.rope_theta)
+    return case
+
+
 @pytest.mark.parametrize("name", ["cfg2", "cfg2_composite", "cfg3", "cfg5", "edges", "mixed_long_short",
-                                  "many_requests"])
+                                  "local_sources", "docs_inline", "strided_pool", "many_requests"])
 def test_gathering_prefill_matches_oracle_and_stitched_path(name):
     import torch
-    cfg, reqs, kw = _case(name)
+    if name == "strided_pool":
+        cfg, reqs, kw = _case("mixed_long_short")
+    else:
+        cfg, reqs, kw = _case(name)
     composite = kw.pop("composite", False)
     case = Case(cfg, reqs=reqs, composite=composite, spare_rows=kw.pop("spare_rows", 0))
+    if name == "strided_pool":
+        case = _strided(case)
     res = run_parity_case(cfg=cfg, case=case, prefill=True, skip_prefix=True, composite=composite, **kw)
     assert res["ok"], res
     got = [case.out.clone(), case.pos_ids.clone(), case.src_map.clone()]
@@ -108,15 +146,12 @@ def test_gathering_prefill_is_deterministic():
 
 
 def test_gathering_prefill_refuses_what_it_cannot_gather():
-    """fp32 pools and request-local sources take the stitched path only."""
+    """fp32 pools take the stitched path only."""
     from rag_precomputed_kv_gb300 import kvr
-    F = W.LOCAL_FLAG
-    reqs = [W.Request(np.asarray([[0, 0, 96], [F | 0, 0, 8]], np.int32), 8)]
-    for cfg, rq in ((W.CONFIGS[1], None), (dataclasses.replace(EDGE, prompt_len=0, batch=1), reqs)):
-        case = Case(cfg, reqs=rq)
-        with pytest.raises(kvr.KvrError) as e:
-            case.run(prefill=True, skip_prefix=True)
-        assert e.value.status == 3, cfg.name
+    case = Case(W.CONFIGS[1])
+    with pytest.raises(kvr.KvrError) as e:
+        case.run(prefill=True, skip_prefix=True)
+    assert e.value.status == 3
 
 
 def test_gathering_prefill_with_pool_keys_kept_before_rope():
