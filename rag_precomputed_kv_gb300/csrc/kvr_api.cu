@@ -1154,7 +1154,9 @@ extern "C" kvr_status kvr_prefill(kvr_pool_t p, int32_t batch, const int32_t *sp
         if (stitch && ap.inl)
             std::memcpy(gl.st.spans, ap.tab.spans, ap.ds.size() * sizeof(DevSpan));
         gl.g.spans = gl.inl ? nullptr : ap.a.spans;
-        gl.g.locals = gl.inl ? nullptr : ap.a.locals;
+        // (NULL when no span names a request-local source: the attention then
+        // runs its pool-only variant)
+        gl.g.locals = n_locals > 0 && !gl.inl ? ap.a.locals : nullptr;
         gl.g.n_spans = (int32_t)ap.ds.size();
         gl.g.entry_len = (int32_t)p->d.entry_len;
         if (stitch) {

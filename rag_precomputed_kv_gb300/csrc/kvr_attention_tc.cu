@@ -703,11 +703,13 @@ __device__ __forceinline__ void geo_of(const Item &t, Geo &o)
     o.kv_row0 = t.w.kv_row0;
 }
 // the kernel's variants: K and V from the stitched cache; or K from the cache
-// and the prefix values gathered from the pool
-constexpr int kModeStitched = 0, kModeGatherV = 1;
-// softmax 8, MMA 1, and the two gather warps (values-gathering variant)
+// and the prefix values gathered from the pool; or the same for calls whose
+// spans may also name request-local sources (the gather warps' row lookup
+// then has a second kind of source)
+constexpr int kModeStitched = 0, kModeGatherV = 1, kModeGatherVLocal = 2;
+// softmax 8, MMA 1, and the two gather warps (values-gathering variants)
 template <int kM>
-constexpr uint32_t geo_consumer_warps() { return kM == kModeGatherV ? 11u : 9u; }
+constexpr uint32_t geo_consumer_warps() { return kM != kModeStitched ? 11u : 9u; }
 
 // The value tile j of a values-gathering item that the gather warps fill: a
 // tile that reaches past the cache block (into rows this variant does not
@@ -748,7 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ GatherArgs g, const __grid_constant__ SpanTable st,
                    const __grid_constant__ CUtensorMap tmo)
 {
-    constexpr bool kV = kM == kModeGatherV;
+    constexpr bool kV = kM != kModeStitched;
+    constexpr bool kLocals = kM == kModeGatherVLocal;
     const DevReq *reqs = a.reqs ? a.reqs : rt.reqs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1644,7 +1647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ++cur;
                         const DevSpan &sp = spans[cur];
                         const int64_t tok = sp.start + (r - sp.row);
-                        if (sp.src & KVR_SRC_LOCAL) {   // a request-local source
+                        if (kLocals && (sp.src & KVR_SRC_LOCAL)) {   // a request-local source
                             const DevLocal &lc = g.locals[sp.src & ~KVR_SRC_LOCAL];
                             src[k] = static_cast<const __nv_bfloat16 *>(lc.v) + l * lc.s_layer + h * lc.s_head +
                                      tok * lc.s_tok;
@@ -1768,7 +1771,7 @@ bool attention_tc_pairs_fit(int n_sms) { return pairs_fit<kModeStitched>(n_sms);
 template <int kM>
 static cudaError_t launch_variant(const TcAttnArgs &ta, int grid, bool pdl, bool pairs, cudaStream_t s)
 {
-    constexpr bool kV = kM == kModeGatherV;
+    constexpr bool kV = kM != kModeStitched;
     cudaError_t e = set_smem_attr<kM>();
     if (e != cudaSuccess)
         return e;
@@ -1820,8 +1823,10 @@ cudaError_t launch_attention_tc(const TcAttnArgs &ta, bool pdl, cudaStream_t s)
     // CTAs 2i and 2i + 1 of the last round when n_full is a multiple of the grid
     if (pairs && ((grid & 1) || ta.base.n_full % grid != 0))
         return cudaErrorInvalidValue;
-    return ta.gather_v ? launch_variant<kModeGatherV>(ta, grid, pdl, pairs, s)
-                       : launch_variant<kModeStitched>(ta, grid, pdl, pairs, s);
+    if (!ta.gather_v)
+        return launch_variant<kModeStitched>(ta, grid, pdl, pairs, s);
+    return ta.g.locals ? launch_variant<kModeGatherVLocal>(ta, grid, pdl, pairs, s)
+                       : launch_variant<kModeGatherV>(ta, grid, pdl, pairs, s);
 }
 
 }  // namespace kvr

@@ -264,7 +264,7 @@ struct SpanTable {
 };
 struct GatherArgs {
     const DevSpan *spans;       // the batch's spans in global memory, or NULL: the SpanTable parameter
-    const DevLocal *locals;     // the batch's request-local sources in global memory (calls with any)
+    const DevLocal *locals;     // the batch's request-local sources in global memory; NULL in calls with none
     int32_t n_spans;            // non-empty spans of the batch (request b's start at DevReq::span0)
     int32_t entry_len;          // pool tokens per entry
     const void *pool_v;         // the pool's values (bf16)
