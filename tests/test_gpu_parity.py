@@ -354,10 +354,13 @@ def test_bounded_wait_timeout_is_reported_and_the_pool_stays_usable():
 def test_query_side_buffers_in_pinned_host_memory():
     """q, kq, vq and out in pinned host memory (read and written by the
     kernels through their unified addresses): the same bits as with device
-    buffers, on the tensor-core, decode and CUDA-core paths."""
+    buffers, on the tensor-core (G = 2 and 4, one and several query tiles),
+    decode and CUDA-core paths."""
     import torch
     for cfg, reqs in (_custom(dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=13),
                               [[[0, 3, 90], [2, 0, 96]], [[1, 7, 60]]]),
+                      _custom(dataclasses.replace(EDGE_BASE, n_q_heads=8, n_kv_heads=2, query_len=70),
+                              [[[0, 3, 90], [2, 0, 96], [1, 0, 96]], [[1, 7, 60]], []]),
                       _custom(dataclasses.replace(EDGE_BASE, n_q_heads=4, n_kv_heads=2, query_len=1),
                               [[[0, 3, 90]], [[1, 7, 60], [3, 0, 96]]]),
                       (W.CONFIGS[1], None)):
