@@ -556,11 +556,12 @@ def run_kvr(args):
     # work then runs in `e2e_chunks` consecutive groups, one kvr_query_attention
     # call each (as a server would split a large batch): each group's Q, K_q and
     # V_q go up on a copy stream (the copies start under the stitch, and a
-    # group's copy overlaps the previous group's attention), and each call
-    # writes its output straight into pinned host memory (the epilogues store
-    # over the CPU-GPU link while the copies use the other direction).  Every
-    # transfer of the step is inside its timed region (the copy stream starts
-    # after the step's start event).
+    # group's copy overlaps the previous group's attention).  Each call's
+    # output is written by the attention kernel straight into pinned host
+    # memory (`--e2e-out host`, the default), or goes to device memory and down
+    # on a second copy stream (`--e2e-out device`: slower, the two copy engines
+    # share the link).  Every transfer of the step is inside its timed region
+    # (the copy streams start after the step's start event).
     B_all = len(wl.reqs)
     n_ch = max(1, min(args.e2e_chunks, B_all))
     groups = [g for g in np.array_split(np.arange(B_all), n_ch) if len(g)]
@@ -579,13 +580,18 @@ def run_kvr(args):
         ch["q_d"], ch["kq_d"], ch["vq_d"] = (torch.empty(ch[k].shape, dtype=ch[k].dtype, device=dev)
                                              for k in ("q_h", "kq_h", "vq_h"))
         ch["out_h"] = torch.empty(ch["q_h"].shape, dtype=wl.out.dtype, pin_memory=True)
+        if args.e2e_out == "device":
+            ch["out_d"] = torch.empty(ch["q_h"].shape, dtype=wl.out.dtype, device=dev)
+            ch["done"] = torch.cuda.Event()
         chunks.append(ch)
     h2d = sum(ch[k].numel() * ch[k].element_size() for ch in chunks for k in ("q_h", "kq_h", "vq_h"))
     d2h = sum(ch["out_h"].numel() * ch["out_h"].element_size() for ch in chunks)
     copy_s = torch.cuda.Stream()
+    down_s = torch.cuda.Stream()
 
     def e2e_step():
         copy_s.wait_stream(stream)
+        down_s.wait_stream(stream)
         with torch.cuda.stream(copy_s):
             for ch in chunks:
                 for k in ("q", "kq", "vq"):
@@ -596,8 +602,14 @@ def run_kvr(args):
         for ch in chunks:
             stream.wait_event(ch["ev"])
             wl.pool.query_attention(ch["co"], plen[ch["b0"]:ch["b1"]], ch["qo"], ch["q_d"], ch["kq_d"],
-                                    ch["vq_d"], wl.cache_k, wl.cache_v, ch["out_h"])
+                                    ch["vq_d"], wl.cache_k, wl.cache_v, ch.get("out_d", ch["out_h"]))
+            if "out_d" in ch:
+                ch["done"].record(stream)
+                down_s.wait_event(ch["done"])
+                with torch.cuda.stream(down_s):
+                    ch["out_h"].copy_(ch["out_d"], non_blocking=True)
         stream.wait_stream(copy_s)
+        stream.wait_stream(down_s)
 
     for _ in range(args.warmup):
         flush()
@@ -665,10 +677,13 @@ def run_kvr(args):
                     "what": "one kvr_prefill call (stitch + query attention) per batch, device time"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3 / args.steps, 5), "query_groups": len(chunks),
+                "out": args.e2e_out,
                 "what": "kvr_assemble for the batch, then one kvr_query_attention per group of requests; each "
                         "group's Q, K_q, V_q up from pinned host memory on a copy stream (under the stitch and the "
-                        "previous group's attention), O written by the attention kernel into pinned host memory; "
-                        "per-step events"},
+                        "previous group's attention); " + (
+                            "each group's O into device memory, then down into pinned host memory on a second "
+                            "copy stream (under the next group's work)" if args.e2e_out == "device" else
+                            "O written by the attention kernel into pinned host memory") + "; per-step events"},
         "gpu_launches": 3 * args.steps,
         "skip_prefix_cache": gather,
         "decode": decode,
@@ -874,6 +889,9 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=5, choices=sorted(W.CONFIGS))
+    ap.add_argument("--e2e-out", default="host", choices=["device", "host"],
+                    help="end-to-end step: output to device memory and copied down (device) or written "
+                         "into pinned host memory by the attention kernel (host)")
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="request groups of the end-to-end leg (one kvr_query_attention call each)")
     ap.add_argument("--latency-reps", type=int, default=LATENCY_REPS,
