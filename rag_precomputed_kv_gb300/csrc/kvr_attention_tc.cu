@@ -1049,10 +1049,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(o_tm + 64 * hh, f);
                 tmem_ld32(o_tm + 64 * hh + 32, f + 32);
                 tmem_wait_ld();
-                if (hh == 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar(kBarOEmpty + x));   // O_x may now take the next unit's PV
-                }
                 if (a.out_tma) {   // the staging is free once the last TMA store has read it
                     if (lane == 0)
                         bulk_wait_read();
@@ -1106,6 +1102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                 }
             }
+            // the output is staged and stored: O_x and the shared memory may
+            // take the next item's MMAs
+            tc_fence_before();
+            mbar_arrive(bar(kBarOEmpty + x));
         }
         if (a.out_tma && lane == 0)
             bulk_wait_all();   // every output store has landed before the CTA ends
@@ -1480,9 +1480,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ++nq;
-                for (int x = 0; x < 2; ++x)
-                    if (jb < jx[x])
+                // a tile's first S of the item waits until the epilogue of its
+                // previous item is done (O read, staged and stored): this MMA
+                // reads both operands from shared memory, at the bandwidth the
+                // epilogue's staging stores also need; its PV MMAs, which
+                // overwrite O, come later still
+                for (int x = 0; x < 2 && ok; ++x)
+                    if (jb < jx[x]) {
+                        if (o_used[x]) {
+                            if (!mbar_wait(bar(kBarOEmpty + x), oe_cnt[x] & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            ++oe_cnt[x];
+                            o_used[x] = false;
+                        }
                         issue_s(x, tt % kSlots);
+                    }
+                if (!ok)
+                    break;
                 if (je - jb == 1)
                     umma_commit(lead, bar(kBarQEmpty));
                 umma_commit(lead, bar(kBarEmpty + tt % kSlots));
@@ -1502,13 +1518,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!v_ready && !(v_ready = wait_v(tv, j))) {
                             ok = false;
                             break;
-                        }
-                        if (j == jb && o_used[x]) {   // O_x still holds the last item until read
-                            if (!mbar_wait(bar(kBarOEmpty + x), oe_cnt[x] & 1, abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            ++oe_cnt[x];
                         }
                         tc_fence_after();
                         const uint32_t d = tmem + col_o(x), pa = tmem + col_s(x);
