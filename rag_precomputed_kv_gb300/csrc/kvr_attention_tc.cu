@@ -6,12 +6,13 @@
 // "Attention Mask"; SemPIC page, causal interleave): query token t of request
 // b sits at position P_b + t and attends to the P_b stitched prefix rows and
 // to query rows 0..t of its (layer, kv-head) block of the cache (the query
-// rows were appended, rotated, by the assemble kernel just before).
+// rows were appended, rotated, by the query prologue just before).
 //
 // Tiling.  A work unit is one (request, 256-row query block, layer, kv-head),
 // split into two 128-row tiles A and B; the kernel is persistent (one CTA per
-// SM walks the units), so the next unit's Q load and first S MMAs overlap the
-// current unit's last softmax and its epilogue.  The G = H_q / H_kv query heads that
+// SM walks the units), so the next unit's Q and K/V loads overlap the current
+// unit's last softmax and its epilogue; a tile's first S MMA of the next unit
+// follows that tile's epilogue.  The G = H_q / H_kv query heads that
 // share a kv head are packed into the rows (row r = t * G + g), so each K/V
 // tile is read once for all of them, and once for both tiles.  Per 128-key
 // tile j and tile X in {A, B}:
@@ -36,23 +37,27 @@
 // one lane (elected once) issuing the tcgen05 instructions: with the
 // schedule's descriptor arithmetic warp-uniform, one MMA issues about as fast
 // as the tensor core retires it (issued from a single-lane branch it was the
-// bottleneck); warps 10-11 only complete the third warpgroup, so that the
+// bottleneck); warps 10-11 complete the third warpgroup, so that the
 // registers can be split by warpgroup (setmaxnreg): the softmax warpgroups
-// hold a whole row of S and run without spills.  Barrier phases run on
-// across units.
+// hold a whole row of S and run without spills (in the values-gathering
+// variant they are the gather warps).  Barrier phases run on across units.
 //
 // Epilogue: each softmax thread holds one output row; its warp stages 32 rows
-// x 64 columns at a time in shared memory and writes them back as whole
-// 128-byte lines (row-per-thread stores touch one line per lane).
+// x 64 columns at a time in shared memory and writes them back with one TMA
+// tensor store (32 / G whole tokens, G a power of two) or as whole 128-byte
+// lines (row-per-thread stores touch one line per lane); then it releases O_x
+// (and, through the MMA warp's wait, the shared memory the next S MMA reads).
 //
 // Values-gathering variant (a prefill whose stitched prefix is not kept): the
 // keys come from the cache, stitched by a keys-only stitch; each value tile
-// that holds prefix rows is gathered from the pool through the span table
-// (runs of 32 consecutive pool rows as one box load, other rows as gather4),
-// which halves the stitch's traffic.  Warp 10 writes the first query rows
-// (from the cache) into the tile that also holds the last prefix rows, and
-// zeroes the rows past a request's keys where a tile reaches past its cache
-// block, whose value rows this variant does not write.
+// that holds prefix rows is read from the pool through the span table, which
+// halves the stitch's traffic.  For a request of long spans the producer loads
+// those tiles (runs of 32 consecutive pool rows as one box load, other rows as
+// gather4); for one of short spans warps 10-11 copy them with 16-byte
+// cp.async copies.  The gather warps also fill the tile that holds the first
+// query rows (from the cache) and zero the rows past a request's keys where a
+// tile reaches past its cache block, whose value rows this variant does not
+// write.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the CTA
 // records KVR_ERR_TIMEOUT in the pool's error word, all roles leave their
@@ -103,7 +108,7 @@ constexpr int kBarEmpty = kBarFull + kSlots;      // [kSlots] K/V tile consumed
 constexpr int kBarSFull = kBarEmpty + kSlots;     // [2] S_x computed
 constexpr int kBarPFull = kBarSFull + 2;          // [2] P_x written (128 arrivals)
 constexpr int kBarOFull = kBarPFull + 2;          // [2] O_x final for the unit
-constexpr int kBarOEmpty = kBarOFull + 2;         // [2] O_x read by the epilogue (128 arrivals)
+constexpr int kBarOEmpty = kBarOFull + 2;         // [2] O_x out, staged and stored (128 arrivals)
 constexpr int kBarQFull = kBarOEmpty + 2;         // Q tiles landed
 constexpr int kBarQEmpty = kBarQFull + 1;         // all S of the unit done with Q
 constexpr int kBarDrain = kBarQEmpty + 1;
