@@ -1377,9 +1377,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tt = __shfl_sync(0xffffffffu, tt, 0);
                 nq = __shfl_sync(0xffffffffu, nq, 0);
                 // the next item's geometry, published for the other roles; its Q
-                // brought into L2 ahead of its load (the K/V tiles are not: their
-                // loads are issued a tile ahead anyway, and a prefetch costs the
-                // SM's TMA unit as much time as the load that follows it)
+                // and its first K and V tiles brought into L2 ahead of their loads
+                // (the whole grid reaches its item boundaries at about the same
+                // time, and those loads would queue together; the other K/V tiles
+                // are not prefetched: their loads are issued a tile ahead anyway,
+                // and a prefetch costs the SM's TMA unit as much time as the load
+                // that follows it)
                 if (ok && more) {
                     if (gk == 0)
                         nxt = item_at(a, reqs, n_blocks, it + gridDim.x, &rr, lane);
@@ -1390,6 +1393,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_prefetch_2d(&tmq, 0, nxt.w.q_row0 + x * kTileM);
                                 tma_prefetch_2d(&tmq, 64, nxt.w.q_row0 + x * kTileM);
                             }
+                        if (ok && nxt.je > nxt.jb) {
+                            const int krow = (int)(nxt.w.kv_row0 + (int64_t)nxt.jb * kTileN);
+                            tma_prefetch_2d(&tmk, 0, krow);
+                            tma_prefetch_2d(&tmk, 64, krow);
+                            tma_prefetch_2d(&tmv, 0, krow);
+                            tma_prefetch_2d(&tmv, 64, krow);
+                        }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                 }
